@@ -1,0 +1,301 @@
+/*
+ * gattn_oracle.c -- plain fp64 CPU oracle for fused CSR graph attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file: only the test-suite, the smoke check and the CPU-baseline
+ * leg of the benchmark use it.  It shares no code, header or constant with
+ * the CUDA library; the two meet only in the seeded input generators.
+ *
+ * What it computes (source: "On Efficient Scaling of GNNs via IO-Aware
+ * Layers Implementations", zh and ko technical summaries, section
+ * "Methodology", attention-based layers):
+ *   the attention layer scores every in-neighbour j of a destination i,
+ *   normalises the scores with a softmax over the neighbourhood and sums the
+ *   neighbours' values with those weights.  The fused method streams this
+ *   with an online softmax and keeps a per-node log-sum-exp for the backward;
+ *   its result equals the plain definition below up to rounding order, so
+ *   the oracle is that definition written out: it MATERIALISES the O(M*H)
+ *   edge logits and probabilities that the fused kernels avoid.
+ *
+ * Score functions (the two layer types the pages name, Graph Transformer
+ * and GATv2; formulas as fixed by the build contract because the pages
+ * print none):
+ *   dot   : s_ijh = scale * sum_d q_ihd k_jhd            (scale = 1/sqrt(D))
+ *   GATv2 : s_ijh = sum_d a_hd * LeakyReLU(q_ihd + k_jhd) (q = xl, k = xr)
+ * with LeakyReLU(z) = z for z > 0, slope*z otherwise, and its derivative
+ * 1 for z > 0, slope otherwise.
+ *
+ * Readings where the pages are silent (listed in the design notes too):
+ *   - a node with no in-edges gets out = 0 and lse = -inf;
+ *   - i is the destination (row of the CSR), j the source (column);
+ *   - no bias, no head concat/mean: outputs are per head [rows, H, D].
+ *
+ * Layouts: every dense tensor is row-major [nodes, H, D] fp64.  The graph is
+ * given as a list of destination rows: row r is node row_ids[r] (or r when
+ * row_ids is NULL), its in-edges are col[row_ptr[r] .. row_ptr[r+1]).  A
+ * subset of rows is allowed: forward rows are independent, so the oracle
+ * on a subset of rows gives the exact values of those rows.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_DOT 0
+#define ORC_GATV2 1
+
+static double leaky(double z, double slope) { return z > 0.0 ? z : slope * z; }
+static double leaky_grad(double z, double slope) { return z > 0.0 ? 1.0 : slope; }
+
+/* One edge, one head: the score s_ijh. q and k point at the head's D values. */
+static double edge_score(int kind, int D, double scale, const double* a_h, double slope,
+                         const double* q, const double* k) {
+  double s = 0.0;
+  if (kind == ORC_DOT) {
+    for (int d = 0; d < D; ++d) s += q[d] * k[d];
+    return scale * s;
+  }
+  for (int d = 0; d < D; ++d) s += a_h[d] * leaky(q[d] + k[d], slope);
+  return s;
+}
+
+static int64_t node_of(const int32_t* row_ids, int64_t r) { return row_ids ? (int64_t)row_ids[r] : r; }
+
+/*
+ * Materialise the edge logits e[nnz, H] and the softmax probabilities
+ * p[nnz, H]; write lse[n_rows, H].  Returns 0, or -1 on allocation failure.
+ */
+static int logits_and_probs(int64_t n_rows, const int32_t* row_ids, const int64_t* row_ptr,
+                            const int32_t* col, int H, int D, int kind, double scale,
+                            const double* a, double slope, const double* Q, const double* K,
+                            double* p, double* lse) {
+  const int64_t HD = (int64_t)H * D;
+  for (int64_t r = 0; r < n_rows; ++r) {
+    const int64_t i = node_of(row_ids, r);
+    const int64_t e0 = row_ptr[r], e1 = row_ptr[r + 1];
+    for (int h = 0; h < H; ++h) {
+      const double* q = Q + i * HD + (int64_t)h * D;
+      const double* a_h = a ? a + (int64_t)h * D : NULL;
+      /* logits */
+      for (int64_t e = e0; e < e1; ++e) {
+        const double* k = K + (int64_t)col[e] * HD + (int64_t)h * D;
+        p[e * H + h] = edge_score(kind, D, scale, a_h, slope, q, k);
+      }
+      if (e1 == e0) { /* isolated destination: reading, lse = -inf */
+        lse[r * H + h] = -INFINITY;
+        continue;
+      }
+      /* softmax over the neighbourhood */
+      double m = -INFINITY;
+      for (int64_t e = e0; e < e1; ++e) m = fmax(m, p[e * H + h]);
+      double z = 0.0;
+      for (int64_t e = e0; e < e1; ++e) z += exp(p[e * H + h] - m);
+      for (int64_t e = e0; e < e1; ++e) p[e * H + h] = exp(p[e * H + h] - m) / z;
+      lse[r * H + h] = m + log(z);
+    }
+  }
+  return 0;
+}
+
+/*
+ * Forward: out[r] = sum_j p_ij v_j per head, lse[r] = log sum_j exp(s_ij).
+ * out is [n_rows, H, D] indexed by row position r; lse is [n_rows, H].
+ */
+int oracle_forward(int64_t n_rows, const int32_t* row_ids, const int64_t* row_ptr,
+                   const int32_t* col, int H, int D, int kind, double scale, const double* a,
+                   double slope, const double* Q, const double* K, const double* V, double* out,
+                   double* lse) {
+  const int64_t HD = (int64_t)H * D;
+  const int64_t nnz = row_ptr[n_rows];
+  double* p = (double*)malloc((size_t)(nnz > 0 ? nnz : 1) * (size_t)H * sizeof(double));
+  if (!p) return -1;
+  logits_and_probs(n_rows, row_ids, row_ptr, col, H, D, kind, scale, a, slope, Q, K, p, lse);
+  for (int64_t r = 0; r < n_rows; ++r) {
+    double* o = out + r * HD;
+    memset(o, 0, (size_t)HD * sizeof(double));
+    for (int64_t e = row_ptr[r]; e < row_ptr[r + 1]; ++e) {
+      const double* v = V + (int64_t)col[e] * HD;
+      for (int h = 0; h < H; ++h) {
+        const double w = p[e * H + h];
+        for (int d = 0; d < D; ++d) o[h * D + d] += w * v[h * D + d];
+      }
+    }
+  }
+  free(p);
+  return 0;
+}
+
+/*
+ * Analytic backward of L = sum out * dO (dO given per row position r).
+ *   dp_ij = dO_i . v_j                         (per head)
+ *   ds_ij = p_ij (dp_ij - sum_k p_ik dp_ik)    (softmax Jacobian)
+ *   dQ_i += ds_ij * ds/dq_i,  dK_j += ds_ij * ds/dk_j,  dV_j += p_ij dO_i,
+ *   da   += ds_ij * ds/da     (GATv2 only)
+ * dQ is [n_rows, H, D] by row position; dK, dV are [N, H, D] by node id and
+ * are overwritten (zeroed here first); da is [H, D] (may be NULL for dot).
+ * The scatter into dK/dV runs serially in edge order.
+ */
+int oracle_backward(int64_t n_rows, const int32_t* row_ids, const int64_t* row_ptr,
+                    const int32_t* col, int64_t N, int H, int D, int kind, double scale,
+                    const double* a, double slope, const double* Q, const double* K,
+                    const double* V, const double* dO, double* dQ, double* dK, double* dV,
+                    double* da) {
+  const int64_t HD = (int64_t)H * D;
+  const int64_t nnz = row_ptr[n_rows];
+  const size_t eh = (size_t)(nnz > 0 ? nnz : 1) * (size_t)H;
+  double* p = (double*)malloc(eh * sizeof(double));
+  double* ds = (double*)malloc(eh * sizeof(double));
+  double* lse = (double*)malloc((size_t)(n_rows > 0 ? n_rows : 1) * (size_t)H * sizeof(double));
+  if (!p || !ds || !lse) { free(p); free(ds); free(lse); return -1; }
+  logits_and_probs(n_rows, row_ids, row_ptr, col, H, D, kind, scale, a, slope, Q, K, p, lse);
+
+  memset(dQ, 0, (size_t)n_rows * (size_t)HD * sizeof(double));
+  memset(dK, 0, (size_t)N * (size_t)HD * sizeof(double));
+  memset(dV, 0, (size_t)N * (size_t)HD * sizeof(double));
+  if (da) memset(da, 0, (size_t)HD * sizeof(double));
+
+  /* ds = p * (dp - sum_k p dp) */
+  for (int64_t r = 0; r < n_rows; ++r) {
+    const double* g = dO + r * HD;
+    for (int h = 0; h < H; ++h) {
+      double delta = 0.0;
+      for (int64_t e = row_ptr[r]; e < row_ptr[r + 1]; ++e) {
+        const double* v = V + (int64_t)col[e] * HD + (int64_t)h * D;
+        double dp = 0.0;
+        for (int d = 0; d < D; ++d) dp += g[h * D + d] * v[d];
+        ds[e * H + h] = dp; /* dp for now */
+        delta += p[e * H + h] * dp;
+      }
+      for (int64_t e = row_ptr[r]; e < row_ptr[r + 1]; ++e)
+        ds[e * H + h] = p[e * H + h] * (ds[e * H + h] - delta);
+    }
+  }
+
+  /* chain rule through the score, edge by edge */
+  for (int64_t r = 0; r < n_rows; ++r) {
+    const int64_t i = node_of(row_ids, r);
+    const double* g = dO + r * HD;
+    for (int64_t e = row_ptr[r]; e < row_ptr[r + 1]; ++e) {
+      const int64_t j = col[e];
+      for (int h = 0; h < H; ++h) {
+        const double w = ds[e * H + h];
+        const double pe = p[e * H + h];
+        const double* q = Q + i * HD + (int64_t)h * D;
+        const double* k = K + j * HD + (int64_t)h * D;
+        double* dq = dQ + r * HD + (int64_t)h * D;
+        double* dk = dK + j * HD + (int64_t)h * D;
+        double* dv = dV + j * HD + (int64_t)h * D;
+        for (int d = 0; d < D; ++d) dv[d] += pe * g[h * D + d];
+        if (kind == ORC_DOT) {
+          for (int d = 0; d < D; ++d) {
+            dq[d] += w * scale * k[d];
+            dk[d] += w * scale * q[d];
+          }
+        } else {
+          const double* a_h = a + (int64_t)h * D;
+          for (int d = 0; d < D; ++d) {
+            const double z = q[d] + k[d];
+            const double gz = w * a_h[d] * leaky_grad(z, slope);
+            dq[d] += gz;
+            dk[d] += gz;
+            if (da) da[h * D + d] += w * leaky(z, slope);
+          }
+        }
+      }
+    }
+  }
+  free(p);
+  free(ds);
+  free(lse);
+  return 0;
+}
+
+/*
+ * Plan oracle: the per-graph metadata of the degree-aware partition
+ * (source: same pages, "Methodology", reduction-based layers: nodes split
+ * by a degree threshold into light and heavy sets, heavy nodes tiled over
+ * edge chunks; SpMM layers: the transposed adjacency cached for backward).
+ * Definition, written as straightforward loops:
+ *   deg[i]      = indptr[i+1] - indptr[i]
+ *   hist[b]     = #{i : bin(deg[i]) = b}, bin(0) = 0, bin(d) = 1 + floor(log2 d)
+ *   light       = ascending i with deg[i] <= T
+ *   chunks      = for ascending i with deg[i] > T, k = 0, 1, ...:
+ *                 (i, indptr[i] + kC, min(indptr[i] + (k+1)C, indptr[i+1]))
+ *   CSC         = the edges stably counting-sorted by source over CSR edge
+ *                 order: indptrT[N+1], csc_dst[M] (destination), csc_eid[M]
+ *                 (CSR edge id); within a column ascending edge id
+ *   outdeg, hist_out, light_src, src_chunks: the same on the CSC
+ * Buffers are caller-allocated: light/light_src hold N entries, chunk
+ * arrays hold cap_chunks triples.  counts[0..3] receive #light, #chunks,
+ * #light_src, #src_chunks.  Returns 0, -1 if a chunk array is too small,
+ * -2 on allocation failure.
+ */
+static int bin_of(int64_t d) {
+  if (d <= 0) return 0;
+  int b = 1;
+  while (d >= 2) { d >>= 1; ++b; }
+  return b;
+}
+
+static int64_t split(int32_t n, const int64_t* ptr, int32_t T, int32_t C, int32_t* light,
+                     int32_t* chunks, int64_t cap, int64_t* n_light) {
+  int64_t nl = 0, nc = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    const int64_t d = ptr[i + 1] - ptr[i];
+    if (d <= T) { light[nl++] = i; continue; }
+    for (int64_t s = ptr[i]; s < ptr[i + 1]; s += C) {
+      if (nc >= cap) return -1;
+      const int64_t e = s + C < ptr[i + 1] ? s + C : ptr[i + 1];
+      chunks[3 * nc + 0] = i;
+      chunks[3 * nc + 1] = (int32_t)s;
+      chunks[3 * nc + 2] = (int32_t)e;
+      ++nc;
+    }
+  }
+  *n_light = nl;
+  return nc;
+}
+
+int oracle_plan(int32_t N, int64_t M, const int32_t* indptr, const int32_t* indices, int32_t T,
+                int32_t C, int32_t* deg, int32_t* hist, int32_t* light, int32_t* chunks,
+                int64_t cap_chunks, int32_t* indptrT, int32_t* csc_dst, int32_t* csc_eid,
+                int32_t* outdeg, int32_t* hist_out, int32_t* light_src, int32_t* src_chunks,
+                int64_t cap_src_chunks, int64_t* counts) {
+  int64_t* ptr = (int64_t*)malloc(((size_t)N + 1) * sizeof(int64_t));
+  int64_t* ptrT = (int64_t*)malloc(((size_t)N + 1) * sizeof(int64_t));
+  int64_t* fill = (int64_t*)malloc(((size_t)N + 1) * sizeof(int64_t));
+  if (!ptr || !ptrT || !fill) { free(ptr); free(ptrT); free(fill); return -2; }
+  for (int b = 0; b < 33; ++b) hist[b] = hist_out[b] = 0;
+  for (int32_t i = 0; i <= N; ++i) ptr[i] = indptr[i];
+  for (int32_t i = 0; i < N; ++i) {
+    deg[i] = (int32_t)(ptr[i + 1] - ptr[i]);
+    hist[bin_of(deg[i])] += 1;
+  }
+  /* transpose: count, prefix, stable placement in CSR edge order */
+  for (int32_t j = 0; j < N; ++j) outdeg[j] = 0;
+  for (int64_t e = 0; e < M; ++e) outdeg[indices[e]] += 1;
+  ptrT[0] = 0;
+  for (int32_t j = 0; j < N; ++j) ptrT[j + 1] = ptrT[j] + outdeg[j];
+  for (int32_t j = 0; j <= N; ++j) { indptrT[j] = (int32_t)ptrT[j]; fill[j] = ptrT[j]; }
+  for (int32_t i = 0; i < N; ++i)
+    for (int64_t e = ptr[i]; e < ptr[i + 1]; ++e) {
+      const int32_t j = indices[e];
+      csc_dst[fill[j]] = i;
+      csc_eid[fill[j]] = (int32_t)e;
+      fill[j] += 1;
+    }
+  for (int32_t j = 0; j < N; ++j) hist_out[bin_of(outdeg[j])] += 1;
+
+  int64_t nl = 0, nls = 0;
+  const int64_t nc = split(N, ptr, T, C, light, chunks, cap_chunks, &nl);
+  const int64_t ncs = split(N, ptrT, T, C, light_src, src_chunks, cap_src_chunks, &nls);
+  free(ptr);
+  free(ptrT);
+  free(fill);
+  if (nc < 0 || ncs < 0) return -1;
+  counts[0] = nl;
+  counts[1] = nc;
+  counts[2] = nls;
+  counts[3] = ncs;
+  return 0;
+}

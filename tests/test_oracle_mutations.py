@@ -1,0 +1,63 @@
+"""Plant plausible mistakes in copies of the oracle and check the pins catch them.
+
+Each mutant is a text edit of the oracle's C source compiled to a separate
+library; the pin battery (hand-worked examples, dense brute force, finite
+differences, plan recount) must fail for every one of them.
+"""
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+MUTANTS = {
+    "drop_dot_scale": ("return scale * s;", "return s;"),
+    "softmax_jacobian_sign": ("p[e * H + h] * (ds[e * H + h] - delta)",
+                              "p[e * H + h] * (ds[e * H + h] + delta)"),
+    "leaky_grad_no_slope": ("z > 0.0 ? 1.0 : slope;", "z > 0.0 ? 1.0 : 0.0;"),
+    "gather_destination_value": ("const double* v = V + (int64_t)col[e] * HD;",
+                                 "const double* v = V + node_of(row_ids, r) * HD;"),
+    "lse_without_log": ("lse[r * H + h] = m + log(z);", "lse[r * H + h] = m + z;"),
+    "da_without_leaky": ("da[h * D + d] += w * leaky(z, slope);", "da[h * D + d] += w * z;"),
+    "dv_uses_ds": ("dv[d] += pe * g[h * D + d];", "dv[d] += w * g[h * D + d];"),
+    "dk_uses_k": ("dk[d] += w * scale * q[d];", "dk[d] += w * scale * k[d];"),
+    "csc_reverse_rows": ("for (int32_t i = 0; i < N; ++i)\n    for (int64_t e = ptr[i];",
+                         "for (int32_t i = N - 1; i >= 0; --i)\n    for (int64_t e = ptr[i];"),
+    "chunk_off_by_one": ("if (d <= T) { light[nl++] = i; continue; }",
+                         "if (d < T) { light[nl++] = i; continue; }"),
+}
+
+
+def _battery():
+    """Run the pins; return the names of those that fail."""
+    failed = []
+    checks = [
+        ("worked_dot", lambda: pins.test_worked_example("dot_worked_example.json", oracle.DOT)),
+        ("worked_gatv2", lambda: pins.test_worked_example("gatv2_worked_example.json",
+                                                          oracle.GATV2)),
+        ("dense_dot", lambda: pins.test_dense_bruteforce(oracle.DOT, 1, 24, 2, 4)),
+        ("dense_gatv2", lambda: pins.test_dense_bruteforce(oracle.GATV2, 1, 24, 2, 4)),
+        ("fd_dot", lambda: pins.test_finite_differences(oracle.DOT)),
+        ("fd_gatv2", lambda: pins.test_finite_differences(oracle.GATV2)),
+        ("plan", lambda: pins.test_plan_recount(10, 200, 6.0, 8, 4)),
+        ("plan_T", lambda: pins.test_plan_recount(11, 500, 20.0, 32, 16)),
+    ]
+    for name, fn in checks:
+        try:
+            fn()
+        except (AssertionError, ValueError, RuntimeError):
+            failed.append(name)
+    return failed
+
+
+def test_unmutated_oracle_passes_battery():
+    assert _battery() == []
+
+
+@pytest.mark.parametrize("mutant", sorted(MUTANTS))
+def test_mutant_is_caught(mutant):
+    old, new = MUTANTS[mutant]
+    src = oracle.source_text()
+    assert src.count(old) == 1, f"mutation site for {mutant} not unique"
+    with oracle.variant(src.replace(old, new), mutant):
+        failed = _battery()
+    assert failed, f"no pin caught mutant {mutant}"
