@@ -1,0 +1,426 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused CSR graph-attention engine: forward + backward edges/s.
+
+Workload: the power-law graph N=170,000, 1.2M Zipf(2.1) in-edges (capped at
+13,000) plus 170,000 self-loops, dot-product score, H=8 heads of D=16, bf16
+I/O with fp32 arithmetic, seeded synthetic inputs.  A step is one forward and
+one backward pass (the three kernels: forward, backward CSR pass, backward
+CSC pass) over the whole graph with inputs resident in HBM; L2 is flushed
+(256 MB write) before every timed step, outside the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl cuda|reference]
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
+oracle on the host cores instead, on a bounded sample of the same workload
+per step.  Under torchrun (N > 1) each rank runs an independent replica on
+its own GPU (the path needs no exchange between GPUs); the value is the
+edges processed by all ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "powerlaw170k"
+METRIC = "edges/sec fwd+bwd (1 GB300) and achieved HBM GB/s as % of gather roofline"
+KERNELS = ("fwd", "bwd_csr", "bwd_csc")
+KERNEL_SYMBOLS = {"fwd": "fwd_kernel", "bwd_csr": "bwd_csr_kernel", "bwd_csc": "bwd_csc_kernel"}
+KERNEL_SOURCES = ("attn_fwd.cuh", "attn_bwd.cuh", "gattn_internal.cuh", "attn_launch.cuh")
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ----------------------------------------------------------------------------
+# bookkeeping shared by both arms
+# ----------------------------------------------------------------------------
+def algorithmic_bytes(N, M, H, D, s):
+    """Bytes each kernel must move at minimum (gathers counted per edge).
+
+    fwd     : K and V row per edge, Q read + out write, lse write, indices, indptr
+    bwd_csr : K and V row per edge, Q, O, dO read + dQ write, lse read + Delta
+              write, indices, indptr
+    bwd_csc : Q and dO row per edge, lse and Delta per edge and head, K, V read
+              + dK, dV write, transposed indices, indptrT
+    """
+    HD = H * D
+    idx = 4 * M + 4 * (N + 1)
+    return {
+        "fwd": M * HD * 2 * s + 2 * N * HD * s + 4 * N * H + idx,
+        "bwd_csr": M * HD * 2 * s + 4 * N * HD * s + 8 * N * H + idx,
+        "bwd_csc": M * HD * 2 * s + 8 * M * H + 4 * N * HD * s + idx,
+    }
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_group(world):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group("gloo")
+    return dist
+
+
+def max_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def load_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "gnn_sparse_attention_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def dram_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes of ``kernel`` from the committed ncu summary, or None
+    when there is none or the kernel sources changed since it was captured."""
+    path = os.path.join(ROOT, "profiles", f"dram_traffic_{workload}.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("src_sha") != kernel_source_sha():
+        return None
+    k = rec.get("kernels", {}).get(kernel)
+    return None if k is None else k.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        busy = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def workload_config(w, N, M, extra=None):
+    cfg = {
+        "workload": (f"{w.name}: power-law graph N={N}, M={M} (1.2M Zipf(2.1) in-edges capped "
+                     f"at 13000 + {N} self-loops), dot score, H={w.H}, D={w.D}, bf16 I/O"),
+        "N": N, "M": M, "H": w.H, "D": w.D, "io_dtype": w.dtype, "score": w.score,
+        "seed": 0,
+    }
+    cfg.update(extra or {})
+    return cfg
+
+
+def oracle_sample_step(indptr, indices, f64, rows):
+    """One oracle fwd+bwd over a row subset; returns (edges, seconds)."""
+    import oracle
+    rp, col, rid = oracle.rows_subgraph(indptr, indices, rows)
+    t0 = time.perf_counter()
+    oracle.forward(rp, col, f64["Q"], f64["K"], f64["V"], rows=rid)
+    oracle.backward(rp, col, f64["Q"], f64["K"], f64["V"], f64["dO"][rows], rows=rid)
+    return int(rp[-1]), time.perf_counter() - t0
+
+
+def decoded_inputs(f):
+    """The bf16 inputs decoded exactly to fp64 (what the GPU path computes on)."""
+    import torch
+    return {k: torch.from_numpy(f[k]).to(torch.bfloat16).double().numpy()
+            for k in ("Q", "K", "V", "dO")}
+
+
+# ----------------------------------------------------------------------------
+# CUDA arm
+# ----------------------------------------------------------------------------
+def run_cuda(args):
+    import numpy as np
+    import torch
+
+    from gnn_sparse_attention_gb300 import binding as gb
+    from gnn_sparse_attention_gb300 import synth
+
+    rank, world, local = dist_env()
+    dist = init_group(world)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = synth.WORKLOADS[WORKLOAD]
+    indptr, indices = synth.make_graph(w, seed=0)
+    f = synth.make_features(w, seed=0)
+    N, M = len(indptr) - 1, int(indptr[-1])
+    H, D, s = w.H, w.D, 2
+    tdt = torch.bfloat16
+    Q, K, V, G = (torch.from_numpy(f[k]).to(dev, tdt) for k in ("Q", "K", "V", "dO"))
+    plan = gb.gattn_plan_create(torch.from_numpy(indptr).to(dev),
+                                torch.from_numpy(indices).to(dev))
+    info = plan.info()
+    score = gb.Score("dot")
+    out = torch.empty_like(Q)
+    lse = torch.empty((N, H), dtype=torch.float32, device=dev)
+    dQ, dK, dV = (torch.empty_like(Q) for _ in range(3))
+    ws = plan.workspace(H, D, tdt, dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        gb.gattn_fwd(plan, Q, K, V, score, out=out, lse=lse, workspace=ws, stream=stream)
+        if ev:
+            ev[1].record(stream)
+        gb.gattn_bwd_dq(plan, Q, K, V, out, G, lse, score, dQ=dQ, workspace=ws, stream=stream)
+        if ev:
+            ev[2].record(stream)
+        gb.gattn_bwd_dkdv(plan, Q, K, V, G, lse, score, dK=dK, dV=dV, workspace=ws,
+                          stream=stream)
+        if ev:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    barrier(dist)
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(local)
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for k in range(args.steps):
+        flush.fill_(k & 255)                      # evict L2 (outside the timed region)
+        step(evs[k])
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    barrier(dist)
+    per = {name: [e[i].elapsed_time(e[i + 1]) for e in evs] for i, name in enumerate(KERNELS)}
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    total_ms = max_over_ranks(dist, sum(step_ms))
+    value = world * M * args.steps / (total_ms / 1e3)
+
+    # end to end through the public API with pinned host buffers
+    pin = {k: torch.from_numpy(f[k]).to(tdt).pin_memory() for k in ("Q", "K", "V", "dO")}
+    host_out = {k: torch.empty(x.shape, dtype=x.dtype).pin_memory()
+                for k, x in (("out", out), ("lse", lse), ("dQ", dQ), ("dK", dK), ("dV", dV))}
+
+    def e2e_step():
+        Q.copy_(pin["Q"], non_blocking=True)
+        K.copy_(pin["K"], non_blocking=True)
+        V.copy_(pin["V"], non_blocking=True)
+        G.copy_(pin["dO"], non_blocking=True)
+        step()
+        for k, x in (("out", out), ("lse", lse), ("dQ", dQ), ("dK", dK), ("dV", dV)):
+            host_out[k].copy_(x, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(dist)
+    e2e_ms = 0.0
+    for k in range(args.steps):
+        flush.fill_(k & 255)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        e2e_step()
+        torch.cuda.synchronize()                  # the step's results are on the host
+        e2e_ms += (time.perf_counter() - t0) * 1e3
+    e2e_ms = max_over_ranks(dist, e2e_ms)
+    h2d = 4 * N * H * D * s
+    d2h = 4 * N * H * D * s + 4 * N * H
+
+    # roofline of the dominant kernel
+    nbytes = algorithmic_bytes(N, M, H, D, s)
+    mean = {k: statistics.mean(v) for k, v in per.items()}
+    dom = max(KERNELS, key=lambda k: mean[k])
+    peak, peak_kind = load_peak()
+    achieved = nbytes[dom] / (mean[dom] / 1e3) / 1e9
+    kernels = {k: {"ms": round(mean[k], 5), "algorithmic_bytes": nbytes[k],
+                   "gbs": round(nbytes[k] / (mean[k] / 1e3) / 1e9, 1),
+                   "frac": round(nbytes[k] / (mean[k] / 1e3) / 1e9 / peak, 4),
+                   "share": round(mean[k] / sum(mean.values()), 4)} for k in KERNELS}
+    step_bytes = sum(nbytes.values())
+    torch.cuda.synchronize()
+
+    # oracle timed on the host cores on a bounded sample (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        f64 = decoded_inputs(f)
+        rows = np.arange(0, N // 2)
+        edges, sec = oracle_sample_step(indptr, indices, f64, rows)
+        cpu = {"value": edges / sec, "unit": "edges/s", "cores": 1, "kind": "oracle",
+               "sample": f"one fp64 oracle fwd+bwd over destination rows [0, {N // 2}) of "
+                         f"{WORKLOAD} ({edges} edges, {sec:.1f} s, serial C, bf16 inputs "
+                         f"decoded exactly)"}
+
+    res = {
+        "metric": METRIC, "value": value, "unit": "edges/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded generator)",
+        "config": workload_config(w, N, M, {
+            "parallelism": "replicas" if world > 1 else "single",
+            "l2": "flushed before every timed step (256 MB write, outside the timed region)",
+            "plan": {"heavy_threshold": info["heavy_threshold"], "chunk": info["chunk"],
+                     "n_heavy": info["n_heavy"], "n_chunks": info["n_chunks"],
+                     "n_heavy_src": info["n_heavy_src"]}}),
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
+                     "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4),
+                     "traffic": dram_traffic(dom, WORKLOAD)},
+        "step_gbs": round(step_bytes / (statistics.mean(step_ms) / 1e3) / 1e9, 1),
+        "kernels": kernels,
+        "e2e": {"value": world * M * args.steps / (e2e_ms / 1e3), "unit": "edges/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    plan.close()
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------
+# reference arm: the fp64 oracle on the host cores
+# ----------------------------------------------------------------------------
+def run_reference(args):
+    import numpy as np
+
+    from gnn_sparse_attention_gb300 import synth
+
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    w = synth.WORKLOADS[WORKLOAD]
+    indptr, indices = synth.make_graph(w, seed=0)
+    f = synth.make_features(w, seed=0)
+    N, M = len(indptr) - 1, int(indptr[-1])
+    f64 = decoded_inputs(f)
+    n_rows = N // 16
+    edges_tot, sec_tot = 0, 0.0
+    r = np.random.default_rng(1)
+    for k in range(args.warmup + args.steps):
+        start = int(r.integers(0, N - n_rows))
+        e, sec = oracle_sample_step(indptr, indices, f64, np.arange(start, start + n_rows))
+        if k >= args.warmup:
+            edges_tot += e
+            sec_tot += sec
+    value = edges_tot / sec_tot
+    sample = (f"per step: one fp64 oracle fwd+bwd over {n_rows} consecutive destination rows "
+              f"of {WORKLOAD} at a random offset ({edges_tot // max(args.steps, 1)} edges "
+              "on average), serial C")
+    res = {
+        "metric": METRIC, "value": value, "unit": "edges/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": sec_tot * 1e3 / max(args.steps, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded generator)", "impl": "reference",
+        "config": workload_config(w, N, M, {"parallelism": "host cores"}),
+        "cpu_baseline": {"value": value, "unit": "edges/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "edges/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(res), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("cuda", "reference"), default="cuda")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the oracle timing (profiling runs)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_cuda(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,491 @@
+// plan.cu -- per-graph plan builder, entirely on the device.
+//
+// "On Efficient Scaling of GNNs via IO-Aware Layers Implementations", zh/ko
+// technical summaries, "Methodology": nodes are split by a degree threshold
+// into light and heavy sets and heavy nodes are tiled over edge chunks
+// (reduction layers); graph metadata and the transposed adjacency are built
+// once and cached for the backward pass (SpMM layers).  Here the same split
+// drives the attention kernels on both the CSR (destinations) and the cached
+// CSC (sources).
+//
+// Steps: validate the CSR -> degrees, histograms and split flags -> integer
+// exclusive scans -> item lists -> CSC by a stable LSD radix sort of the
+// edge ids keyed by source (so each column lists its edges in CSR order).
+// Every result is integer and independent of thread scheduling.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "gattn_internal.cuh"
+
+namespace gattn {
+
+namespace {
+
+constexpr int kScanItems = 8;
+constexpr int kTile = kThreads * kScanItems;  // 2048 elements per scan / sort tile
+
+#define GATTN_CUDA(call)                                                              \
+  do {                                                                                \
+    cudaError_t e_ = (call);                                                          \
+    if (e_ != cudaSuccess) {                                                          \
+      set_error("%s failed: %s (%s:%d)", #call, cudaGetErrorString(e_), __FILE__,     \
+                __LINE__);                                                            \
+      return e_ == cudaErrorMemoryAllocation ? GATTN_ERR_OOM : GATTN_ERR_CUDA;        \
+    }                                                                                 \
+  } while (0)
+
+// ---------------------------------------------------------------------------
+// validation: bit 1 indptr[0] != 0, bit 2 indptr[N] != M, bit 4 decreasing
+// indptr, bit 8 a source outside [0, N)
+// ---------------------------------------------------------------------------
+__global__ void k_validate(const int32_t* __restrict__ indptr, const int32_t* __restrict__ indices,
+                           int32_t N, int64_t M, int32_t* err) {
+  const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  int bad = 0;
+  if (tid == 0) {
+    if (indptr[0] != 0) bad |= 1;
+    if ((int64_t)indptr[N] != M) bad |= 2;
+  }
+  for (int64_t i = tid; i < N; i += stride)
+    if (indptr[i + 1] < indptr[i]) bad |= 4;
+  for (int64_t e = tid; e < M; e += stride) {
+    const int32_t j = indices[e];
+    if (j < 0 || j >= N) bad |= 8;
+  }
+  if (bad) atomicOr(err, bad);
+}
+
+__device__ __forceinline__ int degree_bin(int32_t d) { return d <= 0 ? 0 : 32 - __clz(d); }
+
+// Degrees from a row pointer, histogram, max, and the split counts:
+// light[i] = deg <= T, heavy[i] = deg > T, nchunk[i] = heavy ? ceil(deg/C) : 0.
+// Arrays light/heavy/nchunk have N+1 entries, the last one 0 (scan totals).
+__global__ void k_degrees(const int32_t* __restrict__ ptr, int32_t N, int32_t T, int32_t C,
+                          int32_t* __restrict__ deg, int32_t* __restrict__ hist,
+                          int32_t* __restrict__ maxdeg, int32_t* __restrict__ light,
+                          int32_t* __restrict__ heavy, int32_t* __restrict__ nchunk) {
+  __shared__ int32_t s_hist[33];
+  __shared__ int32_t s_max;
+  if (threadIdx.x < 33) s_hist[threadIdx.x] = 0;
+  if (threadIdx.x == 0) s_max = 0;
+  __syncthreads();
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  int32_t my_max = 0;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i <= N; i += stride) {
+    if (i == N) {
+      light[N] = heavy[N] = nchunk[N] = 0;
+      continue;
+    }
+    const int32_t d = ptr[i + 1] - ptr[i];
+    deg[i] = d;
+    atomicAdd(&s_hist[degree_bin(d)], 1);
+    my_max = max(my_max, d);
+    const bool h = d > T;
+    light[i] = h ? 0 : 1;
+    heavy[i] = h ? 1 : 0;
+    nchunk[i] = h ? (d + C - 1) / C : 0;
+  }
+  atomicMax(&s_max, my_max);
+  __syncthreads();
+  if (threadIdx.x < 33 && s_hist[threadIdx.x]) atomicAdd(&hist[threadIdx.x], s_hist[threadIdx.x]);
+  if (threadIdx.x == 0) atomicMax(maxdeg, s_max);
+}
+
+__global__ void k_count_sources(const int32_t* __restrict__ indices, int64_t M,
+                                int32_t* __restrict__ outdeg) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < M; e += stride)
+    atomicAdd(&outdeg[indices[e]], 1);
+}
+
+// Row pointer from counts: ptr[i] = exclusive scan (computed separately).
+// Item lists: chunks of heavy rows first (item index = chunk index, w =
+// heavy id), then light rows (w = -1).  Also the exported light / chunk
+// arrays and hfirst (first chunk of every heavy row, plus the total).
+__global__ void k_fill_items(const int32_t* __restrict__ ptr, int32_t N, int32_t C,
+                             const int32_t* __restrict__ light_pos,
+                             const int32_t* __restrict__ heavy_pos,
+                             const int32_t* __restrict__ chunk_pos, int64_t n_chunks,
+                             int64_t n_heavy, int32_t* __restrict__ light_list,
+                             int4* __restrict__ items, int32_t* __restrict__ hfirst) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < N; i += stride) {
+    const int32_t e0 = ptr[i], e1 = ptr[i + 1];
+    const int32_t lp = light_pos[i];
+    if (light_pos[i + 1] != lp) {  // light row
+      light_list[lp] = (int32_t)i;
+      items[n_chunks + lp] = make_int4((int)i, e0, e1, -1);
+    } else {
+      const int32_t h = heavy_pos[i];
+      int32_t c = chunk_pos[i];
+      hfirst[h] = c;
+      for (int32_t s = e0; s < e1; s += C, ++c)
+        items[c] = make_int4((int)i, s, min(s + C, e1), h);
+    }
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) hfirst[n_heavy] = (int32_t)n_chunks;
+}
+
+// ---------------------------------------------------------------------------
+// exclusive scan of int32 (tiles of 2048, recursive over tile totals)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int32_t block_exclusive_scan(int32_t v, int32_t* s_warp,
+                                                        int32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int32_t w = lane < kWarpsPerBlock ? s_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < kWarpsPerBlock; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < kWarpsPerBlock) s_warp[lane] = w;  // inclusive warp totals
+  }
+  __syncthreads();
+  const int32_t before = warp ? s_warp[warp - 1] : 0;
+  *total = s_warp[kWarpsPerBlock - 1];
+  __syncthreads();
+  return before + x - v;
+}
+
+__global__ void k_scan_tiles(const int32_t* __restrict__ in, int32_t* __restrict__ out, int64_t n,
+                             int32_t* __restrict__ tile_sums) {
+  __shared__ int32_t s_warp[kWarpsPerBlock];
+  const int64_t base = int64_t(blockIdx.x) * kTile + int64_t(threadIdx.x) * kScanItems;
+  int32_t v[kScanItems];
+  int32_t sum = 0;
+#pragma unroll
+  for (int k = 0; k < kScanItems; ++k) {
+    v[k] = base + k < n ? in[base + k] : 0;
+    sum += v[k];
+  }
+  int32_t total;
+  int32_t run = block_exclusive_scan(sum, s_warp, &total);
+#pragma unroll
+  for (int k = 0; k < kScanItems; ++k) {
+    if (base + k < n) out[base + k] = run;
+    run += v[k];
+  }
+  if (threadIdx.x == 0 && tile_sums) tile_sums[blockIdx.x] = total;
+}
+
+__global__ void k_scan_add(int32_t* __restrict__ out, int64_t n, const int32_t* __restrict__ offs) {
+  const int32_t add = offs[blockIdx.x];
+  const int64_t base = int64_t(blockIdx.x) * kTile;
+  for (int k = threadIdx.x; k < kTile; k += blockDim.x)
+    if (base + k < n) out[base + k] += add;
+}
+
+struct Scratch {
+  std::vector<void*> ptrs;
+  ~Scratch() {
+    for (void* p : ptrs) cudaFree(p);
+  }
+  template <typename T>
+  cudaError_t get(T** p, size_t n) {
+    void* q = nullptr;
+    cudaError_t e = cudaMalloc(&q, (n ? n : 1) * sizeof(T));
+    if (e == cudaSuccess) ptrs.push_back(q);
+    *p = reinterpret_cast<T*>(q);
+    return e;
+  }
+};
+
+gattn_status exclusive_scan(const int32_t* in, int32_t* out, int64_t n, Scratch& scr,
+                            cudaStream_t st) {
+  if (n <= 0) return GATTN_OK;
+  const int64_t tiles = (n + kTile - 1) / kTile;
+  if (tiles == 1) {
+    k_scan_tiles<<<1, kThreads, 0, st>>>(in, out, n, nullptr);
+    GATTN_CUDA(cudaGetLastError());
+    return GATTN_OK;
+  }
+  int32_t *sums = nullptr, *offs = nullptr;
+  GATTN_CUDA(scr.get(&sums, tiles));
+  GATTN_CUDA(scr.get(&offs, tiles));
+  k_scan_tiles<<<(unsigned)tiles, kThreads, 0, st>>>(in, out, n, sums);
+  GATTN_CUDA(cudaGetLastError());
+  gattn_status s = exclusive_scan(sums, offs, tiles, scr, st);
+  if (s != GATTN_OK) return s;
+  k_scan_add<<<(unsigned)tiles, kThreads, 0, st>>>(out, n, offs);
+  GATTN_CUDA(cudaGetLastError());
+  return GATTN_OK;
+}
+
+// ---------------------------------------------------------------------------
+// stable LSD radix sort of (key = source, value = edge id), 8-bit digits
+// ---------------------------------------------------------------------------
+__global__ void k_radix_hist(const int32_t* __restrict__ keys, int64_t n, int shift,
+                             int64_t n_tiles, int32_t* __restrict__ hist) {
+  __shared__ int32_t s_cnt[256];
+  s_cnt[threadIdx.x] = 0;
+  __syncthreads();
+  const int64_t base = int64_t(blockIdx.x) * kTile;
+  for (int k = threadIdx.x; k < kTile; k += blockDim.x)
+    if (base + k < n) atomicAdd(&s_cnt[(keys[base + k] >> shift) & 255], 1);
+  __syncthreads();
+  hist[int64_t(threadIdx.x) * n_tiles + blockIdx.x] = s_cnt[threadIdx.x];
+}
+
+// Elements of a tile are taken in rounds of 256 in index order; within a
+// round, warp w's lanes precede warp w+1's, and lanes are ordered by index,
+// so (previous rounds, earlier warps, lower lanes) is exactly "earlier in the
+// input": the scatter is stable.
+__global__ void k_radix_scatter(const int32_t* __restrict__ kin, const int32_t* __restrict__ vin,
+                                int32_t* __restrict__ kout, int32_t* __restrict__ vout, int64_t n,
+                                int shift, int64_t n_tiles, const int32_t* __restrict__ offs) {
+  __shared__ int32_t s_wcnt[kWarpsPerBlock][256];
+  __shared__ int32_t s_woff[kWarpsPerBlock][256];
+  __shared__ int32_t s_base[256];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int w = 0; w < kWarpsPerBlock; ++w) s_wcnt[w][threadIdx.x] = 0;
+  s_base[threadIdx.x] = offs[int64_t(threadIdx.x) * n_tiles + blockIdx.x];
+  __syncthreads();
+  const int64_t base = int64_t(blockIdx.x) * kTile;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int r = 0; r < kScanItems; ++r) {
+    const int64_t idx = base + int64_t(r) * kThreads + threadIdx.x;
+    const bool valid = idx < n;
+    const int32_t key = valid ? kin[idx] : 0;
+    const int32_t val = valid ? vin[idx] : 0;
+    const int d = valid ? ((key >> shift) & 255) : 256;
+    const unsigned peers = __match_any_sync(0xffffffffu, d);
+    const int rank = __popc(peers & lt_mask);
+    if (valid && rank == 0) s_wcnt[warp][d] = __popc(peers);
+    __syncthreads();
+    {
+      const int dig = threadIdx.x;
+      int32_t acc = s_base[dig];
+      for (int w = 0; w < kWarpsPerBlock; ++w) {
+        const int32_t c = s_wcnt[w][dig];
+        s_woff[w][dig] = acc;
+        acc += c;
+        s_wcnt[w][dig] = 0;
+      }
+      s_base[dig] = acc;
+    }
+    __syncthreads();
+    if (valid) {
+      const int32_t pos = s_woff[warp][d] + rank;
+      kout[pos] = key;
+      vout[pos] = val;
+    }
+  }
+}
+
+__global__ void k_iota(int32_t* __restrict__ v, int64_t n) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+    v[i] = (int32_t)i;
+}
+
+// csc_dst[p] = destination row of CSR edge csc_eid[p] (last i with indptr[i] <= e)
+__global__ void k_edge_rows(const int32_t* __restrict__ indptr, int32_t N,
+                            const int32_t* __restrict__ eid, int64_t M, int32_t* __restrict__ dst) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t p = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; p < M; p += stride) {
+    const int32_t e = eid[p];
+    int32_t lo = 0, hi = N;  // invariant: indptr[lo] <= e < indptr[hi]
+    while (hi - lo > 1) {
+      const int32_t mid = lo + (hi - lo) / 2;
+      if (indptr[mid] <= e) lo = mid;
+      else hi = mid;
+    }
+    dst[p] = lo;
+  }
+}
+
+int grid_1d(int64_t n, int num_sms) {
+  const int64_t want = (n + kThreads - 1) / kThreads;
+  const int64_t cap = int64_t(num_sms) * 8;
+  return (int)(want < 1 ? 1 : (want > cap ? cap : want));
+}
+
+// The light/heavy split on one side (CSR or CSC): degrees, histogram,
+// scans, item list.  Allocates its outputs in the plan.
+struct Side {
+  int32_t *deg, *hist, *maxdeg, *light_list, *hfirst;
+  int4* items;
+  int64_t n_light, n_heavy, n_chunks;
+};
+
+template <typename T>
+cudaError_t plan_alloc(Plan* p, T** ptr, size_t n) {
+  void* q = nullptr;
+  cudaError_t e = cudaMalloc(&q, (n ? n : 1) * sizeof(T));
+  if (e == cudaSuccess) {
+    p->allocs.push_back(q);
+    p->device_bytes += (n ? n : 1) * sizeof(T);
+  }
+  *ptr = reinterpret_cast<T*>(q);
+  return e;
+}
+
+gattn_status build_side(Plan* p, const int32_t* ptr, Scratch& scr, cudaStream_t st, Side* s) {
+  const int32_t N = p->N;
+  int32_t *lf, *hf, *nc, *lpos, *hpos, *cpos;
+  GATTN_CUDA(plan_alloc(p, &s->deg, N));
+  GATTN_CUDA(plan_alloc(p, &s->hist, 33));
+  GATTN_CUDA(scr.get(&s->maxdeg, 1));
+  GATTN_CUDA(scr.get(&lf, N + 1));
+  GATTN_CUDA(scr.get(&hf, N + 1));
+  GATTN_CUDA(scr.get(&nc, N + 1));
+  GATTN_CUDA(scr.get(&lpos, N + 1));
+  GATTN_CUDA(scr.get(&hpos, N + 1));
+  GATTN_CUDA(scr.get(&cpos, N + 1));
+  GATTN_CUDA(cudaMemsetAsync(s->hist, 0, 33 * sizeof(int32_t), st));
+  GATTN_CUDA(cudaMemsetAsync(s->maxdeg, 0, sizeof(int32_t), st));
+  k_degrees<<<grid_1d(N + 1, p->num_sms), kThreads, 0, st>>>(ptr, N, p->T, p->C, s->deg, s->hist,
+                                                             s->maxdeg, lf, hf, nc);
+  GATTN_CUDA(cudaGetLastError());
+  gattn_status r;
+  if ((r = exclusive_scan(lf, lpos, N + 1, scr, st)) != GATTN_OK) return r;
+  if ((r = exclusive_scan(hf, hpos, N + 1, scr, st)) != GATTN_OK) return r;
+  if ((r = exclusive_scan(nc, cpos, N + 1, scr, st)) != GATTN_OK) return r;
+  int32_t tot[3];
+  GATTN_CUDA(cudaMemcpyAsync(&tot[0], lpos + N, 4, cudaMemcpyDeviceToHost, st));
+  GATTN_CUDA(cudaMemcpyAsync(&tot[1], hpos + N, 4, cudaMemcpyDeviceToHost, st));
+  GATTN_CUDA(cudaMemcpyAsync(&tot[2], cpos + N, 4, cudaMemcpyDeviceToHost, st));
+  GATTN_CUDA(cudaStreamSynchronize(st));
+  s->n_light = tot[0];
+  s->n_heavy = tot[1];
+  s->n_chunks = tot[2];
+  GATTN_CUDA(plan_alloc(p, &s->light_list, s->n_light));
+  GATTN_CUDA(plan_alloc(p, &s->items, s->n_light + s->n_chunks));
+  GATTN_CUDA(plan_alloc(p, &s->hfirst, s->n_heavy + 1));
+  k_fill_items<<<grid_1d(N, p->num_sms), kThreads, 0, st>>>(ptr, N, p->C, lpos, hpos, cpos,
+                                                            s->n_chunks, s->n_heavy, s->light_list,
+                                                            s->items, s->hfirst);
+  GATTN_CUDA(cudaGetLastError());
+  return GATTN_OK;
+}
+
+}  // namespace
+
+gattn_status plan_build(Plan* p, const int32_t* indptr, const int32_t* indices, cudaStream_t st) {
+  const int32_t N = p->N;
+  const int64_t M = p->M;
+  Scratch scr;
+  // 1. validate
+  int32_t* err = nullptr;
+  GATTN_CUDA(scr.get(&err, 1));
+  GATTN_CUDA(cudaMemsetAsync(err, 0, sizeof(int32_t), st));
+  k_validate<<<grid_1d(M > N ? M : N + 1, p->num_sms), kThreads, 0, st>>>(indptr, indices, N, M,
+                                                                           err);
+  GATTN_CUDA(cudaGetLastError());
+  int32_t herr = 0;
+  GATTN_CUDA(cudaMemcpyAsync(&herr, err, 4, cudaMemcpyDeviceToHost, st));
+  GATTN_CUDA(cudaStreamSynchronize(st));
+  if (herr) {
+    set_error("invalid CSR graph:%s%s%s%s", (herr & 1) ? " indptr[0] != 0;" : "",
+              (herr & 2) ? " indptr[N] != M;" : "", (herr & 4) ? " indptr decreases;" : "",
+              (herr & 8) ? " source index outside [0, N);" : "");
+    return GATTN_ERR_BAD_GRAPH;
+  }
+  // 2. private copies of the CSR
+  GATTN_CUDA(plan_alloc(p, &p->indptr, N + 1));
+  GATTN_CUDA(plan_alloc(p, &p->indices, M));
+  GATTN_CUDA(cudaMemcpyAsync(p->indptr, indptr, (N + 1) * sizeof(int32_t),
+                             cudaMemcpyDeviceToDevice, st));
+  if (M) GATTN_CUDA(cudaMemcpyAsync(p->indices, indices, M * sizeof(int32_t),
+                                    cudaMemcpyDeviceToDevice, st));
+  // 3. destination side
+  Side d{};
+  gattn_status r = build_side(p, p->indptr, scr, st, &d);
+  if (r != GATTN_OK) return r;
+  // 4. transpose: out-degrees -> indptrT -> stable sort of edge ids by source
+  int32_t* counts = nullptr;
+  GATTN_CUDA(scr.get(&counts, N + 1));
+  GATTN_CUDA(cudaMemsetAsync(counts, 0, (N + 1) * sizeof(int32_t), st));
+  if (M) {
+    k_count_sources<<<grid_1d(M, p->num_sms), kThreads, 0, st>>>(p->indices, M, counts);
+    GATTN_CUDA(cudaGetLastError());
+  }
+  GATTN_CUDA(plan_alloc(p, &p->indptrT, N + 1));
+  if ((r = exclusive_scan(counts, p->indptrT, N + 1, scr, st)) != GATTN_OK) return r;
+  GATTN_CUDA(plan_alloc(p, &p->csc_eid, M));
+  GATTN_CUDA(plan_alloc(p, &p->csc_dst, M));
+  if (M) {
+    int32_t *ka, *kb, *va, *vb, *hist, *offs;
+    const int64_t tiles = (M + kTile - 1) / kTile;
+    GATTN_CUDA(scr.get(&ka, M));
+    GATTN_CUDA(scr.get(&kb, M));
+    GATTN_CUDA(scr.get(&va, M));
+    GATTN_CUDA(scr.get(&vb, M));
+    GATTN_CUDA(scr.get(&hist, tiles * 256));
+    GATTN_CUDA(scr.get(&offs, tiles * 256));
+    GATTN_CUDA(cudaMemcpyAsync(ka, p->indices, M * sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
+    k_iota<<<grid_1d(M, p->num_sms), kThreads, 0, st>>>(va, M);
+    GATTN_CUDA(cudaGetLastError());
+    int bits = 1;
+    while (bits < 31 && (int64_t(1) << bits) < N) ++bits;
+    const int passes = (bits + 7) / 8;
+    int32_t *kin = ka, *kout = kb, *vin = va, *vout = vb;
+    for (int pass = 0; pass < passes; ++pass) {
+      const int shift = 8 * pass;
+      k_radix_hist<<<(unsigned)tiles, kThreads, 0, st>>>(kin, M, shift, tiles, hist);
+      GATTN_CUDA(cudaGetLastError());
+      if ((r = exclusive_scan(hist, offs, tiles * 256, scr, st)) != GATTN_OK) return r;
+      k_radix_scatter<<<(unsigned)tiles, kThreads, 0, st>>>(kin, vin, kout, vout, M, shift, tiles,
+                                                            offs);
+      GATTN_CUDA(cudaGetLastError());
+      int32_t* t = kin;
+      kin = kout;
+      kout = t;
+      t = vin;
+      vin = vout;
+      vout = t;
+    }
+    GATTN_CUDA(cudaMemcpyAsync(p->csc_eid, vin, M * sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
+    k_edge_rows<<<grid_1d(M, p->num_sms), kThreads, 0, st>>>(p->indptr, N, p->csc_eid, M,
+                                                             p->csc_dst);
+    GATTN_CUDA(cudaGetLastError());
+  }
+  // 5. source side
+  Side s{};
+  if ((r = build_side(p, p->indptrT, scr, st, &s)) != GATTN_OK) return r;
+  // 6. counters
+  GATTN_CUDA(plan_alloc(p, &p->cnt_fwd, d.n_heavy));
+  GATTN_CUDA(plan_alloc(p, &p->cnt_dq, d.n_heavy));
+  GATTN_CUDA(plan_alloc(p, &p->cnt_dkv, s.n_heavy));
+  GATTN_CUDA(plan_alloc(p, &p->cnt_da, 1));
+  GATTN_CUDA(cudaMemsetAsync(p->cnt_fwd, 0, (d.n_heavy ? d.n_heavy : 1) * 4, st));
+  GATTN_CUDA(cudaMemsetAsync(p->cnt_dq, 0, (d.n_heavy ? d.n_heavy : 1) * 4, st));
+  GATTN_CUDA(cudaMemsetAsync(p->cnt_dkv, 0, (s.n_heavy ? s.n_heavy : 1) * 4, st));
+  GATTN_CUDA(cudaMemsetAsync(p->cnt_da, 0, 4, st));
+  int32_t mx[2];
+  GATTN_CUDA(cudaMemcpyAsync(&mx[0], d.maxdeg, 4, cudaMemcpyDeviceToHost, st));
+  GATTN_CUDA(cudaMemcpyAsync(&mx[1], s.maxdeg, 4, cudaMemcpyDeviceToHost, st));
+  GATTN_CUDA(cudaStreamSynchronize(st));
+  p->deg = d.deg;
+  p->hist = d.hist;
+  p->light = d.light_list;
+  p->items = d.items;
+  p->hfirst = d.hfirst;
+  p->n_light = d.n_light;
+  p->n_heavy = d.n_heavy;
+  p->n_chunks = d.n_chunks;
+  p->outdeg = s.deg;
+  p->hist_out = s.hist;
+  p->light_src = s.light_list;
+  p->items_src = s.items;
+  p->hfirst_src = s.hfirst;
+  p->n_light_src = s.n_light;
+  p->n_heavy_src = s.n_heavy;
+  p->n_src_chunks = s.n_chunks;
+  p->max_deg = mx[0];
+  p->max_outdeg = mx[1];
+  return GATTN_OK;
+}
+
+}  // namespace gattn

@@ -1,0 +1,223 @@
+/*
+ * gattn.h -- C ABI of the fused CSR graph-attention engine for GB300 (sm_103a).
+ *
+ * The operation ("On Efficient Scaling of GNNs via IO-Aware Layers
+ * Implementations", zh/ko technical summaries, section "Methodology",
+ * attention-based layers): for every destination node i of a graph given in
+ * CSR form (row i lists the sources j of the edges j -> i), score each
+ * in-neighbour j, normalise the scores with a softmax over the neighbourhood
+ * and sum the neighbours' values with those weights -- in one streaming pass
+ * with an online softmax whose running max and sum stay in registers, so no
+ * O(M*H) edge tensor is ever stored.  Only a per-node, per-head log-sum-exp
+ * is kept; the backward pass recomputes the weights from it.  The graph
+ * metadata (degree split, heavy-node edge chunks, transposed adjacency) is
+ * built once per graph and cached ("Methodology", SpMM and reduction layers).
+ *
+ * Two score functions (the two attention layers the pages name):
+ *   GATTN_SCORE_DOT   : s_ijh = scale * sum_d Q[i,h,d] K[j,h,d]
+ *                       (Graph Transformer; scale = 1/sqrt(D) by default)
+ *   GATTN_SCORE_GATV2 : s_ijh = sum_d a[h,d] * LeakyReLU(Q[i,h,d] + K[j,h,d])
+ *                       (GATv2 with Q = x_l, K = x_r, slope 0.2 by default)
+ * Then, for a node with at least one in-edge,
+ *   alpha_ijh = exp(s_ijh - lse[i,h]),  lse[i,h] = log sum_j exp(s_ijh),
+ *   out[i,h,:] = sum_j alpha_ijh V[j,h,:].
+ * A node with no in-edges gets out = 0 and lse = -inf.
+ *
+ * Conventions shared by every entry point
+ *   - Dense tensors (Q, K, V, out, dout, dQ, dK, dV) are row-major
+ *     [N, H, D], contiguous, in the I/O dtype (fp32 or bf16); the base
+ *     address must be 16-byte aligned.  lse is fp32 [N, H].  a and da are
+ *     fp32 [H, D].
+ *   - The graph is int32 CSR by destination: indptr[N+1] (indptr[0] = 0,
+ *     non-decreasing, indptr[N] = M) and indices[M] (sources, in [0, N)).
+ *     Rows need not be sorted; multi-edges are kept as separate edges.
+ *   - Every pointer argument that names tensor data is a DEVICE pointer
+ *     unless the argument's comment says "host".  All device memory is owned
+ *     by the caller, except the plan's own buffers.
+ *   - Calls are asynchronous on the given stream unless stated otherwise;
+ *     a status other than GATTN_OK leaves outputs undefined.  No call aborts
+ *     or traps; gattn_last_error() gives a message for the calling thread.
+ *   - Supported head layouts: D a power of two with D * sizeof(dtype) in
+ *     [16, 512] bytes, H a power of two, and H * D * sizeof(dtype) in
+ *     [32, 2048] bytes.  Other shapes return GATTN_ERR_UNSUPPORTED.
+ */
+#ifndef GATTN_H_
+#define GATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GATTN_API __attribute__((visibility("default")))
+#else
+#define GATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* gattn_stream_t;
+
+typedef enum {
+  GATTN_OK = 0,
+  GATTN_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad enum, small workspace */
+  GATTN_ERR_BAD_GRAPH = 2,   /* CSR violates the conventions above */
+  GATTN_ERR_UNSUPPORTED = 3, /* (H, D, dtype) outside the supported set */
+  GATTN_ERR_OOM = 4,         /* plan buffers could not be allocated */
+  GATTN_ERR_CUDA = 5,        /* a CUDA runtime call or kernel launch failed */
+  GATTN_ERR_TIMEOUT = 6      /* reserved: no entry point waits on the device */
+} gattn_status;
+
+typedef enum { GATTN_F32 = 0, GATTN_BF16 = 1 } gattn_dtype;
+
+typedef enum { GATTN_SCORE_DOT = 0, GATTN_SCORE_GATV2 = 1 } gattn_score_kind;
+
+/* Score parameters.  Host struct; `a` is a device pointer. */
+typedef struct {
+  int32_t kind;    /* gattn_score_kind */
+  float scale;     /* DOT: multiplier of q.k; 0 selects 1/sqrt(D) */
+  const float* a;  /* GATV2: device fp32 [H, D]; ignored for DOT */
+  float neg_slope; /* GATV2: LeakyReLU slope for z <= 0; use 0.2 for the usual layer */
+} gattn_score;
+
+/* Plan options.  Host struct; pass NULL for the defaults. */
+typedef struct {
+  int32_t heavy_threshold; /* node is heavy when its degree > this; <= 0: default 256 */
+  int32_t chunk;           /* edges per heavy-node chunk; <= 0: default 256 */
+  int32_t tile_enable;     /* reserved for the dense-tile path; must be 0 */
+  float tile_density;      /* reserved */
+} gattn_plan_opts;
+
+/* Sizes of a built plan (host struct filled by gattn_plan_get_info). */
+typedef struct {
+  int32_t N;
+  int64_t M;
+  int32_t heavy_threshold;
+  int32_t chunk;
+  int64_t n_light;      /* destinations with degree <= threshold */
+  int64_t n_heavy;      /* destinations with degree > threshold */
+  int64_t n_chunks;     /* edge chunks of the heavy destinations */
+  int64_t n_light_src;  /* sources with out-degree <= threshold */
+  int64_t n_heavy_src;  /* sources with out-degree > threshold */
+  int64_t n_src_chunks; /* edge chunks of the heavy sources (CSC) */
+  int32_t max_deg;
+  int32_t max_outdeg;
+  size_t device_bytes;  /* device memory held by the plan */
+} gattn_plan_info;
+
+typedef struct gattn_plan gattn_plan;
+
+/*
+ * Build the per-graph plan ("Methodology": degree-aware light/heavy split of
+ * the nodes by a degree threshold, heavy nodes cut into edge chunks; the
+ * transposed adjacency cached for the backward pass).
+ *   indptr, indices : device int32 CSR (read during the call, not retained).
+ *   N >= 0, M >= 0  : node and edge counts (M < 2^31).
+ *   opts            : host, nullable.
+ *   out             : host; receives the plan, which owns its device buffers.
+ * The CSR is validated on the device first; a violation returns
+ * GATTN_ERR_BAD_GRAPH.  Synchronises `stream` (sizes are read back).
+ */
+GATTN_API gattn_status gattn_plan_create(const int32_t* indptr, const int32_t* indices, int32_t N,
+                               int64_t M, const gattn_plan_opts* opts, gattn_stream_t stream,
+                               gattn_plan** out);
+
+/* Free the plan's device buffers (synchronises the device first).  NULL is a no-op. */
+GATTN_API gattn_status gattn_plan_destroy(gattn_plan* plan);
+
+/* Host query of the plan's sizes. */
+GATTN_API gattn_status gattn_plan_get_info(const gattn_plan* plan, gattn_plan_info* info);
+
+/*
+ * Copy the plan's integer metadata to HOST buffers (each nullable; sizes in
+ * elements from gattn_plan_get_info).  Synchronous.  Definitions:
+ *   deg[N], hist[33]      : in-degrees; hist[b] counts nodes of degree bin b
+ *                           (bin 0: degree 0; bin b >= 1: 2^(b-1) <= deg < 2^b)
+ *   light[n_light]        : ascending destinations with deg <= threshold
+ *   chunks[3*n_chunks]    : (node, e0, e1) for heavy destinations in
+ *                           ascending order, e0 = indptr[i] + k*chunk,
+ *                           e1 = min(e0 + chunk, indptr[i+1])
+ *   indptrT[N+1], csc_dst[M], csc_eid[M] : the transpose, edges stably
+ *                           sorted by source over CSR edge order
+ *   outdeg[N], hist_out[33], light_src[n_light_src], src_chunks[3*n_src_chunks]
+ *                         : the same partition applied to the transpose
+ */
+GATTN_API gattn_status gattn_plan_export(const gattn_plan* plan, int32_t* deg, int32_t* hist,
+                               int32_t* light, int32_t* chunks, int32_t* indptrT,
+                               int32_t* csc_dst, int32_t* csc_eid, int32_t* outdeg,
+                               int32_t* hist_out, int32_t* light_src, int32_t* src_chunks);
+
+/*
+ * Bytes of caller-owned device workspace that gattn_fwd / gattn_bwd need
+ * for this plan and head layout (heavy-chunk partials, the backward's
+ * per-node Delta, GATv2 da partials).  Host call, no device work.
+ */
+GATTN_API gattn_status gattn_workspace_size(const gattn_plan* plan, int32_t H, int32_t D,
+                                  gattn_dtype dtype, size_t* bytes);
+
+/*
+ * Forward ("Methodology", attention-based layers, forward pass): one
+ * streaming pass over each destination's in-neighbours with an online
+ * softmax; heavy destinations are split over edge chunks whose partial
+ * (max, sum, acc) triples are merged in chunk order.
+ *   Q, K, V   : device [N, H, D] in `dtype` (GATv2: Q = x_l, K = x_r).
+ *   score     : host struct (see gattn_score).
+ *   out       : device [N, H, D] in `dtype` (written).
+ *   lse       : device fp32 [N, H] (written; natural log; -inf for isolated nodes).
+ *   workspace : device, >= gattn_workspace_size bytes, 16-byte aligned;
+ *               its contents need no initialisation.
+ * Calls that share a plan or a workspace must not overlap on the device.
+ */
+GATTN_API gattn_status gattn_fwd(const gattn_plan* plan, int32_t H, int32_t D, gattn_dtype dtype,
+                       const void* Q, const void* K, const void* V, const gattn_score* score,
+                       void* out, float* lse, void* workspace, size_t workspace_bytes,
+                       gattn_stream_t stream);
+
+/*
+ * Backward ("Methodology", attention-based layers, backward pass): the
+ * attention weights are recomputed on the fly from the cached lse; dQ is
+ * gathered over the CSR, dK and dV over the cached transpose.
+ *   Q, K, V, out, lse : as passed to / produced by gattn_fwd with this plan.
+ *   dout      : device [N, H, D] in `dtype`, gradient of the loss w.r.t. out.
+ *   dQ, dK, dV: device [N, H, D] in `dtype` (written, not accumulated).
+ *   da        : GATv2: device fp32 [H, D] (written), or NULL to skip; DOT: ignored.
+ *   workspace : as for gattn_fwd.
+ */
+GATTN_API gattn_status gattn_bwd(const gattn_plan* plan, int32_t H, int32_t D, gattn_dtype dtype,
+                       const void* Q, const void* K, const void* V, const gattn_score* score,
+                       const void* out, const void* dout, const float* lse, void* dQ, void* dK,
+                       void* dV, float* da, void* workspace, size_t workspace_bytes,
+                       gattn_stream_t stream);
+
+/*
+ * The two passes of gattn_bwd as separate calls (gattn_bwd = dq then dkdv on
+ * one stream).  gattn_bwd_dq runs the CSR pass: writes dQ, da (GATv2,
+ * nullable) and the per-node Delta = dout . out into the workspace.
+ * gattn_bwd_dkdv runs the CSC pass: writes dK, dV and reads that Delta, so
+ * it must follow a gattn_bwd_dq with the same plan, inputs and workspace.
+ */
+GATTN_API gattn_status gattn_bwd_dq(const gattn_plan* plan, int32_t H, int32_t D,
+                                    gattn_dtype dtype, const void* Q, const void* K,
+                                    const void* V, const gattn_score* score, const void* out,
+                                    const void* dout, const float* lse, void* dQ, float* da,
+                                    void* workspace, size_t workspace_bytes,
+                                    gattn_stream_t stream);
+GATTN_API gattn_status gattn_bwd_dkdv(const gattn_plan* plan, int32_t H, int32_t D,
+                                      gattn_dtype dtype, const void* Q, const void* K,
+                                      const void* V, const gattn_score* score, const void* dout,
+                                      const float* lse, void* dK, void* dV, void* workspace,
+                                      size_t workspace_bytes, gattn_stream_t stream);
+
+/* Message of the last failing call on this thread ("" if none).  Never NULL. */
+GATTN_API const char* gattn_last_error(void);
+
+/* Library version string, e.g. "gattn 0.1.0 sm_103a". */
+GATTN_API const char* gattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GATTN_H_ */
