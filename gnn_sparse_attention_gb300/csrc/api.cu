@@ -73,13 +73,15 @@ Workspace ws_layout(const Plan& p, int H, int D) {
   w.pstride = (int)align_up(HD + 2 * size_t(H), 4);
   size_t off = 0;
   w.fwd_part = off;
-  off = align_up(off + size_t(p.n_chunks) * w.pstride * 4, 256);
+  const size_t slots = size_t(p.n_chunks + p.n_inner);
+  const size_t slots_src = size_t(p.n_src_chunks + p.n_inner_src);
+  off = align_up(off + slots * w.pstride * 4, 256);
   w.dq_part = off;
-  off = align_up(off + size_t(p.n_chunks) * HD * 4, 256);
+  off = align_up(off + slots * HD * 4, 256);
   w.delta = off;
   off = align_up(off + size_t(p.N) * H * 4, 256);
   w.dkv_part = off;
-  off = align_up(off + size_t(p.n_src_chunks) * 2 * HD * 4, 256);
+  off = align_up(off + slots_src * 2 * HD * 4, 256);
   w.da_part = off;
   off = align_up(off + size_t(p.num_sms) * kMaxBlocksPerSm * HD * 4, 256);
   w.total = off;
@@ -175,10 +177,24 @@ gattn_status gattn_plan_create(const int32_t* indptr, const int32_t* indices, in
                 "need N >= 0 and 0 <= M < 2^31 (N=%d, M=%lld)", N, (long long)M);
   GATTN_REQUIRE(indptr != nullptr && (M == 0 || indices != nullptr), GATTN_ERR_INVALID_ARG,
                 "indptr/indices must be device pointers");
-  int T = 256, C = 256;
+  // Default threshold and chunk: the largest work item should stay small
+  // next to one warp's share of the edges (about M / (256 * SMs) edges per
+  // item keeps the longest-first schedule balanced), between 32 and 256.
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    set_error("no CUDA device: %s", cudaGetErrorString(cudaGetLastError()));
+    return GATTN_ERR_CUDA;
+  }
+  int T = 32;
+  while (T < kMaxItemEdges && int64_t(2 * T) * 256 * sms <= M) T *= 2;
+  int C = T;
   if (opts) {
     if (opts->heavy_threshold > 0) T = opts->heavy_threshold;
     if (opts->chunk > 0) C = opts->chunk;
+    GATTN_REQUIRE(T <= kMaxItemEdges && C <= kMaxItemEdges, GATTN_ERR_INVALID_ARG,
+                  "heavy_threshold and chunk must be at most %d (got %d, %d)", kMaxItemEdges, T,
+                  C);
     GATTN_REQUIRE(opts->tile_enable == 0, GATTN_ERR_UNSUPPORTED,
                   "the dense-tile path is not available in this build");
   }
@@ -189,12 +205,8 @@ gattn_status gattn_plan_create(const int32_t* indptr, const int32_t* indices, in
   p.M = M;
   p.T = T;
   p.C = C;
-  if (cudaGetDevice(&p.device) != cudaSuccess ||
-      cudaDeviceGetAttribute(&p.num_sms, cudaDevAttrMultiProcessorCount, p.device) != cudaSuccess) {
-    set_error("no CUDA device: %s", cudaGetErrorString(cudaGetLastError()));
-    delete h;
-    return GATTN_ERR_CUDA;
-  }
+  p.device = dev;
+  p.num_sms = sms;
   const gattn_status s = plan_build(&p, indptr, indices, reinterpret_cast<cudaStream_t>(stream));
   if (s != GATTN_OK) {
     for (void* q : p.allocs) cudaFree(q);
@@ -322,7 +334,9 @@ gattn_status gattn_fwd(const gattn_plan* plan, int32_t H, int32_t D, gattn_dtype
                 w.total, workspace_bytes);
   char* ws = static_cast<char*>(workspace);
   f.items = p.items;
+  f.sorted = p.sorted;
   f.n_items = p.n_chunks + p.n_light;
+  f.n_chunks = p.n_chunks;
   f.indices = p.indices;
   f.Q = Q;
   f.K = K;
@@ -334,8 +348,7 @@ gattn_status gattn_fwd(const gattn_plan* plan, int32_t H, int32_t D, gattn_dtype
   f.D = D;
   f.part = reinterpret_cast<float*>(ws + w.fwd_part);
   f.pstride = w.pstride;
-  f.cnt = p.cnt_fwd;
-  f.hfirst = p.hfirst;
+  f.tree = Tree{p.parent, p.kids, p.n_chunks, p.cnt_fwd};
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if ((s = launch_fwd(dtype, rb, score->kind, f, p.num_sms, st, nullptr)) != GATTN_OK) return s;
   return launched("forward");
@@ -369,6 +382,8 @@ static gattn_status bwd_common(const gattn_plan* plan, int32_t H, int32_t D, gat
   b->a = score->a;
   b->H = H;
   b->D = D;
+  b->rows16 = (H % 4 == 0) && aligned(lse, 16);
+  b->delta16 = (H % 4 == 0);
   b->da_part = reinterpret_cast<float*>(ws + w->da_part);
   b->da_cnt = plan->p.cnt_da;
   return GATTN_OK;
@@ -399,14 +414,15 @@ gattn_status gattn_bwd_dq(const gattn_plan* plan, int32_t H, int32_t D, gattn_dt
   GATTN_REQUIRE(!gat || !da || aligned(da, 4), GATTN_ERR_INVALID_ARG, "da misaligned");
   b.O = out;
   b.items = p.items;
+  b.sorted = p.sorted;
   b.n_items = p.n_chunks + p.n_light;
+  b.n_chunks = p.n_chunks;
   b.idx = p.indices;
   b.G1 = dQ;
   b.G2 = nullptr;
   b.da = gat ? da : nullptr;
   b.part = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.dq_part);
-  b.cnt = p.cnt_dq;
-  b.hfirst = p.hfirst;
+  b.tree = Tree{p.parent, p.kids, p.n_chunks, p.cnt_dq};
   if ((s = launch_bwd_csr(dtype, rb, score->kind, b, p.num_sms, st, nullptr)) != GATTN_OK)
     return s;
   return launched("backward (CSR pass)");
@@ -427,14 +443,15 @@ gattn_status gattn_bwd_dkdv(const gattn_plan* plan, int32_t H, int32_t D, gattn_
   if (p.N == 0) return GATTN_OK;
   if ((s = check_tensor(dK, "dK")) || (s = check_tensor(dV, "dV"))) return s;
   b.items = p.items_src;
+  b.sorted = p.sorted_src;
   b.n_items = p.n_src_chunks + p.n_light_src;
+  b.n_chunks = p.n_src_chunks;
   b.idx = p.csc_dst;
   b.G1 = dK;
   b.G2 = dV;
   b.da = nullptr;
   b.part = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.dkv_part);
-  b.cnt = p.cnt_dkv;
-  b.hfirst = p.hfirst_src;
+  b.tree = Tree{p.parent_src, p.kids_src, p.n_src_chunks, p.cnt_dkv};
   if ((s = launch_bwd_csc(dtype, rb, score->kind, b, p.num_sms,
                           reinterpret_cast<cudaStream_t>(stream), nullptr)) != GATTN_OK)
     return s;

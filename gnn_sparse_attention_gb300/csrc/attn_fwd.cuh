@@ -6,271 +6,315 @@
 // each destination's in-neighbours; an online softmax keeps the running
 // statistics in registers and only a per-node log-sum-exp is written.
 //
-// One warp owns one work item: a light destination (all of its edges) or one
-// edge chunk of a heavy destination.  Per 32 edges the warp loads the source
-// ids with one coalesced read and broadcasts them by shuffle; each slot of
-// LPR lanes gathers one K row and one V row per step with 16-byte loads, U
-// steps in flight before the online-softmax update.  Scores live in base-2
-// units (q or a pre-multiplied by log2 e) so every exponential is one ex2.
-// At the end the slots' (m, l, acc) states merge by butterfly shuffles.
+// Each group of TPR lanes owns one work item (a light destination with all
+// of its edges, or one edge chunk of a heavy destination) and each lane a
+// 32-byte slice of the rows (see attn_pipe.cuh).  The item's Q row and the
+// K and V rows of its in-neighbours arrive through the warp's cp.async ring.
+// Per stage a lane scores its SE edges (packed fp32 FMAs), takes one running
+// max over them, rescales once and accumulates the values.  Scores live in
+// base-2 units (q or a pre-multiplied by log2 e), so every exponential is one
+// ex2.
 //
 // Heavy destinations: each chunk writes its unnormalised (acc, m, l) triple
-// to the workspace, fences, and bumps the node's counter; the warp that
+// to the workspace, fences, and bumps the node's counter; the group that
 // arrives last merges all chunks in chunk order (a deterministic result) and
-// resets the counter.  No warp ever waits on another.
+// resets the counter.  No lane ever waits on another.
 #pragma once
 
-#include "gattn_internal.cuh"
+#include "attn_pipe.cuh"
 
 namespace gattn {
 
 struct FwdParams {
-  const int4* items;
+  const int4* items;   // plan items (w = heavy id of a chunk)
+  const int4* sorted;  // items by decreasing length
   int64_t n_items;
+  int64_t n_chunks;    // items [0, n_chunks) are heavy chunks
   const int32_t* indices;
   const void* Q;
   const void* K;
   const void* V;
   void* out;
   float* lse;
-  const float* a;  // GATv2 [H*D]
-  float qmul;      // DOT: scale * log2(e)
-  float slope;     // GATv2 LeakyReLU slope
+  const float* a;      // GATv2 [H*D]
+  float qmul;          // DOT: scale * log2(e)
+  float slope;         // GATv2 LeakyReLU slope
   int H, D;
-  float* part;     // [n_chunks][pstride]: acc[HD], m[H], l[H]
+  float* part;         // [n_chunks + n_inner][pstride]: acc[HD], m[H], l[H]
   int pstride;
-  int32_t* cnt;    // [n_heavy]
-  const int32_t* hfirst;
+  Tree tree;           // merge trees of the heavy destinations
 };
 
-// (m, l, acc) <- combine((m, l, acc), (mo, lo, acco)), base-2 exponents.
-template <int VEC>
-__device__ __forceinline__ void softmax_combine(float& m, float& l, float* acc, float mo, float lo,
-                                                const float* acco) {
-  const float mn = fmaxf(m, mo);
-  const float base = mn == neg_inf() ? 0.f : mn;
-  const float c1 = ex2(m - base), c2 = ex2(mo - base);
-  l = l * c1 + lo * c2;
-#pragma unroll
-  for (int v = 0; v < VEC; ++v) acc[v] = acc[v] * c1 + acco[v] * c2;
-  m = mn;
-}
+template <typename T, int RB>
+struct FwdShape {
+  using L = Lay<T, RB>;
+  // Q rows of the G items, then B K rows and B V rows
+  static constexpr int STAGE = RB * (L::G + 2 * L::B);
+  static constexpr int WARP_BYTES = kStages * STAGE + L::META;
+  static constexpr int WARPS = WarpsFor<WARP_BYTES>::value;
+  static constexpr int THREADS = 32 * WARPS;
+  static constexpr int SMEM = WARPS * WARP_BYTES;
+};
 
 template <typename T, int RB, int KIND>
-__global__ void __launch_bounds__(kThreads) fwd_kernel(const FwdParams p) {
-  using L = Layout<T, RB>;
-  constexpr int VEC = L::VEC, CPL = L::CPL, LPR = L::LPR, EPW = L::EPW, U = L::U, B = L::B;
+__global__ void __launch_bounds__(FwdShape<T, RB>::THREADS) fwd_kernel(const FwdParams p) {
+  using L = Lay<T, RB>;
+  using Sh = FwdShape<T, RB>;
+  using PR = Pairs<T>;
+  constexpr int NC = L::NC, TPR = L::TPR, G = L::G, SE = L::SE, B = L::B;
+  constexpr int NCH = L::NCH, PP = PR::P, S = kStages;
   constexpr int HD = RB / (int)sizeof(T);
+  constexpr bool GAT = KIND == GATTN_SCORE_GATV2;
   constexpr unsigned FULL = 0xffffffffu;
+  extern __shared__ __align__(16) uint8_t smem[];
   const int lane = threadIdx.x & 31;
-  const int slot = lane / LPR;
-  const int rl = lane % LPR;
-  const int lph = p.D / VEC;
+  const int g = lane / TPR, t = lane % TPR;
+  const int cph = p.D * (int)sizeof(T) / 16;  // chunks per head
+  Ring<L, Sh::STAGE> ring;
+  ring.init(smem + (threadIdx.x >> 5) * Sh::WARP_BYTES);
   const char* __restrict__ Qb = static_cast<const char*>(p.Q);
   const char* __restrict__ Kb = static_cast<const char*>(p.K);
   const char* __restrict__ Vb = static_cast<const char*>(p.V);
 
-  int elem[CPL], head[CPL];
+  // this lane's chunks: global chunk t*NC + c of the row, its head, and
+  // whether the lane writes that head's per-head values
+  int elem[NC], head[NC];
+  bool hw[NC];
 #pragma unroll
-  for (int c = 0; c < CPL; ++c) {
-    elem[c] = (c * LPR + rl) * VEC;
+  for (int c = 0; c < NC; ++c) {
+    elem[c] = (t * NC + c) * (16 / (int)sizeof(T));
     head[c] = elem[c] / p.D;
+    hw[c] = ((t * NC + c) % cph) == 0;
   }
-  float av[KIND == GATTN_SCORE_GATV2 ? CPL : 1][VEC];
-  if (KIND == GATTN_SCORE_GATV2) {
+  float2 av[GAT ? NC : 1][PP];
+  if (GAT) {
 #pragma unroll
-    for (int c = 0; c < CPL; ++c)
+    for (int c = 0; c < NC; ++c)
 #pragma unroll
-      for (int v = 0; v < VEC; ++v) av[c][v] = __ldg(p.a + elem[c] + v);
+      for (int v = 0; v < PP; ++v)
+        av[c][v] = make_float2(__ldg(p.a + elem[c] + 2 * v), __ldg(p.a + elem[c] + 2 * v + 1));
   }
 
-  const int64_t warp = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
-  const int64_t nwarps = (int64_t(gridDim.x) * kThreads) >> 5;
-  for (int64_t it = warp; it < p.n_items; it += nwarps) {
-    const int4 item = p.items[it];
-    const int node = item.x, e0 = item.y, e1 = item.z, hid = item.w;
+  const int64_t warp = (int64_t(blockIdx.x) * Sh::THREADS + threadIdx.x) >> 5;
+  const int64_t nwarps = (int64_t(gridDim.x) * Sh::THREADS) >> 5;
+  BundleCursor<G, SE> cur;
+  cur.start(p.sorted, p.n_items, p.indices, warp, nwarps, ring.items, lane);
 
-    float q[CPL][VEC];
+  // row copies of stage s into its ring slot
+  auto issue = [&](int s) {
+    const int4* dsc = ring.desc_at(s);
+    const int4 dg = lane < G ? dsc[lane] : make_int4(-1, 0, 0, 0);
+    if (__shfl_sync(FULL, dg.x, 0) != -3) {
+      uint8_t* st = ring.stage_at(s);
+      const int ge = (lane / SE) & 31;
+      const int cn = __shfl_sync(FULL, dg.x >= 0 ? (dg.z & kCntMask) : 0, ge);
+      const int jv = (lane < B && lane % SE < cn) ? ring.ix_at(s)[lane] : -1;
 #pragma unroll
-    for (int c = 0; c < CPL; ++c) {
-      Cvt<T>::to_f32(ldg16(Qb + int64_t(node) * RB + elem[c] * sizeof(T)), q[c]);
-      if (KIND == GATTN_SCORE_DOT) {
-#pragma unroll
-        for (int v = 0; v < VEC; ++v) q[c][v] *= p.qmul;
+      for (int r = 0; r < NC; ++r) {  // Q rows of items that start here: G*NCH = 32*NC chunks
+        const int x = r * 32 + lane, gg = x / NCH, ch = x % NCH;
+        const int node = __shfl_sync(FULL, dg.x, gg);
+        const int fl = __shfl_sync(FULL, dg.z, gg);
+        if (node >= 0 && (fl & kFirst))
+          cp_async16(st + gg * RB + L::pos(ch) * 16, Qb + int64_t(node) * RB + ch * 16);
       }
-    }
-    float m[CPL], l[CPL], acc[CPL][VEC];
+      uint8_t* kd = st + G * RB;
+      uint8_t* vd = kd + B * RB;
 #pragma unroll
-    for (int c = 0; c < CPL; ++c) {
-      m[c] = neg_inf();
-      l[c] = 0.f;
-#pragma unroll
-      for (int v = 0; v < VEC; ++v) acc[c][v] = 0.f;
-    }
-
-    for (int eb = e0; eb < e1; eb += 32) {
-      const int nb = min(32, e1 - eb);
-      const int myj = lane < nb ? __ldg(p.indices + eb + lane) : 0;
-      for (int sb = 0; sb < nb; sb += B) {
-        uint4 kr[U][CPL], vr[U][CPL];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int eo = sb + u * EPW + slot;
-          const int j = __shfl_sync(FULL, myj, eo);
-          if (eo < nb) {
-            const int64_t row = int64_t(j) * RB;
-#pragma unroll
-            for (int c = 0; c < CPL; ++c) {
-              kr[u][c] = ldg16(Kb + row + elem[c] * sizeof(T));
-              vr[u][c] = ldg16(Vb + row + elem[c] * sizeof(T));
-            }
-          } else {
-#pragma unroll
-            for (int c = 0; c < CPL; ++c) kr[u][c] = vr[u][c] = make_uint4(0, 0, 0, 0);
-          }
-        }
-        float s[U][CPL];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-#pragma unroll
-          for (int c = 0; c < CPL; ++c) {
-            float k[VEC];
-            Cvt<T>::to_f32(kr[u][c], k);
-            float t = 0.f;
-            if (KIND == GATTN_SCORE_DOT) {
-#pragma unroll
-              for (int v = 0; v < VEC; ++v) t = fmaf(q[c][v], k[v], t);
-              t = head_sum(t, lph);
-            } else {
-#pragma unroll
-              for (int v = 0; v < VEC; ++v) {
-                const float z = q[c][v] + k[v];
-                t = fmaf(av[c][v], z > 0.f ? z : p.slope * z, t);
-              }
-              t = head_sum(t, lph) * kLog2e;
-            }
-            s[u][c] = (sb + u * EPW + slot < nb) ? t : neg_inf();
-          }
-        }
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) {
-          float mx = m[c];
-#pragma unroll
-          for (int u = 0; u < U; ++u) mx = fmaxf(mx, s[u][c]);
-          const float base = mx == neg_inf() ? 0.f : mx;
-          const float corr = ex2(m[c] - base);
-          l[c] *= corr;
-#pragma unroll
-          for (int v = 0; v < VEC; ++v) acc[c][v] *= corr;
-#pragma unroll
-          for (int u = 0; u < U; ++u) {
-            const float pu = ex2(s[u][c] - base);
-            l[c] += pu;
-            float vv[VEC];
-            Cvt<T>::to_f32(vr[u][c], vv);
-#pragma unroll
-            for (int v = 0; v < VEC; ++v) acc[c][v] = fmaf(pu, vv[v], acc[c][v]);
-          }
-          m[c] = mx;
+      for (int r = 0; r < SE * NC; ++r) {  // B*NCH = 32*SE*NC chunks of K and of V
+        const int x = r * 32 + lane, b = x / NCH, ch = x % NCH;
+        const int j = __shfl_sync(FULL, jv, b);
+        if (j >= 0) {
+          cp_async16(kd + b * RB + L::pos(ch) * 16, Kb + int64_t(j) * RB + ch * 16);
+          cp_async16(vd + b * RB + L::pos(ch) * 16, Vb + int64_t(j) * RB + ch * 16);
         }
       }
     }
+    cp_async_commit();
+  };
 
-    // merge the warp's slots
+  // prologue: indices of stages 0..S-1, then rows of stages 0..S-2
+  for (int s = 0; s < S; ++s) cur.generate(ring.desc_at(s), ring.ix_at(s), lane);
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncwarp();
+  for (int s = 0; s < S - 1; ++s) {
+    cur.generate(ring.desc_at(S + s), ring.ix_at(S + s), lane);
+    issue(s);
+  }
+
+  float2 q[NC][PP], acc[NC][PP];
+  float m[NC], l[NC];
+  for (int i = 0;; ++i) {
+    cur.generate(ring.desc_at(i + 2 * S - 1), ring.ix_at(i + 2 * S - 1), lane);
+    __syncwarp();
+    issue(i + S - 1);
+    cp_async_wait<S - 1>();
+    __syncwarp();
+    const int4* dsc = ring.desc_at(i);
+    if (dsc[0].x == -3) break;
+    const int4 d = dsc[g];
+    const bool act = d.x >= 0;
+    const int cnt = act ? (d.z & kCntMask) : 0;
+    const uint8_t* st = ring.stage_at(i);
+
+    if (act && (d.z & kFirst)) {
 #pragma unroll
-    for (int o = LPR; o < 32; o <<= 1) {
+      for (int c = 0; c < NC; ++c) {
+        PR::load(lds16(st + g * RB + (c * TPR + t) * 16), q[c]);
+        if (!GAT) {
 #pragma unroll
-      for (int c = 0; c < CPL; ++c) {
-        float acco[VEC];
+          for (int v = 0; v < PP; ++v) q[c][v] = f2mul(q[c][v], f2s(p.qmul));
+        }
+        m[c] = neg_inf();
+        l[c] = 0.f;
 #pragma unroll
-        for (int v = 0; v < VEC; ++v) acco[v] = __shfl_xor_sync(FULL, acc[c][v], o);
-        const float mo = __shfl_xor_sync(FULL, m[c], o);
-        const float lo = __shfl_xor_sync(FULL, l[c], o);
-        softmax_combine<VEC>(m[c], l[c], acc[c], mo, lo, acco);
+        for (int v = 0; v < PP; ++v) acc[c][v] = f2s(0.f);
       }
     }
 
-    bool write_final = hid < 0;
-    if (!write_final) {
-      // heavy chunk: publish the partial, the last chunk to arrive merges
-      float* pb = p.part + it * int64_t(p.pstride);
-      if (slot == 0) {
+    const uint8_t* ks = st + G * RB + g * SE * RB;
+    const uint8_t* vs = ks + B * RB;
+    const int kmax = __reduce_max_sync(FULL, cnt);  // edges of the warp's longest item here
+    float sc[SE][NC];
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) {
-          float4* dst = reinterpret_cast<float4*>(pb + elem[c]);
+    for (int k = 0; k < SE; ++k) {
+      if (k >= kmax) break;
 #pragma unroll
-          for (int v = 0; v < VEC; v += 4)
-            dst[v / 4] = make_float4(acc[c][v], acc[c][v + 1], acc[c][v + 2], acc[c][v + 3]);
-          if (rl % lph == 0) {
+      for (int c = 0; c < NC; ++c) {
+        const uint4 kr = k < cnt ? lds16(ks + k * RB + (c * TPR + t) * 16) : make_uint4(0, 0, 0, 0);
+        float2 kf[PP];
+        PR::load(kr, kf);
+        float2 a2 = f2s(0.f);
+        if (!GAT) {
+#pragma unroll
+          for (int v = 0; v < PP; ++v) a2 = f2fma(q[c][v], kf[v], a2);
+        } else {
+#pragma unroll
+          for (int v = 0; v < PP; ++v) {
+            const float2 z = make_float2(q[c][v].x + kf[v].x, q[c][v].y + kf[v].y);
+            const float2 lr = make_float2(z.x > 0.f ? z.x : p.slope * z.x,
+                                          z.y > 0.f ? z.y : p.slope * z.y);
+            a2 = f2fma(av[c][v], lr, a2);
+          }
+        }
+        sc[k][c] = a2.x + a2.y;
+      }
+      head_totals<NC>(sc[k], cph);
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        if (GAT) sc[k][c] *= kLog2e;
+        if (k >= cnt) sc[k][c] = neg_inf();
+      }
+    }
+    if (act) {
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        float mx = m[c];
+#pragma unroll
+        for (int k = 0; k < SE; ++k)
+          if (k < cnt) mx = fmaxf(mx, sc[k][c]);
+        const float base = mx == neg_inf() ? 0.f : mx;
+        const float corr = ex2(m[c] - base);
+        l[c] *= corr;
+#pragma unroll
+        for (int v = 0; v < PP; ++v) acc[c][v] = f2mul(acc[c][v], f2s(corr));
+#pragma unroll
+        for (int k = 0; k < SE; ++k) {
+          if (k < cnt) {
+            const float pk = ex2(sc[k][c] - base);
+            l[c] += pk;
+            float2 vf[PP];
+            PR::load(lds16(vs + k * RB + (c * TPR + t) * 16), vf);
+#pragma unroll
+            for (int v = 0; v < PP; ++v) acc[c][v] = f2fma(f2s(pk), vf[v], acc[c][v]);
+          }
+        }
+        m[c] = mx;
+      }
+    }
+
+    // items that end in this stage; heavy chunks climb their node's merge tree
+    const bool fin = act && (d.z & kLast);
+    const bool heavy = fin && d.y < p.n_chunks;
+    bool write = fin && !heavy;
+    if (heavy) {
+      auto store = [&](int slot) {
+        float* pb = p.part + int64_t(slot) * p.pstride;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+#pragma unroll
+          for (int v = 0; v < PP; v += 2)
+            *reinterpret_cast<float4*>(pb + elem[c] + 2 * v) =
+                make_float4(acc[c][v].x, acc[c][v].y, acc[c][v + 1].x, acc[c][v + 1].y);
+          if (hw[c]) {
             pb[HD + head[c]] = m[c];
             pb[HD + p.H + head[c]] = l[c];
           }
         }
-      }
-      __threadfence();
-      __syncwarp();
-      int old = 0;
-      if (lane == 0) old = atomicAdd(p.cnt + hid, 1);
-      old = __shfl_sync(FULL, old, 0);
-      const int first = p.hfirst[hid];
-      const int n = p.hfirst[hid + 1] - first;
-      if (old == n - 1) {
-        __threadfence();
+      };
+      auto merge = [&](int c0, int cn) {
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) {
+        for (int c = 0; c < NC; ++c) {
           m[c] = neg_inf();
           l[c] = 0.f;
 #pragma unroll
-          for (int v = 0; v < VEC; ++v) acc[c][v] = 0.f;
+          for (int v = 0; v < PP; ++v) acc[c][v] = f2s(0.f);
         }
-        for (int k = slot; k < n; k += EPW) {
-          const float* pc = p.part + int64_t(first + k) * p.pstride;
+        for (int kk = 0; kk < cn; kk += 4) {  // four children's loads in flight at a time
+          float mo[4][NC], lo[4][NC];
+          float4 f[4][NC][PP / 2];
 #pragma unroll
-          for (int c = 0; c < CPL; ++c) {
-            float acco[VEC];
+          for (int j = 0; j < 4; ++j) {
+            const bool ok = kk + j < cn;
+            const float* pc = p.part + int64_t(c0 + (ok ? kk + j : 0)) * p.pstride;
 #pragma unroll
-            for (int v = 0; v < VEC; v += 4) {
-              const float4 f = __ldcg(reinterpret_cast<const float4*>(pc + elem[c] + v));
-              acco[v] = f.x;
-              acco[v + 1] = f.y;
-              acco[v + 2] = f.z;
-              acco[v + 3] = f.w;
+            for (int c = 0; c < NC; ++c) {
+              mo[j][c] = ok ? __ldcg(pc + HD + head[c]) : neg_inf();
+              lo[j][c] = ok ? __ldcg(pc + HD + p.H + head[c]) : 0.f;
+#pragma unroll
+              for (int v = 0; v < PP / 2; ++v)
+                f[j][c][v] = ok ? __ldcg(reinterpret_cast<const float4*>(pc + elem[c] + 4 * v))
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
             }
-            const float mo = __ldcg(pc + HD + head[c]);
-            const float lo = __ldcg(pc + HD + p.H + head[c]);
-            softmax_combine<VEC>(m[c], l[c], acc[c], mo, lo, acco);
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+              const float mn = fmaxf(m[c], mo[j][c]);
+              const float base = mn == neg_inf() ? 0.f : mn;
+              const float c1 = ex2(m[c] - base), c2 = ex2(mo[j][c] - base);
+              l[c] = l[c] * c1 + lo[j][c] * c2;
+#pragma unroll
+              for (int v = 0; v < PP / 2; ++v) {
+                acc[c][2 * v] = f2fma(acc[c][2 * v], f2s(c1),
+                                      f2mul(make_float2(f[j][c][v].x, f[j][c][v].y), f2s(c2)));
+                acc[c][2 * v + 1] = f2fma(acc[c][2 * v + 1], f2s(c1),
+                                          f2mul(make_float2(f[j][c][v].z, f[j][c][v].w), f2s(c2)));
+              }
+              m[c] = mn;
+            }
           }
         }
-#pragma unroll
-        for (int o = LPR; o < 32; o <<= 1) {
-#pragma unroll
-          for (int c = 0; c < CPL; ++c) {
-            float acco[VEC];
-#pragma unroll
-            for (int v = 0; v < VEC; ++v) acco[v] = __shfl_xor_sync(FULL, acc[c][v], o);
-            const float mo = __shfl_xor_sync(FULL, m[c], o);
-            const float lo = __shfl_xor_sync(FULL, l[c], o);
-            softmax_combine<VEC>(m[c], l[c], acc[c], mo, lo, acco);
-          }
-        }
-        if (lane == 0) p.cnt[hid] = 0;
-        write_final = true;
-      }
+      };
+      write = climb(p.tree, d.y, group_mask<TPR>(g), g * TPR, t == 0, merge, store);
     }
-    if (write_final && slot == 0) {
-      char* ob = static_cast<char*>(p.out) + int64_t(node) * RB;
+    if (write) {
+      char* ob = static_cast<char*>(p.out) + int64_t(d.x) * RB;
 #pragma unroll
-      for (int c = 0; c < CPL; ++c) {
+      for (int c = 0; c < NC; ++c) {
         const float inv = l[c] > 0.f ? 1.f / l[c] : 0.f;
-        float o[VEC];
+        float2 o[PP];
 #pragma unroll
-        for (int v = 0; v < VEC; ++v) o[v] = acc[c][v] * inv;
-        *reinterpret_cast<uint4*>(ob + elem[c] * sizeof(T)) = Cvt<T>::from_f32(o);
-        if (rl % lph == 0)
-          p.lse[int64_t(node) * p.H + head[c]] = l[c] > 0.f ? (m[c] + lg2(l[c])) * kLn2 : neg_inf();
+        for (int v = 0; v < PP; ++v) o[v] = f2mul(acc[c][v], f2s(inv));
+        *reinterpret_cast<uint4*>(ob + (t * NC + c) * 16) = PR::store(o);
+        if (hw[c])
+          p.lse[int64_t(d.x) * p.H + head[c]] = l[c] > 0.f ? (m[c] + lg2(l[c])) * kLn2 : neg_inf();
       }
     }
+    __syncwarp();
   }
+  cp_async_wait<0>();
 }
 
 }  // namespace gattn

@@ -9,16 +9,27 @@
 
 namespace gattn {
 
-// Grid of a persistent kernel: every SM gets as many 256-thread blocks as fit
-// (capped at kMaxBlocksPerSm), but never more blocks than work items need.
+// Blocks per SM of a persistent kernel with `smem` bytes of dynamic shared
+// memory (the attribute that allows more than 48 KB is set on first use).
+// Cached per kernel: the first call of each instantiation does the queries.
 template <typename Kern>
-int persistent_grid(Kern kernel, int num_sms, int64_t n_items) {
+int blocks_per_sm(Kern kernel, int threads, int smem, int* cache) {
+  if (*cache > 0) return *cache;
   int bps = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kernel, kThreads, 0) != cudaSuccess ||
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kernel, threads, smem) != cudaSuccess ||
       bps < 1)
     bps = 1;
   if (bps > kMaxBlocksPerSm) bps = kMaxBlocksPerSm;
-  const int64_t need = (n_items + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  *cache = bps;
+  return bps;
+}
+
+// Grid of a persistent kernel: every SM gets as many blocks as fit, but
+// never more blocks than there are work items for their warps.
+inline int persistent_grid(int bps, int warps_per_block, int num_sms, int64_t n_items) {
+  const int64_t need = (n_items + warps_per_block - 1) / warps_per_block;
   int64_t g = int64_t(num_sms) * bps;
   if (g > need) g = need;
   return (int)(g < 1 ? 1 : g);
@@ -32,11 +43,14 @@ struct Launch {
                           int* grid_out) {
 #define GATTN_FWD_CASE(RB_)                                                        \
   case RB_: {                                                                      \
-    auto k = kind == GATTN_SCORE_DOT ? fwd_kernel<T, RB_, GATTN_SCORE_DOT>         \
-                                     : fwd_kernel<T, RB_, GATTN_SCORE_GATV2>;      \
-    const int g = persistent_grid(k, num_sms, p.n_items);                          \
-    if (grid_out) *grid_out = g;                                                   \
-    k<<<g, kThreads, 0, st>>>(p);                                                  \
+    using Sh = FwdShape<T, RB_>;                                                          \
+    static int cache[2] = {0, 0};                                                    \
+    auto k = kind == GATTN_SCORE_DOT ? fwd_kernel<T, RB_, GATTN_SCORE_DOT>                    \
+                                     : fwd_kernel<T, RB_, GATTN_SCORE_GATV2>;                 \
+    const int bps = blocks_per_sm(k, Sh::THREADS, Sh::SMEM, &cache[kind != 0]);       \
+    const int g = persistent_grid(bps, Sh::WARPS, num_sms, (p.n_items + kUnit - 1) / kUnit);               \
+    if (grid_out) *grid_out = g;                                                     \
+    k<<<g, Sh::THREADS, Sh::SMEM, st>>>(p);                                          \
     return GATTN_OK;                                                               \
   }
     switch (rb) { GATTN_RB_CASES(GATTN_FWD_CASE) default: return GATTN_ERR_UNSUPPORTED; }
@@ -46,11 +60,14 @@ struct Launch {
                               int* grid_out) {
 #define GATTN_CSR_CASE(RB_)                                                         \
   case RB_: {                                                                       \
-    auto k = kind == GATTN_SCORE_DOT ? bwd_csr_kernel<T, RB_, GATTN_SCORE_DOT>      \
-                                     : bwd_csr_kernel<T, RB_, GATTN_SCORE_GATV2>;   \
-    const int g = persistent_grid(k, num_sms, p.n_items);                           \
-    if (grid_out) *grid_out = g;                                                    \
-    k<<<g, kThreads, 0, st>>>(p);                                                   \
+    using Sh = CsrShape<T, RB_>;                                                          \
+    static int cache[2] = {0, 0};                                                    \
+    auto k = kind == GATTN_SCORE_DOT ? bwd_csr_kernel<T, RB_, GATTN_SCORE_DOT>                    \
+                                     : bwd_csr_kernel<T, RB_, GATTN_SCORE_GATV2>;                 \
+    const int bps = blocks_per_sm(k, Sh::THREADS, Sh::SMEM, &cache[kind != 0]);       \
+    const int g = persistent_grid(bps, Sh::WARPS, num_sms, (p.n_items + kUnit - 1) / kUnit);               \
+    if (grid_out) *grid_out = g;                                                     \
+    k<<<g, Sh::THREADS, Sh::SMEM, st>>>(p);                                          \
     return GATTN_OK;                                                                \
   }
     switch (rb) { GATTN_RB_CASES(GATTN_CSR_CASE) default: return GATTN_ERR_UNSUPPORTED; }
@@ -60,11 +77,14 @@ struct Launch {
                               int* grid_out) {
 #define GATTN_CSC_CASE(RB_)                                                         \
   case RB_: {                                                                       \
-    auto k = kind == GATTN_SCORE_DOT ? bwd_csc_kernel<T, RB_, GATTN_SCORE_DOT>      \
-                                     : bwd_csc_kernel<T, RB_, GATTN_SCORE_GATV2>;   \
-    const int g = persistent_grid(k, num_sms, p.n_items);                           \
-    if (grid_out) *grid_out = g;                                                    \
-    k<<<g, kThreads, 0, st>>>(p);                                                   \
+    using Sh = CscShape<T, RB_>;                                                          \
+    static int cache[2] = {0, 0};                                                    \
+    auto k = kind == GATTN_SCORE_DOT ? bwd_csc_kernel<T, RB_, GATTN_SCORE_DOT>                    \
+                                     : bwd_csc_kernel<T, RB_, GATTN_SCORE_GATV2>;                 \
+    const int bps = blocks_per_sm(k, Sh::THREADS, Sh::SMEM, &cache[kind != 0]);       \
+    const int g = persistent_grid(bps, Sh::WARPS, num_sms, (p.n_items + kUnit - 1) / kUnit);               \
+    if (grid_out) *grid_out = g;                                                     \
+    k<<<g, Sh::THREADS, Sh::SMEM, st>>>(p);                                          \
     return GATTN_OK;                                                                \
   }
     switch (rb) { GATTN_RB_CASES(GATTN_CSC_CASE) default: return GATTN_ERR_UNSUPPORTED; }

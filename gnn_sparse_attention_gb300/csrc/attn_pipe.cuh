@@ -1,0 +1,322 @@
+// attn_pipe.cuh -- thread layout and the per-warp asynchronous gather
+// pipeline shared by the attention kernels.
+//
+// Thread layout.  A row (the H*D values of one node, RB bytes) is cut into
+// TPR slices of PT = 32 bytes (64 for 2 KB rows); thread t of a group of TPR
+// lanes owns slice t, i.e. NC consecutive 16-byte chunks.  A warp holds
+// G = 32 / TPR groups and every group works on its OWN work item, so a warp
+// advances G items at once (G = 4 for 256-byte rows).  A head whose D values
+// fit in one slice needs no shuffle for its score; wider heads reduce over
+// the lanes that share them.
+//
+// Degree binning.  The plan lists the work items (light nodes, heavy-node
+// edge chunks) by decreasing edge count, so the G items of a bundle
+// (consecutive items of that list) have (almost) equal length and their
+// groups run in lockstep.
+//
+// Pipeline (one per warp, three levels, no inter-warp waits):
+//   units  : 32 consecutive sorted items; the NEXT unit of the warp is loaded
+//            into registers (one item per lane) when the current one starts,
+//            and stored to shared memory when it becomes current;
+//   indices: stage t's descriptors (one per group: node, item, edge count,
+//            FIRST/LAST flags) are generated and its source indices copied
+//            (cp.async) 2S - 1 stages before t is computed;
+//   rows   : stage t's rows (Q/K/V or their gradients' operands) are copied
+//            (cp.async, 16-byte pieces) S - 1 stages before t is computed.
+// A stage holds SE edges of each of the G items; its rows land in shared
+// memory with each thread's chunks placed so that the G groups' reads of one
+// chunk index are conflict-free.  cp.async.wait_group is a hardware wait on
+// the thread's own copies, so nothing ever spins.
+#pragma once
+
+#include "gattn_internal.cuh"
+
+namespace gattn {
+
+constexpr int kStages = 3;           // row stages in flight + 1
+constexpr int kRing = 2 * kStages;   // descriptor / index ring entries
+constexpr int kUnit = 32;            // items per unit
+constexpr int kFirst = 1 << 29;
+constexpr int kLast = 1 << 30;
+constexpr int kCntMask = 0xffff;
+constexpr int kSmemPerSm = 227 * 1024;
+
+template <typename T, int RB>
+struct Lay {
+  static constexpr int VEC = 16 / (int)sizeof(T);  // elements per 16-byte chunk
+  static constexpr int PT = RB <= 1024 ? 32 : RB / 32;
+  static constexpr int NC = PT / 16;                // chunks per thread
+  static constexpr int VP = NC * VEC / 2;           // float2 pairs per thread
+  static constexpr int TPR = RB / PT;               // threads per row
+  static constexpr int G = 32 / TPR;                // groups (items) per warp
+  static constexpr int NCH = RB / 16;               // chunks per row
+  // edges per item per stage: ~8 KB of gathered rows per stage
+  static constexpr int SE0 = 8192 / (2 * RB) / G;
+  static constexpr int SE1 = SE0 < 1 ? 1 : SE0;
+  static constexpr int SE = SE1 * G > 32 ? 32 / G : SE1;  // at most 32 edges per stage
+  static constexpr int B = G * SE;                  // edges per stage
+  static constexpr int IDXB = (B * 4 + 15) / 16 * 16;
+  // the warp's descriptor ring, index ring and unit buffer
+  static constexpr int META = kRing * G * 16 + kRing * IDXB + kUnit * 16;
+  static_assert(TPR >= 1 && TPR <= 32 && 32 % TPR == 0, "thread layout");
+  static_assert(B <= 32, "stage edges");
+  // shared-memory position (in 16-byte units) of global chunk ch of a row
+  __device__ __forceinline__ static int pos(int ch) { return (ch % NC) * TPR + ch / NC; }
+};
+
+// Warps per block: as many as keep a block under a quarter of the SM's shared
+// memory (so that several blocks fit), between 1 and 8.
+template <int WARP_BYTES>
+struct WarpsFor {
+  static constexpr int raw = (kSmemPerSm / 4) / WARP_BYTES;
+  static constexpr int value = raw < 1 ? 1 : (raw > 8 ? 8 : raw);
+};
+
+// ---------------------------------------------------------------------------
+// async copies
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint4 lds16(const void* p) {
+  return *reinterpret_cast<const uint4*>(p);
+}
+
+// ---------------------------------------------------------------------------
+// 16-byte chunk <-> float2 pairs
+// ---------------------------------------------------------------------------
+template <typename T>
+struct Pairs;
+
+template <>
+struct Pairs<__nv_bfloat16> {
+  static constexpr int P = 4;  // pairs per chunk
+  __device__ __forceinline__ static void load(const uint4& u, float2* f) {
+    f[0] = make_float2(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u));
+    f[1] = make_float2(__uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+    f[2] = make_float2(__uint_as_float(u.z << 16), __uint_as_float(u.z & 0xffff0000u));
+    f[3] = make_float2(__uint_as_float(u.w << 16), __uint_as_float(u.w & 0xffff0000u));
+  }
+  __device__ __forceinline__ static uint32_t pack(float2 v) {
+    __nv_bfloat162 b = __floats2bfloat162_rn(v.x, v.y);  // round to nearest even
+    return *reinterpret_cast<uint32_t*>(&b);
+  }
+  __device__ __forceinline__ static uint4 store(const float2* f) {
+    return make_uint4(pack(f[0]), pack(f[1]), pack(f[2]), pack(f[3]));
+  }
+};
+
+template <>
+struct Pairs<float> {
+  static constexpr int P = 2;
+  __device__ __forceinline__ static void load(const uint4& u, float2* f) {
+    f[0] = make_float2(__uint_as_float(u.x), __uint_as_float(u.y));
+    f[1] = make_float2(__uint_as_float(u.z), __uint_as_float(u.w));
+  }
+  __device__ __forceinline__ static uint4 store(const float2* f) {
+    return make_uint4(__float_as_uint(f[0].x), __float_as_uint(f[0].y), __float_as_uint(f[1].x),
+                      __float_as_uint(f[1].y));
+  }
+};
+
+__device__ __forceinline__ float2 f2fma(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 f2mul(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 f2s(float s) { return make_float2(s, s); }
+
+// Combine per-chunk partial sums into per-head totals.  cph = chunks per
+// head (D / VEC, runtime).  Chunks of one thread that share a head are
+// summed in-thread; heads wider than a thread reduce over tph lanes.
+// Every lane of the warp must call this (it may shuffle).
+template <int NC>
+__device__ __forceinline__ void head_totals(float* x, int cph) {
+  if (cph == 1) return;
+  if (NC == 2 || cph >= NC) {
+    float s = 0.f;
+#pragma unroll
+    for (int c = 0; c < NC; ++c) s += x[c];
+    const int tph = cph / NC;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1)
+      if (o < tph) s += __shfl_xor_sync(0xffffffffu, s, o);
+#pragma unroll
+    for (int c = 0; c < NC; ++c) x[c] = s;
+  } else {  // NC == 4, cph == 2
+    const float a = x[0] + x[1], b = x[2] + x[3];
+    x[0] = x[1] = a;
+    x[2] = x[3] = b;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// the warp's cursor: bundles -> stages
+// ---------------------------------------------------------------------------
+// Bundle b is sorted items [b*G, b*G + G).  Bundles go to the W warps of the
+// grid in rounds, in snake order (round r: bundles rW .. rW + W - 1, to warps
+// 0..W-1 on even rounds and W-1..0 on odd ones).  With bundles sorted by
+// decreasing length this is the classic longest-first greedy schedule: every
+// warp ends up with nearly the same number of edges, deterministically and
+// without atomics.  A warp's next 32/G bundles (one item per lane) are loaded
+// into registers one such block ahead of use.
+template <int G, int SE>
+struct BundleCursor {
+  static constexpr int B = G * SE;
+  static constexpr int R = kUnit / G;  // bundles per block
+  const int4* sorted;     // items by decreasing length: (node, e0, e1, item index)
+  const int32_t* idx;     // CSR sources (or CSC destinations)
+  int64_t n_items, n_bundles, W, w, r_next;
+  int4* s_items;          // [kUnit] current block of bundles, shared memory
+  int4 pf;                // next block's item of this lane
+  bool live;
+  int bi, off, maxlen;
+
+  __device__ __forceinline__ int64_t bundle_of(int64_t r) const {
+    return r * W + ((r & 1) ? (W - 1 - w) : w);
+  }
+  __device__ __forceinline__ void prefetch(int lane) {
+    const int64_t b = bundle_of(r_next + lane / G);
+    const int64_t i = b * G + lane % G;
+    pf = (b < n_bundles && i < n_items) ? sorted[i] : make_int4(-1, 0, 0, -1);
+  }
+  __device__ __forceinline__ void advance(int lane) {
+    __syncwarp();
+    live = bundle_of(r_next) < n_bundles;
+    if (live) {
+      s_items[lane] = pf;
+      bi = 0;
+      off = 0;
+      r_next += R;
+      prefetch(lane);
+    }
+    __syncwarp();
+    if (live) maxlen = s_items[0].z - s_items[0].y;
+  }
+  __device__ __forceinline__ void start(const int4* sorted_, int64_t n_items_, const int32_t* idx_,
+                                        int64_t warp, int64_t nwarps, int4* s_items_, int lane) {
+    sorted = sorted_;
+    idx = idx_;
+    n_items = n_items_;
+    n_bundles = (n_items_ + G - 1) / G;
+    W = nwarps;
+    w = warp;
+    r_next = 0;
+    s_items = s_items_;
+    prefetch(lane);
+    advance(lane);
+  }
+
+  // Generate the next stage into ring slot (desc[G], ix[B]): lane g < G
+  // writes group g's descriptor {node (-1 idle, -3 end), item, count|flags,
+  // first edge}; lanes b < B copy the stage's source indices.
+  __device__ __forceinline__ void generate(int4* desc, int* ix, int lane) {
+    constexpr unsigned FULL = 0xffffffffu;
+    int4 d = make_int4(-1, 0, 0, 0);
+    if (!live) {
+      if (lane < G) desc[lane] = make_int4(-3, 0, 0, 0);
+      return;
+    }
+    if (lane < G) {
+      const int4 it = s_items[bi + lane];
+      const int len = it.z - it.y;
+      if (it.x >= 0 && (off < len || (off == 0 && len == 0))) {
+        const int cnt = min(SE, len - off);
+        const int fl = (off == 0 ? kFirst : 0) | (off + SE >= len ? kLast : 0);
+        d = make_int4(it.x, it.w, cnt | fl, it.y + off);
+      }
+      desc[lane] = d;
+    }
+    const int g = (lane / SE) & 31, k = lane % SE;
+    const int es = __shfl_sync(FULL, d.w, g);
+    const int cn = __shfl_sync(FULL, d.x >= 0 ? (d.z & kCntMask) : 0, g);
+    if (lane < B && k < cn) cp_async4(ix + lane, idx + es + k);
+    off += SE;
+    if (off >= maxlen) {
+      bi += G;
+      off = 0;
+      // the rest of a block is empty once one of its bundles is
+      if (bi >= kUnit || s_items[bi].x < 0) advance(lane);
+      else maxlen = s_items[bi].z - s_items[bi].y;
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
+// merge trees of heavy nodes
+// ---------------------------------------------------------------------------
+// Lanes of group g (TPR consecutive lanes) as a shuffle mask.
+template <int TPR>
+__device__ __forceinline__ unsigned group_mask(int g) {
+  return TPR == 32 ? 0xffffffffu : (((1u << TPR) - 1u) << (g * TPR));
+}
+
+struct Tree {
+  const int32_t* parent;  // [n_leaves + n_inner], -1 at a root
+  const int2* kids;       // [n_inner]: (first child slot, count)
+  int64_t n_leaves;       // slots [0, n_leaves) are the chunks
+  int32_t* cnt;           // [n_inner] arrivals, zero between calls
+};
+
+// Climb the merge tree from leaf `slot` with the group's partial state.
+// While the slot has a parent: store(slot) publishes the state, the group
+// fences and counts its arrival at the parent; the group that arrives last
+// loads the parent's children (merge(first, count), in slot order) into its
+// state and continues from the parent.  Returns true for the one group that
+// ends at the root holding the complete result.  Called by all lanes of a
+// group and by no other lane; nothing waits.
+template <class Merge, class Store>
+__device__ __forceinline__ bool climb(const Tree& tr, int slot, unsigned gmask, int leader,
+                                      bool is_leader, Merge merge, Store store) {
+  for (;;) {
+    const int par = tr.parent[slot];
+    if (par < 0) return true;
+    store(slot);
+    __threadfence();
+    __syncwarp(gmask);
+    int old = 0;
+    if (is_leader) old = atomicAdd(tr.cnt + (par - tr.n_leaves), 1);
+    old = __shfl_sync(gmask, old, leader);
+    const int2 kd = tr.kids[par - tr.n_leaves];
+    if (old != kd.y - 1) return false;
+    __threadfence();
+    merge(kd.x, kd.y);
+    __syncwarp(gmask);
+    if (is_leader) tr.cnt[par - tr.n_leaves] = 0;
+    slot = par;
+  }
+}
+
+// Per-warp ring bookkeeping shared by the kernels' main loops.
+template <typename L, int STAGE>
+struct Ring {
+  uint8_t* data;  // [kStages][STAGE]
+  int4* desc;     // [kRing][G]
+  uint8_t* ix;    // [kRing][IDXB]
+  int4* items;    // [kUnit]
+  __device__ __forceinline__ void init(uint8_t* base) {
+    data = base;
+    desc = reinterpret_cast<int4*>(base + kStages * STAGE);
+    ix = reinterpret_cast<uint8_t*>(desc + kRing * L::G);
+    items = reinterpret_cast<int4*>(ix + kRing * L::IDXB);
+  }
+  __device__ __forceinline__ int4* desc_at(int t) { return desc + (t % kRing) * L::G; }
+  __device__ __forceinline__ int* ix_at(int t) {
+    return reinterpret_cast<int*>(ix + (t % kRing) * L::IDXB);
+  }
+  __device__ __forceinline__ uint8_t* stage_at(int t) { return data + (t % kStages) * STAGE; }
+};
+
+}  // namespace gattn

@@ -46,6 +46,15 @@ struct Plan {
   int32_t* light = nullptr;    // [N] capacity
   int4* items = nullptr;       // [n_chunks + n_light]: chunks first (w = heavy id), then light (w = -1)
   int32_t* hfirst = nullptr;   // [n_heavy + 1] first chunk (item index) of each heavy node
+  int4* units = nullptr;       // [n_units]: (item_begin, item_end, edge_begin, edge_end)
+  int64_t n_units = 0;
+  int4* sorted = nullptr;      // items by decreasing edge count: (node, e0, e1, item index)
+  // merge tree of the heavy chunks: slots [0, n_chunks) are the chunks,
+  // slots [n_chunks, n_chunks + n_inner) the inner nodes of every heavy
+  // node's tree; parent[s] = -1 at a root
+  int32_t* parent = nullptr;   // [n_chunks + n_inner]
+  int2* kids = nullptr;        // [n_inner]: (first child slot, child count)
+  int64_t n_inner = 0;
   // CSC side
   int32_t* indptrT = nullptr;  // [N+1]
   int32_t* csc_dst = nullptr;  // [M]
@@ -55,15 +64,31 @@ struct Plan {
   int32_t* light_src = nullptr;
   int4* items_src = nullptr;
   int32_t* hfirst_src = nullptr;
+  int4* units_src = nullptr;
+  int64_t n_units_src = 0;
+  int4* sorted_src = nullptr;
+  int32_t* parent_src = nullptr;
+  int2* kids_src = nullptr;
+  int64_t n_inner_src = 0;
   // last-arriver counters (zero between calls; the merging warp resets them)
-  int32_t* cnt_fwd = nullptr;  // [n_heavy]
-  int32_t* cnt_dq = nullptr;   // [n_heavy]
-  int32_t* cnt_dkv = nullptr;  // [n_heavy_src]
+  int32_t* cnt_fwd = nullptr;  // [n_inner]
+  int32_t* cnt_dq = nullptr;   // [n_inner]
+  int32_t* cnt_dkv = nullptr;  // [n_inner_src]
   int32_t* cnt_da = nullptr;   // [1]
   std::vector<void*> allocs;   // every device buffer above, freed by destroy
 };
 
 constexpr int kMaxBlocksPerSm = 8;  // grid cap of the persistent kernels (bounds da partials)
+
+// Work units: runs of consecutive items whose edges are contiguous, at most
+// kUnitItems items, all starting inside one kUnitBucket-edge bucket of the
+// item list's edge prefix.  With items of at most kMaxItemEdges edges a unit
+// spans at most kUnitEdges edges.
+constexpr int kUnitItems = 32;
+constexpr int kUnitBucket = 128;
+constexpr int kMaxItemEdges = 256;
+constexpr int kUnitEdges = kUnitBucket + kMaxItemEdges;
+constexpr int kTreeFanIn = 16;  // children per inner node of a chunk merge tree
 
 // ---------------------------------------------------------------------------
 // lane layout

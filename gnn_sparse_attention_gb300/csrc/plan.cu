@@ -128,6 +128,105 @@ __global__ void k_fill_items(const int32_t* __restrict__ ptr, int32_t N, int32_t
   if (blockIdx.x == 0 && threadIdx.x == 0) hfirst[n_heavy] = (int32_t)n_chunks;
 }
 
+// Item edge counts (for the unit segmentation).
+__global__ void k_item_edges(const int4* __restrict__ items, int64_t n, int32_t* __restrict__ len) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i <= n; i += stride)
+    len[i] = i < n ? items[i].z - items[i].y : 0;
+}
+
+// Unit starts: item 0, every multiple of kUnitItems, a new kUnitBucket edge
+// bucket of the exclusive edge prefix, or a gap in the edge ranges.
+__global__ void k_unit_flags(const int4* __restrict__ items, int64_t n,
+                             const int32_t* __restrict__ epre, int32_t* __restrict__ flag) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i <= n; i += stride) {
+    if (i == n) {
+      flag[n] = 0;
+      continue;
+    }
+    bool f = i == 0 || (i % kUnitItems) == 0 || epre[i] / kUnitBucket != epre[i - 1] / kUnitBucket ||
+             items[i].y != items[i - 1].z;
+    flag[i] = f ? 1 : 0;
+  }
+}
+
+__global__ void k_fill_units(const int4* __restrict__ items, int64_t n,
+                             const int32_t* __restrict__ flag, const int32_t* __restrict__ upos,
+                             int4* __restrict__ units) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    if (!flag[i]) continue;
+    int64_t e = i + 1;
+    while (e < n && !flag[e]) ++e;  // at most kUnitItems - 1 steps
+    units[upos[i]] = make_int4((int)i, (int)e, items[i].y, items[e - 1].z);
+  }
+}
+
+// Merge trees over the chunks of every heavy node (fan-in kTreeFanIn).
+__device__ __forceinline__ int32_t tree_inner(int32_t n) {
+  int32_t total = 0;
+  while (n > 1) {
+    n = (n + kTreeFanIn - 1) / kTreeFanIn;
+    total += n;
+  }
+  return total;
+}
+
+__global__ void k_tree_sizes(const int32_t* __restrict__ hfirst, int64_t n_heavy,
+                             int32_t* __restrict__ inner) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t h = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; h <= n_heavy; h += stride)
+    inner[h] = h < n_heavy ? tree_inner(hfirst[h + 1] - hfirst[h]) : 0;
+}
+
+// One thread per heavy node builds its tree level by level: the children of
+// inner node p of a level are consecutive slots of the level below.
+__global__ void k_tree_fill(const int32_t* __restrict__ hfirst, int64_t n_heavy, int64_t n_chunks,
+                            const int32_t* __restrict__ inner_pos, int32_t* __restrict__ parent,
+                            int2* __restrict__ kids) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t h = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; h < n_heavy; h += stride) {
+    int32_t lo = hfirst[h], n = hfirst[h + 1] - hfirst[h];
+    int32_t next = (int32_t)n_chunks + inner_pos[h];  // next free inner slot
+    if (n == 1) parent[lo] = -1;
+    while (n > 1) {
+      const int32_t m = (n + kTreeFanIn - 1) / kTreeFanIn;
+      for (int32_t q = 0; q < m; ++q) {
+        const int32_t c0 = lo + q * kTreeFanIn;
+        const int32_t cn = min(kTreeFanIn, n - q * kTreeFanIn);
+        kids[next + q - n_chunks] = make_int2(c0, cn);
+        for (int32_t c = 0; c < cn; ++c) parent[c0 + c] = next + q;
+      }
+      if (m == 1) parent[next] = -1;
+      lo = next;
+      next += m;
+      n = m;
+    }
+  }
+}
+
+// Degree binning of the work items: key = kMaxItemEdges - edge count, so a
+// stable ascending sort lists items by decreasing length, ties in item order.
+__global__ void k_length_keys(const int4* __restrict__ items, int64_t n, int32_t* __restrict__ key,
+                              int32_t* __restrict__ val) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    key[i] = kMaxItemEdges - (items[i].z - items[i].y);
+    val[i] = (int32_t)i;
+  }
+}
+
+__global__ void k_gather_sorted(const int4* __restrict__ items, const int32_t* __restrict__ order,
+                                int64_t n, int4* __restrict__ sorted) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const int32_t it = order[i];
+    const int4 x = items[it];
+    sorted[i] = make_int4(x.x, x.y, x.z, it);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // exclusive scan of int32 (tiles of 2048, recursive over tile totals)
 // ---------------------------------------------------------------------------
@@ -311,12 +410,45 @@ int grid_1d(int64_t n, int num_sms) {
   return (int)(want < 1 ? 1 : (want > cap ? cap : want));
 }
 
+// Stable LSD radix sort of (key, value) pairs, keys in [0, 2^bits); the
+// sorted values end in *vout_final (one of the scratch buffers).
+gattn_status radix_sort(int32_t* keys, int32_t* vals, int64_t n, int bits, Scratch& scr,
+                        cudaStream_t st, int32_t** vout_final) {
+  int32_t *kb, *vb, *hist, *offs;
+  const int64_t tiles = (n + kTile - 1) / kTile;
+  GATTN_CUDA(scr.get(&kb, n));
+  GATTN_CUDA(scr.get(&vb, n));
+  GATTN_CUDA(scr.get(&hist, tiles * 256));
+  GATTN_CUDA(scr.get(&offs, tiles * 256));
+  const int passes = (bits + 7) / 8;
+  int32_t *kin = keys, *kout = kb, *vin = vals, *vout = vb;
+  gattn_status r;
+  for (int pass = 0; pass < passes; ++pass) {
+    const int shift = 8 * pass;
+    k_radix_hist<<<(unsigned)tiles, kThreads, 0, st>>>(kin, n, shift, tiles, hist);
+    GATTN_CUDA(cudaGetLastError());
+    if ((r = exclusive_scan(hist, offs, tiles * 256, scr, st)) != GATTN_OK) return r;
+    k_radix_scatter<<<(unsigned)tiles, kThreads, 0, st>>>(kin, vin, kout, vout, n, shift, tiles,
+                                                          offs);
+    GATTN_CUDA(cudaGetLastError());
+    int32_t* t = kin;
+    kin = kout;
+    kout = t;
+    t = vin;
+    vin = vout;
+    vout = t;
+  }
+  *vout_final = vin;
+  return GATTN_OK;
+}
+
 // The light/heavy split on one side (CSR or CSC): degrees, histogram,
 // scans, item list.  Allocates its outputs in the plan.
 struct Side {
-  int32_t *deg, *hist, *maxdeg, *light_list, *hfirst;
-  int4* items;
-  int64_t n_light, n_heavy, n_chunks;
+  int32_t *deg, *hist, *maxdeg, *light_list, *hfirst, *parent;
+  int4 *items, *units, *sorted;
+  int2* kids;
+  int64_t n_light, n_heavy, n_chunks, n_units, n_inner;
 };
 
 template <typename T>
@@ -367,6 +499,62 @@ gattn_status build_side(Plan* p, const int32_t* ptr, Scratch& scr, cudaStream_t 
                                                             s->n_chunks, s->n_heavy, s->light_list,
                                                             s->items, s->hfirst);
   GATTN_CUDA(cudaGetLastError());
+  // work units over the item list
+  const int64_t n_items = s->n_light + s->n_chunks;
+  int32_t *len, *epre, *flag, *upos;
+  GATTN_CUDA(scr.get(&len, n_items + 1));
+  GATTN_CUDA(scr.get(&epre, n_items + 1));
+  GATTN_CUDA(scr.get(&flag, n_items + 1));
+  GATTN_CUDA(scr.get(&upos, n_items + 1));
+  k_item_edges<<<grid_1d(n_items + 1, p->num_sms), kThreads, 0, st>>>(s->items, n_items, len);
+  GATTN_CUDA(cudaGetLastError());
+  if ((r = exclusive_scan(len, epre, n_items + 1, scr, st)) != GATTN_OK) return r;
+  k_unit_flags<<<grid_1d(n_items + 1, p->num_sms), kThreads, 0, st>>>(s->items, n_items, epre,
+                                                                      flag);
+  GATTN_CUDA(cudaGetLastError());
+  if ((r = exclusive_scan(flag, upos, n_items + 1, scr, st)) != GATTN_OK) return r;
+  int32_t nu = 0;
+  GATTN_CUDA(cudaMemcpyAsync(&nu, upos + n_items, 4, cudaMemcpyDeviceToHost, st));
+  GATTN_CUDA(cudaStreamSynchronize(st));
+  s->n_units = nu;
+  GATTN_CUDA(plan_alloc(p, &s->units, s->n_units));
+  k_fill_units<<<grid_1d(n_items, p->num_sms), kThreads, 0, st>>>(s->items, n_items, flag, upos,
+                                                                  s->units);
+  GATTN_CUDA(cudaGetLastError());
+  // merge trees over the heavy nodes' chunks
+  {
+    int32_t *inner, *ipos;
+    GATTN_CUDA(scr.get(&inner, s->n_heavy + 1));
+    GATTN_CUDA(scr.get(&ipos, s->n_heavy + 1));
+    k_tree_sizes<<<grid_1d(s->n_heavy + 1, p->num_sms), kThreads, 0, st>>>(s->hfirst, s->n_heavy,
+                                                                          inner);
+    GATTN_CUDA(cudaGetLastError());
+    if ((r = exclusive_scan(inner, ipos, s->n_heavy + 1, scr, st)) != GATTN_OK) return r;
+    int32_t ni = 0;
+    GATTN_CUDA(cudaMemcpyAsync(&ni, ipos + s->n_heavy, 4, cudaMemcpyDeviceToHost, st));
+    GATTN_CUDA(cudaStreamSynchronize(st));
+    s->n_inner = ni;
+    GATTN_CUDA(plan_alloc(p, &s->parent, s->n_chunks + s->n_inner));
+    GATTN_CUDA(plan_alloc(p, &s->kids, s->n_inner));
+    if (s->n_heavy > 0) {
+      k_tree_fill<<<grid_1d(s->n_heavy, p->num_sms), kThreads, 0, st>>>(
+          s->hfirst, s->n_heavy, s->n_chunks, ipos, s->parent, s->kids);
+      GATTN_CUDA(cudaGetLastError());
+    }
+  }
+  // items by decreasing length (degree binning for the attention kernels)
+  GATTN_CUDA(plan_alloc(p, &s->sorted, n_items));
+  if (n_items > 0) {
+    int32_t *key, *val, *order;
+    GATTN_CUDA(scr.get(&key, n_items));
+    GATTN_CUDA(scr.get(&val, n_items));
+    k_length_keys<<<grid_1d(n_items, p->num_sms), kThreads, 0, st>>>(s->items, n_items, key, val);
+    GATTN_CUDA(cudaGetLastError());
+    if ((r = radix_sort(key, val, n_items, 9, scr, st, &order)) != GATTN_OK) return r;
+    k_gather_sorted<<<grid_1d(n_items, p->num_sms), kThreads, 0, st>>>(s->items, order, n_items,
+                                                                       s->sorted);
+    GATTN_CUDA(cudaGetLastError());
+  }
   return GATTN_OK;
 }
 
@@ -416,37 +604,17 @@ gattn_status plan_build(Plan* p, const int32_t* indptr, const int32_t* indices, 
   GATTN_CUDA(plan_alloc(p, &p->csc_eid, M));
   GATTN_CUDA(plan_alloc(p, &p->csc_dst, M));
   if (M) {
-    int32_t *ka, *kb, *va, *vb, *hist, *offs;
-    const int64_t tiles = (M + kTile - 1) / kTile;
+    int32_t *ka, *va, *sorted_eid;
     GATTN_CUDA(scr.get(&ka, M));
-    GATTN_CUDA(scr.get(&kb, M));
     GATTN_CUDA(scr.get(&va, M));
-    GATTN_CUDA(scr.get(&vb, M));
-    GATTN_CUDA(scr.get(&hist, tiles * 256));
-    GATTN_CUDA(scr.get(&offs, tiles * 256));
     GATTN_CUDA(cudaMemcpyAsync(ka, p->indices, M * sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
     k_iota<<<grid_1d(M, p->num_sms), kThreads, 0, st>>>(va, M);
     GATTN_CUDA(cudaGetLastError());
     int bits = 1;
     while (bits < 31 && (int64_t(1) << bits) < N) ++bits;
-    const int passes = (bits + 7) / 8;
-    int32_t *kin = ka, *kout = kb, *vin = va, *vout = vb;
-    for (int pass = 0; pass < passes; ++pass) {
-      const int shift = 8 * pass;
-      k_radix_hist<<<(unsigned)tiles, kThreads, 0, st>>>(kin, M, shift, tiles, hist);
-      GATTN_CUDA(cudaGetLastError());
-      if ((r = exclusive_scan(hist, offs, tiles * 256, scr, st)) != GATTN_OK) return r;
-      k_radix_scatter<<<(unsigned)tiles, kThreads, 0, st>>>(kin, vin, kout, vout, M, shift, tiles,
-                                                            offs);
-      GATTN_CUDA(cudaGetLastError());
-      int32_t* t = kin;
-      kin = kout;
-      kout = t;
-      t = vin;
-      vin = vout;
-      vout = t;
-    }
-    GATTN_CUDA(cudaMemcpyAsync(p->csc_eid, vin, M * sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
+    if ((r = radix_sort(ka, va, M, bits, scr, st, &sorted_eid)) != GATTN_OK) return r;
+    GATTN_CUDA(cudaMemcpyAsync(p->csc_eid, sorted_eid, M * sizeof(int32_t),
+                               cudaMemcpyDeviceToDevice, st));
     k_edge_rows<<<grid_1d(M, p->num_sms), kThreads, 0, st>>>(p->indptr, N, p->csc_eid, M,
                                                              p->csc_dst);
     GATTN_CUDA(cudaGetLastError());
@@ -455,13 +623,13 @@ gattn_status plan_build(Plan* p, const int32_t* indptr, const int32_t* indices, 
   Side s{};
   if ((r = build_side(p, p->indptrT, scr, st, &s)) != GATTN_OK) return r;
   // 6. counters
-  GATTN_CUDA(plan_alloc(p, &p->cnt_fwd, d.n_heavy));
-  GATTN_CUDA(plan_alloc(p, &p->cnt_dq, d.n_heavy));
-  GATTN_CUDA(plan_alloc(p, &p->cnt_dkv, s.n_heavy));
+  GATTN_CUDA(plan_alloc(p, &p->cnt_fwd, d.n_inner));
+  GATTN_CUDA(plan_alloc(p, &p->cnt_dq, d.n_inner));
+  GATTN_CUDA(plan_alloc(p, &p->cnt_dkv, s.n_inner));
   GATTN_CUDA(plan_alloc(p, &p->cnt_da, 1));
-  GATTN_CUDA(cudaMemsetAsync(p->cnt_fwd, 0, (d.n_heavy ? d.n_heavy : 1) * 4, st));
-  GATTN_CUDA(cudaMemsetAsync(p->cnt_dq, 0, (d.n_heavy ? d.n_heavy : 1) * 4, st));
-  GATTN_CUDA(cudaMemsetAsync(p->cnt_dkv, 0, (s.n_heavy ? s.n_heavy : 1) * 4, st));
+  GATTN_CUDA(cudaMemsetAsync(p->cnt_fwd, 0, (d.n_inner ? d.n_inner : 1) * 4, st));
+  GATTN_CUDA(cudaMemsetAsync(p->cnt_dq, 0, (d.n_inner ? d.n_inner : 1) * 4, st));
+  GATTN_CUDA(cudaMemsetAsync(p->cnt_dkv, 0, (s.n_inner ? s.n_inner : 1) * 4, st));
   GATTN_CUDA(cudaMemsetAsync(p->cnt_da, 0, 4, st));
   int32_t mx[2];
   GATTN_CUDA(cudaMemcpyAsync(&mx[0], d.maxdeg, 4, cudaMemcpyDeviceToHost, st));
@@ -472,6 +640,12 @@ gattn_status plan_build(Plan* p, const int32_t* indptr, const int32_t* indices, 
   p->light = d.light_list;
   p->items = d.items;
   p->hfirst = d.hfirst;
+  p->units = d.units;
+  p->n_units = d.n_units;
+  p->sorted = d.sorted;
+  p->parent = d.parent;
+  p->kids = d.kids;
+  p->n_inner = d.n_inner;
   p->n_light = d.n_light;
   p->n_heavy = d.n_heavy;
   p->n_chunks = d.n_chunks;
@@ -480,6 +654,12 @@ gattn_status plan_build(Plan* p, const int32_t* indptr, const int32_t* indices, 
   p->light_src = s.light_list;
   p->items_src = s.items;
   p->hfirst_src = s.hfirst;
+  p->units_src = s.units;
+  p->n_units_src = s.n_units;
+  p->sorted_src = s.sorted;
+  p->parent_src = s.parent;
+  p->kids_src = s.kids;
+  p->n_inner_src = s.n_inner;
   p->n_light_src = s.n_light;
   p->n_heavy_src = s.n_heavy;
   p->n_src_chunks = s.n_chunks;

@@ -84,8 +84,9 @@ typedef struct {
 
 /* Plan options.  Host struct; pass NULL for the defaults. */
 typedef struct {
-  int32_t heavy_threshold; /* node is heavy when its degree > this; <= 0: default 256 */
-  int32_t chunk;           /* edges per heavy-node chunk; <= 0: default 256 */
+  int32_t heavy_threshold; /* node is heavy when its degree > this (max 256); <= 0: chosen
+                              from the graph size, a power of two in [32, 256] */
+  int32_t chunk;           /* edges per heavy-node chunk (max 256); <= 0: the threshold */
   int32_t tile_enable;     /* reserved for the dense-tile path; must be 0 */
   float tile_density;      /* reserved */
 } gattn_plan_opts;
