@@ -24,7 +24,8 @@ GATTN_F32, GATTN_BF16 = 0, 1
 GATTN_SCORE_DOT, GATTN_SCORE_GATV2 = 0, 1
 EXPORTED = ("gattn_plan_create", "gattn_plan_destroy", "gattn_plan_get_info",
             "gattn_plan_export", "gattn_workspace_size", "gattn_fwd", "gattn_bwd",
-            "gattn_bwd_dq", "gattn_bwd_dkdv", "gattn_last_error", "gattn_version")
+            "gattn_bwd_dq", "gattn_bwd_dkdv", "gattn_plan_check_errors", "gattn_last_error",
+            "gattn_version")
 
 
 class GattnError(RuntimeError):
@@ -88,7 +89,8 @@ def load_library(path: str | None = None):
                                      P, P, P, P, P, P, sz, P]
         lib.gattn_bwd_dkdv.argtypes = [P, i32, i32, ctypes.c_int, P, P, P,
                                        ctypes.POINTER(_Score), P, P, P, P, P, sz, P]
-        for name in EXPORTED[:9]:
+        lib.gattn_plan_check_errors.argtypes = [P]
+        for name in EXPORTED[:10]:
             getattr(lib, name).restype = st
         lib.gattn_last_error.restype = ctypes.c_char_p
         lib.gattn_last_error.argtypes = []
@@ -308,3 +310,8 @@ def gattn_bwd_dkdv(plan: Plan, Q, K, V, dout, lse, score: Score, dK=None, dV=Non
                                          _ptr(lse), _ptr(dK), _ptr(dV), _ptr(ws), ws.numel(),
                                          _stream(stream)), "gattn_bwd_dkdv")
     return dK, dV
+
+
+def gattn_plan_check_errors(plan: Plan) -> None:
+    """Raise GattnError(GATTN_ERR_TIMEOUT) if a kernel gave up a bounded wait."""
+    _check(load_library().gattn_plan_check_errors(plan.handle), "gattn_plan_check_errors")

@@ -27,13 +27,6 @@ void set_error(const char* fmt, ...) {
 
 gattn_status plan_build(Plan* p, const int32_t* indptr, const int32_t* indices, cudaStream_t st);
 
-gattn_status launch_fwd_f32(int, int, const FwdParams&, int, cudaStream_t, int*);
-gattn_status launch_fwd_bf16(int, int, const FwdParams&, int, cudaStream_t, int*);
-gattn_status launch_bwd_csr_f32(int, int, const BwdParams&, int, cudaStream_t, int*);
-gattn_status launch_bwd_csr_bf16(int, int, const BwdParams&, int, cudaStream_t, int*);
-gattn_status launch_bwd_csc_f32(int, int, const BwdParams&, int, cudaStream_t, int*);
-gattn_status launch_bwd_csc_bf16(int, int, const BwdParams&, int, cudaStream_t, int*);
-
 namespace {
 
 size_t dtype_size(gattn_dtype dt) { return dt == GATTN_F32 ? 4 : (dt == GATTN_BF16 ? 2 : 0); }
@@ -133,21 +126,38 @@ gattn_status launched(const char* what) {
 
 }  // namespace
 
-gattn_status launch_fwd(gattn_dtype dt, int rb, int kind, const FwdParams& p, int num_sms,
+#define GATTN_ROW_CASE(PASS_NAME, PT, TNAME, RB_) \
+  case RB_:                                      \
+    return launch_##PASS_NAME##_##TNAME##_##RB_(db, kind, p, num_sms, st, g);
+
+gattn_status launch_fwd(gattn_dtype dt, int rb, int db, int kind, const FwdParams& p, int num_sms,
                         cudaStream_t st, int* g) {
-  return dt == GATTN_F32 ? launch_fwd_f32(rb, kind, p, num_sms, st, g)
-                         : launch_fwd_bf16(rb, kind, p, num_sms, st, g);
+  if (dt == GATTN_F32) {
+    switch (rb) { GATTN_FOR_ROWS(GATTN_ROW_CASE, fwd, FwdParams, f32) }
+  } else {
+    switch (rb) { GATTN_FOR_ROWS(GATTN_ROW_CASE, fwd, FwdParams, bf16) }
+  }
+  return GATTN_ERR_UNSUPPORTED;
 }
-gattn_status launch_bwd_csr(gattn_dtype dt, int rb, int kind, const BwdParams& p, int num_sms,
-                            cudaStream_t st, int* g) {
-  return dt == GATTN_F32 ? launch_bwd_csr_f32(rb, kind, p, num_sms, st, g)
-                         : launch_bwd_csr_bf16(rb, kind, p, num_sms, st, g);
+gattn_status launch_bwd_csr(gattn_dtype dt, int rb, int db, int kind, const BwdParams& p,
+                            int num_sms, cudaStream_t st, int* g) {
+  if (dt == GATTN_F32) {
+    switch (rb) { GATTN_FOR_ROWS(GATTN_ROW_CASE, csr, BwdParams, f32) }
+  } else {
+    switch (rb) { GATTN_FOR_ROWS(GATTN_ROW_CASE, csr, BwdParams, bf16) }
+  }
+  return GATTN_ERR_UNSUPPORTED;
 }
-gattn_status launch_bwd_csc(gattn_dtype dt, int rb, int kind, const BwdParams& p, int num_sms,
-                            cudaStream_t st, int* g) {
-  return dt == GATTN_F32 ? launch_bwd_csc_f32(rb, kind, p, num_sms, st, g)
-                         : launch_bwd_csc_bf16(rb, kind, p, num_sms, st, g);
+gattn_status launch_bwd_csc(gattn_dtype dt, int rb, int db, int kind, const BwdParams& p,
+                            int num_sms, cudaStream_t st, int* g) {
+  if (dt == GATTN_F32) {
+    switch (rb) { GATTN_FOR_ROWS(GATTN_ROW_CASE, csc, BwdParams, f32) }
+  } else {
+    switch (rb) { GATTN_FOR_ROWS(GATTN_ROW_CASE, csc, BwdParams, bf16) }
+  }
+  return GATTN_ERR_UNSUPPORTED;
 }
+#undef GATTN_ROW_CASE
 
 }  // namespace gattn
 
@@ -301,6 +311,23 @@ gattn_status gattn_plan_export(const gattn_plan* plan, int32_t* deg, int32_t* hi
   return GATTN_OK;
 }
 
+gattn_status gattn_plan_check_errors(const gattn_plan* plan) {
+  GATTN_REQUIRE(plan, GATTN_ERR_INVALID_ARG, "plan is NULL");
+  cudaError_t e = cudaDeviceSynchronize();
+  int32_t flag = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&flag, plan->p.err, 4, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) {
+    set_error("checking the plan's error flag failed: %s", cudaGetErrorString(e));
+    return GATTN_ERR_CUDA;
+  }
+  if (flag) {
+    cudaMemset(plan->p.err, 0, 4);
+    set_error("a kernel gave up waiting for its asynchronous copies");
+    return GATTN_ERR_TIMEOUT;
+  }
+  return GATTN_OK;
+}
+
 gattn_status gattn_workspace_size(const gattn_plan* plan, int32_t H, int32_t D,
                                   gattn_dtype dtype, size_t* bytes) {
   GATTN_REQUIRE(plan && bytes, GATTN_ERR_INVALID_ARG, "plan and bytes must be non-null");
@@ -349,8 +376,11 @@ gattn_status gattn_fwd(const gattn_plan* plan, int32_t H, int32_t D, gattn_dtype
   f.part = reinterpret_cast<float*>(ws + w.fwd_part);
   f.pstride = w.pstride;
   f.tree = Tree{p.parent, p.kids, p.n_chunks, p.cnt_fwd};
+  f.err = p.err;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if ((s = launch_fwd(dtype, rb, score->kind, f, p.num_sms, st, nullptr)) != GATTN_OK) return s;
+  if ((s = launch_fwd(dtype, rb, D * (int)dtype_size(dtype), score->kind, f, p.num_sms, st,
+                      nullptr)) != GATTN_OK)
+    return s;
   return launched("forward");
 }
 
@@ -386,6 +416,7 @@ static gattn_status bwd_common(const gattn_plan* plan, int32_t H, int32_t D, gat
   b->delta16 = (H % 4 == 0);
   b->da_part = reinterpret_cast<float*>(ws + w->da_part);
   b->da_cnt = plan->p.cnt_da;
+  b->err = plan->p.err;
   return GATTN_OK;
 }
 
@@ -423,7 +454,8 @@ gattn_status gattn_bwd_dq(const gattn_plan* plan, int32_t H, int32_t D, gattn_dt
   b.da = gat ? da : nullptr;
   b.part = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.dq_part);
   b.tree = Tree{p.parent, p.kids, p.n_chunks, p.cnt_dq};
-  if ((s = launch_bwd_csr(dtype, rb, score->kind, b, p.num_sms, st, nullptr)) != GATTN_OK)
+  if ((s = launch_bwd_csr(dtype, rb, D * (int)dtype_size(dtype), score->kind, b, p.num_sms,
+                          st, nullptr)) != GATTN_OK)
     return s;
   return launched("backward (CSR pass)");
 }
@@ -452,7 +484,7 @@ gattn_status gattn_bwd_dkdv(const gattn_plan* plan, int32_t H, int32_t D, gattn_
   b.da = nullptr;
   b.part = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.dkv_part);
   b.tree = Tree{p.parent_src, p.kids_src, p.n_src_chunks, p.cnt_dkv};
-  if ((s = launch_bwd_csc(dtype, rb, score->kind, b, p.num_sms,
+  if ((s = launch_bwd_csc(dtype, rb, D * (int)dtype_size(dtype), score->kind, b, p.num_sms,
                           reinterpret_cast<cudaStream_t>(stream), nullptr)) != GATTN_OK)
     return s;
   return launched("backward (CSC pass)");

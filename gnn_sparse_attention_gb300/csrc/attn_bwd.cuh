@@ -53,6 +53,7 @@ struct BwdParams {
   Tree tree;           // merge trees of the heavy items of this pass
   float* da_part;      // [gridDim.x][HD]
   int32_t* da_cnt;
+  int32_t* err;        // set when a wait gives up
 };
 
 // Largest per-node fp32 row (lse or Delta): H <= RB/16 floats, padded to 16 B.
@@ -107,7 +108,7 @@ __device__ __forceinline__ void copy_stat_rows(uint8_t* dst, const float* src, i
 // ---------------------------------------------------------------------------
 // pass 1: CSR
 // ---------------------------------------------------------------------------
-template <typename T, int RB, int KIND>
+template <typename T, int RB, int DB, int KIND>
 __global__ void __launch_bounds__(CsrShape<T, RB>::THREADS) bwd_csr_kernel(const BwdParams p) {
   using L = Lay<T, RB>;
   using Sh = CsrShape<T, RB>;
@@ -115,14 +116,15 @@ __global__ void __launch_bounds__(CsrShape<T, RB>::THREADS) bwd_csr_kernel(const
   constexpr int NC = L::NC, TPR = L::TPR, G = L::G, SE = L::SE, B = L::B;
   constexpr int NCH = L::NCH, PP = PR::P, S = kStages, LS = Sh::LS;
   constexpr int HD = RB / (int)sizeof(T);
+  constexpr int D = DB / (int)sizeof(T);  // head width
+  constexpr int CPH = DB / 16;            // 16-byte chunks per head
   constexpr bool GAT = KIND == GATTN_SCORE_GATV2;
   constexpr unsigned FULL = 0xffffffffu;
   extern __shared__ __align__(16) uint8_t smem[];
   const int lane = threadIdx.x & 31;
   const int g = lane / TPR, t = lane % TPR;
-  const int cph = p.D * (int)sizeof(T) / 16;
   Ring<L, Sh::STAGE> ring;
-  ring.init(smem + (threadIdx.x >> 5) * Sh::WARP_BYTES);
+  ring.init(smem + (threadIdx.x >> 5) * Sh::WARP_BYTES, lane);
   const char* __restrict__ Qb = static_cast<const char*>(p.Q);
   const char* __restrict__ Kb = static_cast<const char*>(p.K);
   const char* __restrict__ Vb = static_cast<const char*>(p.V);
@@ -134,8 +136,8 @@ __global__ void __launch_bounds__(CsrShape<T, RB>::THREADS) bwd_csr_kernel(const
 #pragma unroll
   for (int c = 0; c < NC; ++c) {
     elem[c] = (t * NC + c) * (16 / (int)sizeof(T));
-    head[c] = elem[c] / p.D;
-    hw[c] = ((t * NC + c) % cph) == 0;
+    head[c] = elem[c] / D;
+    hw[c] = ((t * NC + c) % CPH) == 0;
   }
   float2 av[GAT ? NC : 1][PP], dacc[GAT ? NC : 1][PP];
   if (GAT) {
@@ -153,38 +155,48 @@ __global__ void __launch_bounds__(CsrShape<T, RB>::THREADS) bwd_csr_kernel(const
   BundleCursor<G, SE> cur;
   cur.start(p.sorted, p.n_items, p.idx, warp, nwarps, ring.items, lane);
 
-  // stage: [G][Q, dO, O rows] [G][lse row] [B][K row] [B][V row]
+  // stage: [G][Q, dO, O rows] [G][lse row] [B][K row] [B][V row]; rows by
+  // TMA bulk copies (lse rows too when they are 16-byte pieces, else 4-byte
+  // cp.async).  Row r: [0,G) Q, [G,2G) dO, [2G,3G) O, [3G,4G) lse, then
+  // [4G, 4G+B) K and [4G+B, 4G+2B) V.
   auto issue = [&](int s) {
     const int4* dsc = ring.desc_at(s);
     const int4 dg = lane < G ? dsc[lane] : make_int4(-1, 0, 0, 0);
     if (__shfl_sync(FULL, dg.x, 0) != -3) {
       uint8_t* st = ring.stage_at(s);
+      uint64_t* bar = ring.bar_at(s);
       const int ge = (lane / SE) & 31;
       const int cn = __shfl_sync(FULL, dg.x >= 0 ? (dg.z & kCntMask) : 0, ge);
       const int jv = (lane < B && lane % SE < cn) ? ring.ix_at(s)[lane] : -1;
       const int fnode = (lane < G && dg.x >= 0 && (dg.z & kFirst)) ? dg.x : -1;
-#pragma unroll
-      for (int r = 0; r < NC; ++r) {
-        const int x = r * 32 + lane, gg = x / NCH, ch = x % NCH;
-        const int node = __shfl_sync(FULL, fnode, gg);
-        if (node >= 0) {
-          const int64_t src = int64_t(node) * RB + ch * 16;
-          uint8_t* dst = st + gg * 3 * RB + L::pos(ch) * 16;
-          cp_async16(dst, Qb + src);
-          cp_async16(dst + RB, dOb + src);
-          cp_async16(dst + 2 * RB, Ob + src);
-        }
-      }
-      copy_stat_rows<LS>(st + G * 3 * RB, p.lse, fnode, G, p.H, p.rows16, lane);
+      const int nq = __popc(__ballot_sync(FULL, fnode >= 0));
+      const int ne = __popc(__ballot_sync(FULL, jv >= 0));
+      const uint32_t bytes = nq * (3 * RB + (p.rows16 ? 4 * p.H : 0)) + ne * 2 * RB;
+      fence_proxy_async();
+      if (lane == 0) mbar_expect_tx(bar, bytes);
+      __syncwarp();
+      if (!p.rows16) copy_stat_rows<LS>(st + G * 3 * RB, p.lse, fnode, G, p.H, false, lane);
       uint8_t* kd = st + G * (3 * RB + LS);
-      uint8_t* vd = kd + B * RB;
 #pragma unroll
-      for (int r = 0; r < SE * NC; ++r) {
-        const int x = r * 32 + lane, b = x / NCH, ch = x % NCH;
-        const int j = __shfl_sync(FULL, jv, b);
-        if (j >= 0) {
-          cp_async16(kd + b * RB + L::pos(ch) * 16, Kb + int64_t(j) * RB + ch * 16);
-          cp_async16(vd + b * RB + L::pos(ch) * 16, Vb + int64_t(j) * RB + ch * 16);
+      for (int r0 = 0; r0 < 4 * G + 2 * B; r0 += 32) {
+        const int r = r0 + lane;
+        const int b = r < 4 * G + B ? r - 4 * G : r - 4 * G - B;
+        const int node = __shfl_sync(FULL, fnode, (r % G) & 31);
+        const int j = __shfl_sync(FULL, jv, b & 31);
+        if (r < 4 * G) {
+          const int gg = r % G, kind = r / G;
+          if (node >= 0) {
+            if (kind < 3) {
+              const char* src = (kind == 0 ? Qb : (kind == 1 ? dOb : Ob)) + int64_t(node) * RB;
+              bulk_g2s(st + gg * 3 * RB + kind * RB, src, RB, bar);
+            } else if (p.rows16) {
+              bulk_g2s(st + G * 3 * RB + gg * LS, p.lse + int64_t(node) * p.H, 4 * p.H, bar);
+            }
+          }
+        } else if (r < 4 * G + B) {
+          if (j >= 0) bulk_g2s(kd + b * RB, Kb + int64_t(j) * RB, RB, bar);
+        } else if (r < 4 * G + 2 * B) {
+          if (j >= 0) bulk_g2s(kd + B * RB + b * RB, Vb + int64_t(j) * RB, RB, bar);
         }
       }
     }
@@ -210,6 +222,7 @@ __global__ void __launch_bounds__(CsrShape<T, RB>::THREADS) bwd_csr_kernel(const
     __syncwarp();
     const int4* dsc = ring.desc_at(i);
     if (dsc[0].x == -3) break;
+    if (!__all_sync(FULL, ring.wait_rows(i, p.err, lane))) break;
     const int4 d = dsc[g];
     const bool act = d.x >= 0;
     const int cnt = act ? (d.z & kCntMask) : 0;
@@ -222,7 +235,7 @@ __global__ void __launch_bounds__(CsrShape<T, RB>::THREADS) bwd_csr_kernel(const
       for (int c = 0; c < NC; ++c) {
         float2 o[PP];
         if (first) {
-          const uint8_t* rows = st + g * 3 * RB + (c * TPR + t) * 16;
+          const uint8_t* rows = st + g * 3 * RB + (t * NC + c) * 16;
           PR::load(lds16(rows), q[c]);
           PR::load(lds16(rows + RB), gq[c]);
           PR::load(lds16(rows + 2 * RB), o);
@@ -235,7 +248,7 @@ __global__ void __launch_bounds__(CsrShape<T, RB>::THREADS) bwd_csr_kernel(const
         for (int v = 0; v < PP; ++v) a2 = f2fma(first ? gq[c][v] : f2s(0.f), o[v], a2);
         part[c] = a2.x + a2.y;
       }
-      head_totals<NC>(part, cph);
+      head_totals<NC, CPH>(part);
       if (first) {
         const float* ls = reinterpret_cast<const float*>(st + G * 3 * RB + g * LS);
 #pragma unroll
@@ -266,7 +279,7 @@ __global__ void __launch_bounds__(CsrShape<T, RB>::THREADS) bwd_csr_kernel(const
       float2 kf[NC][PP];
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
-        const int off = k * RB + (c * TPR + t) * 16;
+        const int off = k * RB + (t * NC + c) * 16;
         float2 vf[PP];
         PR::load(valid ? lds16(ks + off) : make_uint4(0, 0, 0, 0), kf[c]);
         PR::load(valid ? lds16(vs + off) : make_uint4(0, 0, 0, 0), vf);
@@ -286,8 +299,8 @@ __global__ void __launch_bounds__(CsrShape<T, RB>::THREADS) bwd_csr_kernel(const
         sc[c] = s2.x + s2.y;
         dp[c] = p2.x + p2.y;
       }
-      head_totals<NC>(sc, cph);
-      head_totals<NC>(dp, cph);
+      head_totals<NC, CPH>(sc);
+      head_totals<NC, CPH>(dp);
       if (act && valid) {
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
@@ -371,6 +384,7 @@ __global__ void __launch_bounds__(CsrShape<T, RB>::THREADS) bwd_csr_kernel(const
     __syncwarp();
   }
   cp_async_wait<0>();
+  ring.release(lane);
 
   if (GAT && p.da != nullptr) {
     // warp -> block -> last block over block partials, all in fixed order
@@ -421,7 +435,7 @@ __global__ void __launch_bounds__(CsrShape<T, RB>::THREADS) bwd_csr_kernel(const
 // ---------------------------------------------------------------------------
 // pass 2: CSC
 // ---------------------------------------------------------------------------
-template <typename T, int RB, int KIND>
+template <typename T, int RB, int DB, int KIND>
 __global__ void __launch_bounds__(CscShape<T, RB>::THREADS) bwd_csc_kernel(const BwdParams p) {
   using L = Lay<T, RB>;
   using Sh = CscShape<T, RB>;
@@ -429,14 +443,15 @@ __global__ void __launch_bounds__(CscShape<T, RB>::THREADS) bwd_csc_kernel(const
   constexpr int NC = L::NC, TPR = L::TPR, G = L::G, SE = L::SE, B = L::B;
   constexpr int NCH = L::NCH, PP = PR::P, S = kStages, LS = Sh::LS;
   constexpr int HD = RB / (int)sizeof(T);
+  constexpr int D = DB / (int)sizeof(T);  // head width
+  constexpr int CPH = DB / 16;            // 16-byte chunks per head
   constexpr bool GAT = KIND == GATTN_SCORE_GATV2;
   constexpr unsigned FULL = 0xffffffffu;
   extern __shared__ __align__(16) uint8_t smem[];
   const int lane = threadIdx.x & 31;
   const int g = lane / TPR, t = lane % TPR;
-  const int cph = p.D * (int)sizeof(T) / 16;
   Ring<L, Sh::STAGE> ring;
-  ring.init(smem + (threadIdx.x >> 5) * Sh::WARP_BYTES);
+  ring.init(smem + (threadIdx.x >> 5) * Sh::WARP_BYTES, lane);
   const char* __restrict__ Qb = static_cast<const char*>(p.Q);
   const char* __restrict__ Kb = static_cast<const char*>(p.K);
   const char* __restrict__ Vb = static_cast<const char*>(p.V);
@@ -446,7 +461,7 @@ __global__ void __launch_bounds__(CscShape<T, RB>::THREADS) bwd_csc_kernel(const
 #pragma unroll
   for (int c = 0; c < NC; ++c) {
     elem[c] = (t * NC + c) * (16 / (int)sizeof(T));
-    head[c] = elem[c] / p.D;
+    head[c] = elem[c] / D;
   }
   float2 av[GAT ? NC : 1][PP];
   if (GAT) {
@@ -462,41 +477,52 @@ __global__ void __launch_bounds__(CscShape<T, RB>::THREADS) bwd_csc_kernel(const
   BundleCursor<G, SE> cur;
   cur.start(p.sorted, p.n_items, p.idx, warp, nwarps, ring.items, lane);
 
-  // stage: [G][K, V rows] [B][Q row] [B][dO row] [B][lse row] [B][Delta row]
+  // stage: [G][K, V rows] [B][Q row] [B][dO row] [B][lse row] [B][Delta row];
+  // rows by TMA bulk copies (stat rows too when they are 16-byte pieces).
+  // Row r: [0,G) K, [G,2G) V, [2G, 2G+B) Q, [2G+B, 2G+2B) dO,
+  // [2G+2B, 2G+3B) lse, [2G+3B, 2G+4B) Delta.
   auto issue = [&](int s) {
     const int4* dsc = ring.desc_at(s);
     const int4 dg = lane < G ? dsc[lane] : make_int4(-1, 0, 0, 0);
     if (__shfl_sync(FULL, dg.x, 0) != -3) {
       uint8_t* st = ring.stage_at(s);
+      uint64_t* bar = ring.bar_at(s);
       const int ge = (lane / SE) & 31;
       const int cn = __shfl_sync(FULL, dg.x >= 0 ? (dg.z & kCntMask) : 0, ge);
       const int jv = (lane < B && lane % SE < cn) ? ring.ix_at(s)[lane] : -1;
       const int fnode = (lane < G && dg.x >= 0 && (dg.z & kFirst)) ? dg.x : -1;
-#pragma unroll
-      for (int r = 0; r < NC; ++r) {
-        const int x = r * 32 + lane, gg = x / NCH, ch = x % NCH;
-        const int node = __shfl_sync(FULL, fnode, gg);
-        if (node >= 0) {
-          const int64_t src = int64_t(node) * RB + ch * 16;
-          uint8_t* dst = st + gg * 2 * RB + L::pos(ch) * 16;
-          cp_async16(dst, Kb + src);
-          cp_async16(dst + RB, Vb + src);
-        }
-      }
+      const int nq = __popc(__ballot_sync(FULL, fnode >= 0));
+      const int ne = __popc(__ballot_sync(FULL, jv >= 0));
+      const uint32_t bytes =
+          nq * 2 * RB + ne * (2 * RB + (p.rows16 ? 4 * p.H : 0) + (p.delta16 ? 4 * p.H : 0));
+      fence_proxy_async();
+      if (lane == 0) mbar_expect_tx(bar, bytes);
+      __syncwarp();
       uint8_t* qd = st + G * 2 * RB;
       uint8_t* gd = qd + B * RB;
+      uint8_t* lsd = gd + B * RB;
+      if (!p.rows16) copy_stat_rows<LS>(lsd, p.lse, jv, B, p.H, false, lane);
+      if (!p.delta16) copy_stat_rows<LS>(lsd + B * LS, p.delta, jv, B, p.H, false, lane);
 #pragma unroll
-      for (int r = 0; r < SE * NC; ++r) {
-        const int x = r * 32 + lane, b = x / NCH, ch = x % NCH;
-        const int i2 = __shfl_sync(FULL, jv, b);
-        if (i2 >= 0) {
-          cp_async16(qd + b * RB + L::pos(ch) * 16, Qb + int64_t(i2) * RB + ch * 16);
-          cp_async16(gd + b * RB + L::pos(ch) * 16, dOb + int64_t(i2) * RB + ch * 16);
+      for (int r0 = 0; r0 < 2 * G + 4 * B; r0 += 32) {
+        const int r = r0 + lane;
+        const int e = (r - 2 * G) % B;
+        const int node = __shfl_sync(FULL, fnode, (r % G) & 31);
+        const int i2 = __shfl_sync(FULL, jv, (e < 0 ? 0 : e) & 31);
+        if (r < 2 * G) {
+          if (node >= 0)
+            bulk_g2s(st + (r % G) * 2 * RB + (r / G) * RB,
+                     (r < G ? Kb : Vb) + int64_t(node) * RB, RB, bar);
+        } else if (r < 2 * G + 4 * B && i2 >= 0) {
+          const int kind = (r - 2 * G) / B;
+          if (kind == 0) bulk_g2s(qd + e * RB, Qb + int64_t(i2) * RB, RB, bar);
+          else if (kind == 1) bulk_g2s(gd + e * RB, dOb + int64_t(i2) * RB, RB, bar);
+          else if (kind == 2 && p.rows16)
+            bulk_g2s(lsd + e * LS, p.lse + int64_t(i2) * p.H, 4 * p.H, bar);
+          else if (kind == 3 && p.delta16)
+            bulk_g2s(lsd + B * LS + e * LS, p.delta + int64_t(i2) * p.H, 4 * p.H, bar);
         }
       }
-      uint8_t* lsd = gd + B * RB;
-      copy_stat_rows<LS>(lsd, p.lse, jv, B, p.H, p.rows16, lane);
-      copy_stat_rows<LS>(lsd + B * LS, p.delta, jv, B, p.H, p.delta16, lane);
     }
     cp_async_commit();
   };
@@ -519,6 +545,7 @@ __global__ void __launch_bounds__(CscShape<T, RB>::THREADS) bwd_csc_kernel(const
     __syncwarp();
     const int4* dsc = ring.desc_at(i);
     if (dsc[0].x == -3) break;
+    if (!__all_sync(FULL, ring.wait_rows(i, p.err, lane))) break;
     const int4 d = dsc[g];
     const bool act = d.x >= 0;
     const int cnt = act ? (d.z & kCntMask) : 0;
@@ -527,7 +554,7 @@ __global__ void __launch_bounds__(CscShape<T, RB>::THREADS) bwd_csc_kernel(const
     if (act && (d.z & kFirst)) {
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
-        const uint8_t* rows = st + g * 2 * RB + (c * TPR + t) * 16;
+        const uint8_t* rows = st + g * 2 * RB + (t * NC + c) * 16;
         PR::load(lds16(rows), k[c]);
         PR::load(lds16(rows + RB), vv[c]);
 #pragma unroll
@@ -551,7 +578,7 @@ __global__ void __launch_bounds__(CscShape<T, RB>::THREADS) bwd_csc_kernel(const
       float2 qf[NC][PP], gf[NC][PP];
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
-        const int off = e * RB + (c * TPR + t) * 16;
+        const int off = e * RB + (t * NC + c) * 16;
         PR::load(valid ? lds16(qs + off) : make_uint4(0, 0, 0, 0), qf[c]);
         PR::load(valid ? lds16(gs + off) : make_uint4(0, 0, 0, 0), gf[c]);
         float2 s2 = f2s(0.f), p2 = f2s(0.f);
@@ -570,8 +597,8 @@ __global__ void __launch_bounds__(CscShape<T, RB>::THREADS) bwd_csc_kernel(const
         sc[c] = s2.x + s2.y;
         dp[c] = p2.x + p2.y;
       }
-      head_totals<NC>(sc, cph);
-      head_totals<NC>(dp, cph);
+      head_totals<NC, CPH>(sc);
+      head_totals<NC, CPH>(dp);
       if (act && valid) {
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
@@ -669,6 +696,7 @@ __global__ void __launch_bounds__(CscShape<T, RB>::THREADS) bwd_csc_kernel(const
     __syncwarp();
   }
   cp_async_wait<0>();
+  ring.release(lane);
 }
 
 }  // namespace gattn

@@ -43,6 +43,7 @@ struct FwdParams {
   float* part;         // [n_chunks + n_inner][pstride]: acc[HD], m[H], l[H]
   int pstride;
   Tree tree;           // merge trees of the heavy destinations
+  int32_t* err;        // set when a wait gives up
 };
 
 template <typename T, int RB>
@@ -56,7 +57,7 @@ struct FwdShape {
   static constexpr int SMEM = WARPS * WARP_BYTES;
 };
 
-template <typename T, int RB, int KIND>
+template <typename T, int RB, int DB, int KIND>
 __global__ void __launch_bounds__(FwdShape<T, RB>::THREADS) fwd_kernel(const FwdParams p) {
   using L = Lay<T, RB>;
   using Sh = FwdShape<T, RB>;
@@ -64,14 +65,15 @@ __global__ void __launch_bounds__(FwdShape<T, RB>::THREADS) fwd_kernel(const Fwd
   constexpr int NC = L::NC, TPR = L::TPR, G = L::G, SE = L::SE, B = L::B;
   constexpr int NCH = L::NCH, PP = PR::P, S = kStages;
   constexpr int HD = RB / (int)sizeof(T);
+  constexpr int D = DB / (int)sizeof(T);  // head width
+  constexpr int CPH = DB / 16;            // 16-byte chunks per head
   constexpr bool GAT = KIND == GATTN_SCORE_GATV2;
   constexpr unsigned FULL = 0xffffffffu;
   extern __shared__ __align__(16) uint8_t smem[];
   const int lane = threadIdx.x & 31;
   const int g = lane / TPR, t = lane % TPR;
-  const int cph = p.D * (int)sizeof(T) / 16;  // chunks per head
   Ring<L, Sh::STAGE> ring;
-  ring.init(smem + (threadIdx.x >> 5) * Sh::WARP_BYTES);
+  ring.init(smem + (threadIdx.x >> 5) * Sh::WARP_BYTES, lane);
   const char* __restrict__ Qb = static_cast<const char*>(p.Q);
   const char* __restrict__ Kb = static_cast<const char*>(p.K);
   const char* __restrict__ Vb = static_cast<const char*>(p.V);
@@ -83,8 +85,8 @@ __global__ void __launch_bounds__(FwdShape<T, RB>::THREADS) fwd_kernel(const Fwd
 #pragma unroll
   for (int c = 0; c < NC; ++c) {
     elem[c] = (t * NC + c) * (16 / (int)sizeof(T));
-    head[c] = elem[c] / p.D;
-    hw[c] = ((t * NC + c) % cph) == 0;
+    head[c] = elem[c] / D;
+    hw[c] = ((t * NC + c) % CPH) == 0;
   }
   float2 av[GAT ? NC : 1][PP];
   if (GAT) {
@@ -100,36 +102,39 @@ __global__ void __launch_bounds__(FwdShape<T, RB>::THREADS) fwd_kernel(const Fwd
   BundleCursor<G, SE> cur;
   cur.start(p.sorted, p.n_items, p.indices, warp, nwarps, ring.items, lane);
 
-  // row copies of stage s into its ring slot
+  // rows of stage s into its ring slot: one TMA bulk copy per row, bytes
+  // counted on the slot's barrier.  Row r of the stage: [0, G) Q rows of
+  // items that start here, [G, G+B) K rows, [G+B, G+2B) V rows.
   auto issue = [&](int s) {
     const int4* dsc = ring.desc_at(s);
     const int4 dg = lane < G ? dsc[lane] : make_int4(-1, 0, 0, 0);
     if (__shfl_sync(FULL, dg.x, 0) != -3) {
       uint8_t* st = ring.stage_at(s);
+      uint64_t* bar = ring.bar_at(s);
       const int ge = (lane / SE) & 31;
       const int cn = __shfl_sync(FULL, dg.x >= 0 ? (dg.z & kCntMask) : 0, ge);
       const int jv = (lane < B && lane % SE < cn) ? ring.ix_at(s)[lane] : -1;
+      const int fq = (lane < G && dg.x >= 0 && (dg.z & kFirst)) ? dg.x : -1;
+      const int rows = __popc(__ballot_sync(FULL, fq >= 0)) + 2 * __popc(__ballot_sync(FULL, jv >= 0));
+      fence_proxy_async();
+      if (lane == 0) mbar_expect_tx(bar, rows * RB);
+      __syncwarp();
 #pragma unroll
-      for (int r = 0; r < NC; ++r) {  // Q rows of items that start here: G*NCH = 32*NC chunks
-        const int x = r * 32 + lane, gg = x / NCH, ch = x % NCH;
-        const int node = __shfl_sync(FULL, dg.x, gg);
-        const int fl = __shfl_sync(FULL, dg.z, gg);
-        if (node >= 0 && (fl & kFirst))
-          cp_async16(st + gg * RB + L::pos(ch) * 16, Qb + int64_t(node) * RB + ch * 16);
-      }
-      uint8_t* kd = st + G * RB;
-      uint8_t* vd = kd + B * RB;
-#pragma unroll
-      for (int r = 0; r < SE * NC; ++r) {  // B*NCH = 32*SE*NC chunks of K and of V
-        const int x = r * 32 + lane, b = x / NCH, ch = x % NCH;
-        const int j = __shfl_sync(FULL, jv, b);
-        if (j >= 0) {
-          cp_async16(kd + b * RB + L::pos(ch) * 16, Kb + int64_t(j) * RB + ch * 16);
-          cp_async16(vd + b * RB + L::pos(ch) * 16, Vb + int64_t(j) * RB + ch * 16);
+      for (int r0 = 0; r0 < G + 2 * B; r0 += 32) {
+        const int r = r0 + lane;
+        const int b = r < G + B ? r - G : r - G - B;
+        const int node = __shfl_sync(FULL, fq, r & 31);
+        const int j = __shfl_sync(FULL, jv, b & 31);
+        if (r < G) {
+          if (node >= 0) bulk_g2s(st + r * RB, Qb + int64_t(node) * RB, RB, bar);
+        } else if (r < G + B) {
+          if (j >= 0) bulk_g2s(st + G * RB + b * RB, Kb + int64_t(j) * RB, RB, bar);
+        } else if (r < G + 2 * B) {
+          if (j >= 0) bulk_g2s(st + (G + B) * RB + b * RB, Vb + int64_t(j) * RB, RB, bar);
         }
       }
     }
-    cp_async_commit();
+    cp_async_commit();  // this iteration's index copies
   };
 
   // prologue: indices of stages 0..S-1, then rows of stages 0..S-2
@@ -152,6 +157,7 @@ __global__ void __launch_bounds__(FwdShape<T, RB>::THREADS) fwd_kernel(const Fwd
     __syncwarp();
     const int4* dsc = ring.desc_at(i);
     if (dsc[0].x == -3) break;
+    if (!__all_sync(FULL, ring.wait_rows(i, p.err, lane))) break;
     const int4 d = dsc[g];
     const bool act = d.x >= 0;
     const int cnt = act ? (d.z & kCntMask) : 0;
@@ -160,7 +166,7 @@ __global__ void __launch_bounds__(FwdShape<T, RB>::THREADS) fwd_kernel(const Fwd
     if (act && (d.z & kFirst)) {
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
-        PR::load(lds16(st + g * RB + (c * TPR + t) * 16), q[c]);
+        PR::load(lds16(st + g * RB + (t * NC + c) * 16), q[c]);
         if (!GAT) {
 #pragma unroll
           for (int v = 0; v < PP; ++v) q[c][v] = f2mul(q[c][v], f2s(p.qmul));
@@ -181,7 +187,7 @@ __global__ void __launch_bounds__(FwdShape<T, RB>::THREADS) fwd_kernel(const Fwd
       if (k >= kmax) break;
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
-        const uint4 kr = k < cnt ? lds16(ks + k * RB + (c * TPR + t) * 16) : make_uint4(0, 0, 0, 0);
+        const uint4 kr = k < cnt ? lds16(ks + k * RB + (t * NC + c) * 16) : make_uint4(0, 0, 0, 0);
         float2 kf[PP];
         PR::load(kr, kf);
         float2 a2 = f2s(0.f);
@@ -199,7 +205,7 @@ __global__ void __launch_bounds__(FwdShape<T, RB>::THREADS) fwd_kernel(const Fwd
         }
         sc[k][c] = a2.x + a2.y;
       }
-      head_totals<NC>(sc[k], cph);
+      head_totals<NC, CPH>(sc[k]);
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
         if (GAT) sc[k][c] *= kLog2e;
@@ -224,7 +230,7 @@ __global__ void __launch_bounds__(FwdShape<T, RB>::THREADS) fwd_kernel(const Fwd
             const float pk = ex2(sc[k][c] - base);
             l[c] += pk;
             float2 vf[PP];
-            PR::load(lds16(vs + k * RB + (c * TPR + t) * 16), vf);
+            PR::load(lds16(vs + k * RB + (t * NC + c) * 16), vf);
 #pragma unroll
             for (int v = 0; v < PP; ++v) acc[c][v] = f2fma(f2s(pk), vf[v], acc[c][v]);
           }
@@ -315,6 +321,7 @@ __global__ void __launch_bounds__(FwdShape<T, RB>::THREADS) fwd_kernel(const Fwd
     __syncwarp();
   }
   cp_async_wait<0>();
+  ring.release(lane);
 }
 
 }  // namespace gattn

@@ -35,69 +35,100 @@ inline int persistent_grid(int bps, int warps_per_block, int num_sms, int64_t n_
   return (int)(g < 1 ? 1 : g);
 }
 
-#define GATTN_RB_CASES(X) X(32) X(64) X(128) X(256) X(512) X(1024) X(2048)
+// One (row bytes, head bytes) instantiation of a kernel; head bytes DB =
+// D * sizeof(T) in {16, ..., 512} and never above the row.
+template <typename T, int RB, int DB>
+struct Case {
+  static constexpr bool ok = DB <= RB;
 
-template <typename T>
-struct Launch {
-  static gattn_status fwd(int rb, int kind, const FwdParams& p, int num_sms, cudaStream_t st,
-                          int* grid_out) {
-#define GATTN_FWD_CASE(RB_)                                                        \
-  case RB_: {                                                                      \
-    using Sh = FwdShape<T, RB_>;                                                          \
-    static int cache[2] = {0, 0};                                                    \
-    auto k = kind == GATTN_SCORE_DOT ? fwd_kernel<T, RB_, GATTN_SCORE_DOT>                    \
-                                     : fwd_kernel<T, RB_, GATTN_SCORE_GATV2>;                 \
-    const int bps = blocks_per_sm(k, Sh::THREADS, Sh::SMEM, &cache[kind != 0]);       \
-    const int g = persistent_grid(bps, Sh::WARPS, num_sms, (p.n_items + kUnit - 1) / kUnit);               \
-    if (grid_out) *grid_out = g;                                                     \
-    k<<<g, Sh::THREADS, Sh::SMEM, st>>>(p);                                          \
-    return GATTN_OK;                                                               \
+  static gattn_status fwd(int kind, const FwdParams& p, int num_sms, cudaStream_t st, int* g) {
+    if constexpr (!ok) {
+      return GATTN_ERR_UNSUPPORTED;
+    } else {
+      using Sh = FwdShape<T, RB>;
+      static int cache[2] = {0, 0};
+      auto k = kind == GATTN_SCORE_DOT ? fwd_kernel<T, RB, DB, GATTN_SCORE_DOT>
+                                       : fwd_kernel<T, RB, DB, GATTN_SCORE_GATV2>;
+      return go(k, Sh::THREADS, Sh::WARPS, Sh::SMEM, &cache[kind != 0], p, num_sms, st, g);
+    }
   }
-    switch (rb) { GATTN_RB_CASES(GATTN_FWD_CASE) default: return GATTN_ERR_UNSUPPORTED; }
-#undef GATTN_FWD_CASE
+  static gattn_status csr(int kind, const BwdParams& p, int num_sms, cudaStream_t st, int* g) {
+    if constexpr (!ok) {
+      return GATTN_ERR_UNSUPPORTED;
+    } else {
+      using Sh = CsrShape<T, RB>;
+      static int cache[2] = {0, 0};
+      auto k = kind == GATTN_SCORE_DOT ? bwd_csr_kernel<T, RB, DB, GATTN_SCORE_DOT>
+                                       : bwd_csr_kernel<T, RB, DB, GATTN_SCORE_GATV2>;
+      return go(k, Sh::THREADS, Sh::WARPS, Sh::SMEM, &cache[kind != 0], p, num_sms, st, g);
+    }
   }
-  static gattn_status bwd_csr(int rb, int kind, const BwdParams& p, int num_sms, cudaStream_t st,
-                              int* grid_out) {
-#define GATTN_CSR_CASE(RB_)                                                         \
-  case RB_: {                                                                       \
-    using Sh = CsrShape<T, RB_>;                                                          \
-    static int cache[2] = {0, 0};                                                    \
-    auto k = kind == GATTN_SCORE_DOT ? bwd_csr_kernel<T, RB_, GATTN_SCORE_DOT>                    \
-                                     : bwd_csr_kernel<T, RB_, GATTN_SCORE_GATV2>;                 \
-    const int bps = blocks_per_sm(k, Sh::THREADS, Sh::SMEM, &cache[kind != 0]);       \
-    const int g = persistent_grid(bps, Sh::WARPS, num_sms, (p.n_items + kUnit - 1) / kUnit);               \
-    if (grid_out) *grid_out = g;                                                     \
-    k<<<g, Sh::THREADS, Sh::SMEM, st>>>(p);                                          \
-    return GATTN_OK;                                                                \
+  static gattn_status csc(int kind, const BwdParams& p, int num_sms, cudaStream_t st, int* g) {
+    if constexpr (!ok) {
+      return GATTN_ERR_UNSUPPORTED;
+    } else {
+      using Sh = CscShape<T, RB>;
+      static int cache[2] = {0, 0};
+      auto k = kind == GATTN_SCORE_DOT ? bwd_csc_kernel<T, RB, DB, GATTN_SCORE_DOT>
+                                       : bwd_csc_kernel<T, RB, DB, GATTN_SCORE_GATV2>;
+      return go(k, Sh::THREADS, Sh::WARPS, Sh::SMEM, &cache[kind != 0], p, num_sms, st, g);
+    }
   }
-    switch (rb) { GATTN_RB_CASES(GATTN_CSR_CASE) default: return GATTN_ERR_UNSUPPORTED; }
-#undef GATTN_CSR_CASE
-  }
-  static gattn_status bwd_csc(int rb, int kind, const BwdParams& p, int num_sms, cudaStream_t st,
-                              int* grid_out) {
-#define GATTN_CSC_CASE(RB_)                                                         \
-  case RB_: {                                                                       \
-    using Sh = CscShape<T, RB_>;                                                          \
-    static int cache[2] = {0, 0};                                                    \
-    auto k = kind == GATTN_SCORE_DOT ? bwd_csc_kernel<T, RB_, GATTN_SCORE_DOT>                    \
-                                     : bwd_csc_kernel<T, RB_, GATTN_SCORE_GATV2>;                 \
-    const int bps = blocks_per_sm(k, Sh::THREADS, Sh::SMEM, &cache[kind != 0]);       \
-    const int g = persistent_grid(bps, Sh::WARPS, num_sms, (p.n_items + kUnit - 1) / kUnit);               \
-    if (grid_out) *grid_out = g;                                                     \
-    k<<<g, Sh::THREADS, Sh::SMEM, st>>>(p);                                          \
-    return GATTN_OK;                                                                \
-  }
-    switch (rb) { GATTN_RB_CASES(GATTN_CSC_CASE) default: return GATTN_ERR_UNSUPPORTED; }
-#undef GATTN_CSC_CASE
+
+  template <typename Kern, typename P>
+  static gattn_status go(Kern k, int threads, int warps, int smem, int* cache, const P& p,
+                         int num_sms, cudaStream_t st, int* g) {
+    const int bps = blocks_per_sm(k, threads, smem, cache);
+    const int grid = persistent_grid(bps, warps, num_sms, (p.n_items + kUnit - 1) / kUnit);
+    if (g) *g = grid;
+    k<<<grid, threads, smem, st>>>(p);
+    return GATTN_OK;
   }
 };
 
-// Entry points implemented by attn_f32.cu / attn_bf16.cu.
-gattn_status launch_fwd(gattn_dtype dt, int rb, int kind, const FwdParams& p, int num_sms,
+// Runtime dispatch over the head bytes for one row size.
+template <typename T, int RB, int PASS, typename P>
+gattn_status dispatch_db(int db, int kind, const P& p, int num_sms, cudaStream_t st, int* g) {
+#define GATTN_DB_CASE(DB_)                                                     \
+  case DB_:                                                                    \
+    if constexpr (PASS == 0) return Case<T, RB, DB_>::fwd(kind, p, num_sms, st, g); \
+    else if constexpr (PASS == 1) return Case<T, RB, DB_>::csr(kind, p, num_sms, st, g); \
+    else return Case<T, RB, DB_>::csc(kind, p, num_sms, st, g);
+  switch (db) {
+    GATTN_DB_CASE(16)
+    GATTN_DB_CASE(32)
+    GATTN_DB_CASE(64)
+    GATTN_DB_CASE(128)
+    GATTN_DB_CASE(256)
+    GATTN_DB_CASE(512)
+    default:
+      return GATTN_ERR_UNSUPPORTED;
+  }
+#undef GATTN_DB_CASE
+}
+
+// Launchers for one (pass, dtype, row size); each lives in its own
+// translation unit (k_<pass>_<dtype>_<row bytes>.cu) so the library builds in
+// parallel.  PASS: 0 forward, 1 backward CSR pass, 2 backward CSC pass.
+#define GATTN_DECLARE_LAUNCHER(PASS_NAME, PT, TNAME, RB_)                               \
+  gattn_status launch_##PASS_NAME##_##TNAME##_##RB_(int db, int kind, const PT& p,     \
+                                                    int num_sms, cudaStream_t st, int* g);
+#define GATTN_FOR_ROWS(X, PASS_NAME, PT, TNAME) \
+  X(PASS_NAME, PT, TNAME, 32) X(PASS_NAME, PT, TNAME, 64) X(PASS_NAME, PT, TNAME, 128) \
+  X(PASS_NAME, PT, TNAME, 256) X(PASS_NAME, PT, TNAME, 512) X(PASS_NAME, PT, TNAME, 1024) \
+  X(PASS_NAME, PT, TNAME, 2048)
+GATTN_FOR_ROWS(GATTN_DECLARE_LAUNCHER, fwd, FwdParams, f32)
+GATTN_FOR_ROWS(GATTN_DECLARE_LAUNCHER, fwd, FwdParams, bf16)
+GATTN_FOR_ROWS(GATTN_DECLARE_LAUNCHER, csr, BwdParams, f32)
+GATTN_FOR_ROWS(GATTN_DECLARE_LAUNCHER, csr, BwdParams, bf16)
+GATTN_FOR_ROWS(GATTN_DECLARE_LAUNCHER, csc, BwdParams, f32)
+GATTN_FOR_ROWS(GATTN_DECLARE_LAUNCHER, csc, BwdParams, bf16)
+
+gattn_status launch_fwd(gattn_dtype dt, int rb, int db, int kind, const FwdParams& p, int num_sms,
                         cudaStream_t st, int* grid_out);
-gattn_status launch_bwd_csr(gattn_dtype dt, int rb, int kind, const BwdParams& p, int num_sms,
-                            cudaStream_t st, int* grid_out);
-gattn_status launch_bwd_csc(gattn_dtype dt, int rb, int kind, const BwdParams& p, int num_sms,
-                            cudaStream_t st, int* grid_out);
+gattn_status launch_bwd_csr(gattn_dtype dt, int rb, int db, int kind, const BwdParams& p,
+                            int num_sms, cudaStream_t st, int* grid_out);
+gattn_status launch_bwd_csc(gattn_dtype dt, int rb, int db, int kind, const BwdParams& p,
+                            int num_sms, cudaStream_t st, int* grid_out);
 
 }  // namespace gattn

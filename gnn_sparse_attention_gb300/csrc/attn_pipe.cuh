@@ -22,11 +22,13 @@
 //            FIRST/LAST flags) are generated and its source indices copied
 //            (cp.async) 2S - 1 stages before t is computed;
 //   rows   : stage t's rows (Q/K/V or their gradients' operands) are copied
-//            (cp.async, 16-byte pieces) S - 1 stages before t is computed.
-// A stage holds SE edges of each of the G items; its rows land in shared
-// memory with each thread's chunks placed so that the G groups' reads of one
-// chunk index are conflict-free.  cp.async.wait_group is a hardware wait on
-// the thread's own copies, so nothing ever spins.
+//            by the TMA engine, one cp.async.bulk per row issued by one lane,
+//            S - 1 stages before t is computed; completion is counted in
+//            bytes on the stage slot's mbarrier.
+// A stage holds SE edges of each of the G items.  Index copies complete
+// through cp.async.wait_group (a hardware wait on the thread's own copies);
+// the row barriers are polled with mbarrier.try_wait under an iteration
+// limit, after which the kernel records an error instead of hanging.
 #pragma once
 
 #include "gattn_internal.cuh"
@@ -50,26 +52,28 @@ struct Lay {
   static constexpr int TPR = RB / PT;               // threads per row
   static constexpr int G = 32 / TPR;                // groups (items) per warp
   static constexpr int NCH = RB / 16;               // chunks per row
-  // edges per item per stage: ~8 KB of gathered rows per stage
-  static constexpr int SE0 = 8192 / (2 * RB) / G;
+  // edges per item per stage: ~4 KB of gathered rows per stage
+  static constexpr int SE0 = 4096 / (2 * RB) / G;
   static constexpr int SE1 = SE0 < 1 ? 1 : SE0;
   static constexpr int SE = SE1 * G > 32 ? 32 / G : SE1;  // at most 32 edges per stage
   static constexpr int B = G * SE;                  // edges per stage
   static constexpr int IDXB = (B * 4 + 15) / 16 * 16;
-  // the warp's descriptor ring, index ring and unit buffer
-  static constexpr int META = kRing * G * 16 + kRing * IDXB + kUnit * 16;
+  // the warp's descriptor ring, index ring, unit buffer and row barriers
+  static constexpr int META = kRing * G * 16 + kRing * IDXB + kUnit * 16 + 16 * ((kStages + 1) / 2);
   static_assert(TPR >= 1 && TPR <= 32 && 32 % TPR == 0, "thread layout");
   static_assert(B <= 32, "stage edges");
   // shared-memory position (in 16-byte units) of global chunk ch of a row
   __device__ __forceinline__ static int pos(int ch) { return (ch % NC) * TPR + ch / NC; }
 };
 
-// Warps per block: as many as keep a block under a quarter of the SM's shared
-// memory (so that several blocks fit), between 1 and 8.
+// Warps per block: the count (1..8) that fits the most warps in an SM's
+// shared memory (1 KB per block is reserved by the system); ties go to the
+// larger block.
 template <int WARP_BYTES>
 struct WarpsFor {
-  static constexpr int raw = (kSmemPerSm / 4) / WARP_BYTES;
-  static constexpr int value = raw < 1 ? 1 : (raw > 8 ? 8 : raw);
+  static constexpr int fit(int w) { return (kSmemPerSm / (w * WARP_BYTES + 1024)) * w; }
+  static constexpr int best(int w, int bw) { return w > 8 ? bw : best(w + 1, fit(w) >= fit(bw) ? w : bw); }
+  static constexpr int value = best(1, 1);
 };
 
 // ---------------------------------------------------------------------------
@@ -95,6 +99,51 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 __device__ __forceinline__ uint4 lds16(const void* p) {
   return *reinterpret_cast<const uint4*>(p);
+}
+
+// mbarrier + TMA bulk copies (global -> this CTA's shared memory)
+constexpr uint32_t kWaitLimit = 1u << 22;  // polls before a wait is declared failed
+__device__ __forceinline__ void mbar_init(uint64_t* bar, int count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+__device__ __forceinline__ void mbar_inval(uint64_t* bar) {
+  asm volatile("mbarrier.inval.shared::cta.b64 [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the completion of the barrier phase with this parity.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  for (uint32_t it = 0; it < kWaitLimit; ++it)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -138,27 +187,31 @@ __device__ __forceinline__ float2 f2fma(float2 a, float2 b, float2 c) { return _
 __device__ __forceinline__ float2 f2mul(float2 a, float2 b) { return __fmul2_rn(a, b); }
 __device__ __forceinline__ float2 f2s(float s) { return make_float2(s, s); }
 
-// Combine per-chunk partial sums into per-head totals.  cph = chunks per
-// head (D / VEC, runtime).  Chunks of one thread that share a head are
-// summed in-thread; heads wider than a thread reduce over tph lanes.
-// Every lane of the warp must call this (it may shuffle).
-template <int NC>
-__device__ __forceinline__ void head_totals(float* x, int cph) {
-  if (cph == 1) return;
-  if (NC == 2 || cph >= NC) {
+// Combine per-chunk partial sums into per-head totals.  CPH = 16-byte chunks
+// per head.  Chunks of one thread that share a head are summed in-thread;
+// heads wider than a thread (CPH > NC) reduce over CPH / NC lanes.  Every
+// lane of the warp must call this (it may shuffle).
+template <int NC, int CPH>
+__device__ __forceinline__ void head_totals(float* x) {
+  if constexpr (CPH == 1) {
+    return;
+  } else if constexpr (CPH >= NC) {
     float s = 0.f;
 #pragma unroll
     for (int c = 0; c < NC; ++c) s += x[c];
-    const int tph = cph / NC;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1)
-      if (o < tph) s += __shfl_xor_sync(0xffffffffu, s, o);
+    for (int o = 1; o < CPH / NC; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
 #pragma unroll
     for (int c = 0; c < NC; ++c) x[c] = s;
-  } else {  // NC == 4, cph == 2
-    const float a = x[0] + x[1], b = x[2] + x[3];
-    x[0] = x[1] = a;
-    x[2] = x[3] = b;
+  } else {  // 1 < CPH < NC: in-thread groups of CPH chunks
+#pragma unroll
+    for (int c0 = 0; c0 < NC; c0 += CPH) {
+      float s = 0.f;
+#pragma unroll
+      for (int c = 0; c < CPH; ++c) s += x[c0 + c];
+#pragma unroll
+      for (int c = 0; c < CPH; ++c) x[c0 + c] = s;
+    }
   }
 }
 
@@ -306,11 +359,35 @@ struct Ring {
   int4* desc;     // [kRing][G]
   uint8_t* ix;    // [kRing][IDXB]
   int4* items;    // [kUnit]
-  __device__ __forceinline__ void init(uint8_t* base) {
+  uint64_t* bar;  // [kStages] row barriers
+  __device__ __forceinline__ void init(uint8_t* base, int lane) {
     data = base;
     desc = reinterpret_cast<int4*>(base + kStages * STAGE);
     ix = reinterpret_cast<uint8_t*>(desc + kRing * L::G);
     items = reinterpret_cast<int4*>(ix + kRing * L::IDXB);
+    bar = reinterpret_cast<uint64_t*>(items + kUnit);
+    if (lane == 0) {
+      for (int k = 0; k < kStages; ++k) mbar_init(bar + k, 1);
+      mbar_init_fence();
+    }
+    __syncwarp();
+  }
+  __device__ __forceinline__ void release(int lane) {
+    __syncwarp();
+    if (lane == 0)
+      for (int k = 0; k < kStages; ++k) mbar_inval(bar + k);
+    __syncwarp();
+  }
+  __device__ __forceinline__ uint64_t* bar_at(int t) { return bar + (t % kStages); }
+  // Wait for stage t's rows.  On a failed (timed-out) wait, record it in
+  // *err and wait, again bounded, for the rows of the stages issued after t
+  // so that no copy into this warp's ring is still in flight; returns false.
+  __device__ __forceinline__ bool wait_rows(int t, int32_t* err, int lane) {
+    if (mbar_wait(bar_at(t), (t / kStages) & 1)) return true;
+    if (lane == 0) atomicOr(err, 1);
+    for (int u = t + 1; u < t + kStages; ++u) mbar_wait(bar_at(u), (u / kStages) & 1);
+    cp_async_wait<0>();
+    return false;
   }
   __device__ __forceinline__ int4* desc_at(int t) { return desc + (t % kRing) * L::G; }
   __device__ __forceinline__ int* ix_at(int t) {

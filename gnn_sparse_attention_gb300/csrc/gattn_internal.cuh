@@ -75,10 +75,11 @@ struct Plan {
   int32_t* cnt_dq = nullptr;   // [n_inner]
   int32_t* cnt_dkv = nullptr;  // [n_inner_src]
   int32_t* cnt_da = nullptr;   // [1]
+  int32_t* err = nullptr;      // [1] nonzero once a kernel's bounded wait gave up
   std::vector<void*> allocs;   // every device buffer above, freed by destroy
 };
 
-constexpr int kMaxBlocksPerSm = 8;  // grid cap of the persistent kernels (bounds da partials)
+constexpr int kMaxBlocksPerSm = 32;  // grid cap of the persistent kernels (bounds da partials)
 
 // Work units: runs of consecutive items whose edges are contiguous, at most
 // kUnitItems items, all starting inside one kUnitBucket-edge bucket of the

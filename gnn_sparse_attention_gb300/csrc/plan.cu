@@ -627,6 +627,8 @@ gattn_status plan_build(Plan* p, const int32_t* indptr, const int32_t* indices, 
   GATTN_CUDA(plan_alloc(p, &p->cnt_dq, d.n_inner));
   GATTN_CUDA(plan_alloc(p, &p->cnt_dkv, s.n_inner));
   GATTN_CUDA(plan_alloc(p, &p->cnt_da, 1));
+  GATTN_CUDA(plan_alloc(p, &p->err, 1));
+  GATTN_CUDA(cudaMemsetAsync(p->err, 0, 4, st));
   GATTN_CUDA(cudaMemsetAsync(p->cnt_fwd, 0, (d.n_inner ? d.n_inner : 1) * 4, st));
   GATTN_CUDA(cudaMemsetAsync(p->cnt_dq, 0, (d.n_inner ? d.n_inner : 1) * 4, st));
   GATTN_CUDA(cudaMemsetAsync(p->cnt_dkv, 0, (s.n_inner ? s.n_inner : 1) * 4, st));

@@ -67,7 +67,7 @@ typedef enum {
   GATTN_ERR_UNSUPPORTED = 3, /* (H, D, dtype) outside the supported set */
   GATTN_ERR_OOM = 4,         /* plan buffers could not be allocated */
   GATTN_ERR_CUDA = 5,        /* a CUDA runtime call or kernel launch failed */
-  GATTN_ERR_TIMEOUT = 6      /* reserved: no entry point waits on the device */
+  GATTN_ERR_TIMEOUT = 6      /* a kernel gave up a bounded wait (see gattn_plan_check_errors) */
 } gattn_status;
 
 typedef enum { GATTN_F32 = 0, GATTN_BF16 = 1 } gattn_dtype;
@@ -149,6 +149,15 @@ GATTN_API gattn_status gattn_plan_export(const gattn_plan* plan, int32_t* deg, i
                                int32_t* light, int32_t* chunks, int32_t* indptrT,
                                int32_t* csc_dst, int32_t* csc_eid, int32_t* outdeg,
                                int32_t* hist_out, int32_t* light_src, int32_t* src_chunks);
+
+/*
+ * Synchronise the device and report whether any kernel run with this plan
+ * since the last check gave up a bounded wait for its asynchronous copies
+ * (every wait in the kernels has an iteration limit; on expiry the kernel
+ * records the failure and returns instead of hanging; its outputs are then
+ * undefined).  Returns GATTN_OK or GATTN_ERR_TIMEOUT and clears the record.
+ */
+GATTN_API gattn_status gattn_plan_check_errors(const gattn_plan* plan);
 
 /*
  * Bytes of caller-owned device workspace that gattn_fwd / gattn_bwd need

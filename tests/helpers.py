@@ -92,6 +92,7 @@ class GpuCase:
         out, lse = gb.gattn_fwd(self.plan, Q, K, V, self.score)
         dQ, dK, dV, da = gb.gattn_bwd(self.plan, Q, K, V, out, G, lse, self.score)
         torch.cuda.synchronize()
+        gb.gattn_plan_check_errors(self.plan)
         self.out_t = out
         return {"out": out, "lse": lse, "dQ": dQ, "dK": dK, "dV": dV, "da": da}
 
