@@ -7,6 +7,7 @@
 #include <new>
 
 #include "attn_launch.cuh"
+#include "tma.cuh"
 
 struct gattn_plan {
   gattn::Plan p;
@@ -364,6 +365,15 @@ gattn_status gattn_fwd(const gattn_plan* plan, int32_t H, int32_t D, gattn_dtype
   f.sorted = p.sorted;
   f.n_items = p.n_chunks + p.n_light;
   f.n_chunks = p.n_chunks;
+  f.N = p.N;
+  {
+    const int es = (int)dtype_size(dtype);
+    const bool bf = dtype == GATTN_BF16;
+    const int64_t HD = int64_t(H) * D;
+    if (!encode_rows_map(&f.mq, Q, es, bf, p.N, HD) || !encode_rows_map(&f.mk, K, es, bf, p.N, HD) ||
+        !encode_rows_map(&f.mv, V, es, bf, p.N, HD))
+      return GATTN_ERR_CUDA;
+  }
   f.indices = p.indices;
   f.Q = Q;
   f.K = K;
@@ -448,6 +458,18 @@ gattn_status gattn_bwd_dq(const gattn_plan* plan, int32_t H, int32_t D, gattn_dt
   b.sorted = p.sorted;
   b.n_items = p.n_chunks + p.n_light;
   b.n_chunks = p.n_chunks;
+  b.N = p.N;
+  {
+    const int es = (int)dtype_size(dtype);
+    const bool bf = dtype == GATTN_BF16;
+    const int64_t HD = int64_t(H) * D;
+    if (!encode_rows_map(&b.mi0, Q, es, bf, p.N, HD) ||
+        !encode_rows_map(&b.mi1, dout, es, bf, p.N, HD) ||
+        !encode_rows_map(&b.mi2, out, es, bf, p.N, HD) ||
+        !encode_rows_map(&b.me0, K, es, bf, p.N, HD) || !encode_rows_map(&b.me1, V, es, bf, p.N, HD) ||
+        (b.rows16 && !encode_rows_map(&b.ms0, lse, 4, false, p.N, H)))
+      return GATTN_ERR_CUDA;
+  }
   b.idx = p.indices;
   b.G1 = dQ;
   b.G2 = nullptr;
@@ -478,6 +500,18 @@ gattn_status gattn_bwd_dkdv(const gattn_plan* plan, int32_t H, int32_t D, gattn_
   b.sorted = p.sorted_src;
   b.n_items = p.n_src_chunks + p.n_light_src;
   b.n_chunks = p.n_src_chunks;
+  b.N = p.N;
+  {
+    const int es = (int)dtype_size(dtype);
+    const bool bf = dtype == GATTN_BF16;
+    const int64_t HD = int64_t(H) * D;
+    if (!encode_rows_map(&b.mi0, K, es, bf, p.N, HD) || !encode_rows_map(&b.mi1, V, es, bf, p.N, HD) ||
+        !encode_rows_map(&b.me0, Q, es, bf, p.N, HD) ||
+        !encode_rows_map(&b.me1, dout, es, bf, p.N, HD) ||
+        (b.rows16 && !encode_rows_map(&b.ms0, lse, 4, false, p.N, H)) ||
+        (b.delta16 && !encode_rows_map(&b.ms1, b.delta, 4, false, p.N, H)))
+      return GATTN_ERR_CUDA;
+  }
   b.idx = p.csc_dst;
   b.G1 = dK;
   b.G2 = dV;

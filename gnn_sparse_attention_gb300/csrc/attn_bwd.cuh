@@ -27,10 +27,16 @@
 namespace gattn {
 
 struct BwdParams {
+  // row-gather maps (tma.cuh).  Pass 1: mi0..mi2 = Q, dO, O (item rows),
+  // me0, me1 = K, V (edge rows), ms0 = lse (item stat rows).  Pass 2: mi0,
+  // mi1 = K, V (item rows), me0, me1 = Q, dO (edge rows), ms0, ms1 = lse,
+  // Delta (edge stat rows).
+  CUtensorMap mi0, mi1, mi2, me0, me1, ms0, ms1;
   const int4* items;   // plan items (w = heavy id of a chunk)
   const int4* sorted;  // items by decreasing length
   int64_t n_items;
   int64_t n_chunks;    // items [0, n_chunks) are heavy chunks
+  int N;               // rows; row index N is the zero-filled pad row
   const int32_t* idx;  // pass 1: CSR sources; pass 2: CSC destinations
   const void* Q;
   const void* K;
@@ -47,8 +53,8 @@ struct BwdParams {
   float scale;         // DOT: scale
   float slope;
   int H, D;
-  int rows16;          // lse rows may be copied in 16-byte pieces (H % 4 == 0, lse 16-B aligned)
-  int delta16;         // Delta rows may be copied in 16-byte pieces (H % 4 == 0)
+  int rows16;          // lse rows are gathered by TMA (H % 4 == 0, lse 16-B aligned)
+  int delta16;         // Delta rows are gathered by TMA (H % 4 == 0)
   float* part;         // partials per tree slot: pass 1 [slots][HD], pass 2 [slots][2*HD]
   Tree tree;           // merge trees of the heavy items of this pass
   float* da_part;      // [gridDim.x][HD]
@@ -66,9 +72,12 @@ template <typename T, int RB>
 struct CsrShape {
   using L = Lay<T, RB>;
   static constexpr int LS = StatBytes<RB>::value;
-  // per item: Q, dO, O rows and the lse row; per edge: K row, V row
-  static constexpr int STAGE = L::G * (3 * RB + LS) + 2 * L::B * RB;
-  static constexpr int WARP_BYTES = kStages * STAGE + L::META;
+  // per item slot: Q, dO, O rows and the lse row; per edge: K row, V row
+  static constexpr int OL = 3 * L::QR * RB;             // lse sets
+  static constexpr int OK = OL + L::QR / 4 * L::SSB;    // K rows
+  static constexpr int OV = OK + L::B * RB;             // V rows
+  static constexpr int STAGE = OV + L::B * RB;
+  static constexpr int WARP_BYTES = align128(kStages * STAGE + L::META);
   static constexpr int WARPS = WarpsFor<WARP_BYTES>::value;
   static constexpr int THREADS = 32 * WARPS;
   static constexpr int SMEM = WARPS * WARP_BYTES;
@@ -78,30 +87,33 @@ template <typename T, int RB>
 struct CscShape {
   using L = Lay<T, RB>;
   static constexpr int LS = StatBytes<RB>::value;
-  // per item: K, V rows; per edge: Q row, dO row, lse row, Delta row
-  static constexpr int STAGE = L::G * 2 * RB + L::B * (2 * RB + 2 * LS);
-  static constexpr int WARP_BYTES = kStages * STAGE + L::META;
+  // per item slot: K, V rows; per edge: Q row, dO row, lse row, Delta row
+  static constexpr int OQE = 2 * L::QR * RB;            // Q rows of the edges
+  static constexpr int OGE = OQE + L::B * RB;           // dO rows
+  static constexpr int OLS = OGE + L::B * RB;           // lse sets
+  static constexpr int ODL = OLS + L::B / 4 * L::SSB;   // Delta sets
+  static constexpr int STAGE = ODL + L::B / 4 * L::SSB;
+  static constexpr int WARP_BYTES = align128(kStages * STAGE + L::META);
   static constexpr int WARPS = WarpsFor<WARP_BYTES>::value;
   static constexpr int THREADS = 32 * WARPS;
   static constexpr int SMEM = WARPS * WARP_BYTES;
 };
 
-// Copy the fp32 rows src + node_r * H (r < n, node_r < 0: skip) to
-// dst + r * LS, node_r taken from lane r of `nodes`.  Uniform trip count.
-template <int LS>
+// Copy the fp32 rows src + node_r * H (r < n, node_r < 0: skip) into the
+// stat-set layout (row r at set r / 4, slot r % 4, H floats a row) with 4-byte cp.async, node_r taken from lane r of
+// `nodes` (the fallback when the rows are not whole 16-byte pieces).
+// Uniform trip count.
+template <int SSB>
 __device__ __forceinline__ void copy_stat_rows(uint8_t* dst, const float* src, int nodes, int n,
-                                               int H, bool rows16, int lane) {
+                                               int H, int lane) {
   constexpr unsigned FULL = 0xffffffffu;
-  const int per = rows16 ? H / 4 : H;  // pieces per row
-  const int trips = (n * per + 31) / 32;
+  const int trips = (n * H + 31) / 32;
   for (int tr = 0; tr < trips; ++tr) {
     const int x = tr * 32 + lane;
-    const int r = x / per, f = x % per;
+    const int r = x / H, f = x % H;
     const int i = __shfl_sync(FULL, nodes, r & 31);
-    if (x < n * per && i >= 0) {
-      if (rows16) cp_async16(dst + r * LS + f * 16, src + int64_t(i) * H + f * 4);
-      else cp_async4(dst + r * LS + f * 4, src + int64_t(i) * H + f);
-    }
+    if (x < n * H && i >= 0)
+      cp_async4(dst + (r / 4) * SSB + ((r % 4) * H + f) * 4, src + int64_t(i) * H + f);
   }
 }
 
@@ -109,7 +121,7 @@ __device__ __forceinline__ void copy_stat_rows(uint8_t* dst, const float* src, i
 // pass 1: CSR
 // ---------------------------------------------------------------------------
 template <typename T, int RB, int DB, int KIND>
-__global__ void __launch_bounds__(CsrShape<T, RB>::THREADS) bwd_csr_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(CsrShape<T, RB>::THREADS) bwd_csr_kernel(const __grid_constant__ BwdParams p) {
   using L = Lay<T, RB>;
   using Sh = CsrShape<T, RB>;
   using PR = Pairs<T>;
@@ -120,16 +132,11 @@ __global__ void __launch_bounds__(CsrShape<T, RB>::THREADS) bwd_csr_kernel(const
   constexpr int CPH = DB / 16;            // 16-byte chunks per head
   constexpr bool GAT = KIND == GATTN_SCORE_GATV2;
   constexpr unsigned FULL = 0xffffffffu;
-  extern __shared__ __align__(16) uint8_t smem[];
+  extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x & 31;
   const int g = lane / TPR, t = lane % TPR;
   Ring<L, Sh::STAGE> ring;
   ring.init(smem + (threadIdx.x >> 5) * Sh::WARP_BYTES, lane);
-  const char* __restrict__ Qb = static_cast<const char*>(p.Q);
-  const char* __restrict__ Kb = static_cast<const char*>(p.K);
-  const char* __restrict__ Vb = static_cast<const char*>(p.V);
-  const char* __restrict__ Ob = static_cast<const char*>(p.O);
-  const char* __restrict__ dOb = static_cast<const char*>(p.dO);
 
   int elem[NC], head[NC];
   bool hw[NC];
@@ -155,51 +162,62 @@ __global__ void __launch_bounds__(CsrShape<T, RB>::THREADS) bwd_csr_kernel(const
   BundleCursor<G, SE> cur;
   cur.start(p.sorted, p.n_items, p.idx, warp, nwarps, ring.items, lane);
 
-  // stage: [G][Q, dO, O rows] [G][lse row] [B][K row] [B][V row]; rows by
-  // TMA bulk copies (lse rows too when they are 16-byte pieces, else 4-byte
-  // cp.async).  Row r: [0,G) Q, [G,2G) dO, [2G,3G) O, [3G,4G) lse, then
-  // [4G, 4G+B) K and [4G+B, 4G+2B) V.
+  // stage: [QR][Q row] [QR][dO row] [QR][O row] [QR][lse row] [B][K row]
+  // [B][V row].  TMA gathers from lane 0 (item rows only for 4-row sets that
+  // hold a starting item, pad row N elsewhere); lse rows by gather when
+  // they are whole 16-byte pieces, else by 4-byte cp.async.
+  constexpr int OQ = 0, ODO = L::QR * RB, OO = 2 * L::QR * RB;
+  constexpr int OL = Sh::OL, OK = Sh::OK, OV = Sh::OV;
   auto issue = [&](int s) {
     const int4* dsc = ring.desc_at(s);
-    const int4 dg = lane < G ? dsc[lane] : make_int4(-1, 0, 0, 0);
-    if (__shfl_sync(FULL, dg.x, 0) != -3) {
+    if (lane == 0 && dsc[0].x != -3) {
       uint8_t* st = ring.stage_at(s);
       uint64_t* bar = ring.bar_at(s);
-      const int ge = (lane / SE) & 31;
-      const int cn = __shfl_sync(FULL, dg.x >= 0 ? (dg.z & kCntMask) : 0, ge);
-      const int jv = (lane < B && lane % SE < cn) ? ring.ix_at(s)[lane] : -1;
-      const int fnode = (lane < G && dg.x >= 0 && (dg.z & kFirst)) ? dg.x : -1;
-      const int nq = __popc(__ballot_sync(FULL, fnode >= 0));
-      const int ne = __popc(__ballot_sync(FULL, jv >= 0));
-      const uint32_t bytes = nq * (3 * RB + (p.rows16 ? 4 * p.H : 0)) + ne * 2 * RB;
-      fence_proxy_async();
-      if (lane == 0) mbar_expect_tx(bar, bytes);
-      __syncwarp();
-      if (!p.rows16) copy_stat_rows<LS>(st + G * 3 * RB, p.lse, fnode, G, p.H, false, lane);
-      uint8_t* kd = st + G * (3 * RB + LS);
+      const int* ix = ring.ix_at(s);
+      auto qrow = [&](int gg) {
+        if (gg >= G) return p.N;
+        const int4 dd = dsc[gg];
+        return (dd.x >= 0 && (dd.z & kFirst)) ? dd.x : p.N;
+      };
+      auto erow = [&](int b) {
+        const int4 dd = dsc[b / SE];
+        return (dd.x >= 0 && b % SE < (dd.z & kCntMask)) ? ix[b] : p.N;
+      };
+      uint32_t qmask = 0;
 #pragma unroll
-      for (int r0 = 0; r0 < 4 * G + 2 * B; r0 += 32) {
-        const int r = r0 + lane;
-        const int b = r < 4 * G + B ? r - 4 * G : r - 4 * G - B;
-        const int node = __shfl_sync(FULL, fnode, (r % G) & 31);
-        const int j = __shfl_sync(FULL, jv, b & 31);
-        if (r < 4 * G) {
-          const int gg = r % G, kind = r / G;
-          if (node >= 0) {
-            if (kind < 3) {
-              const char* src = (kind == 0 ? Qb : (kind == 1 ? dOb : Ob)) + int64_t(node) * RB;
-              bulk_g2s(st + gg * 3 * RB + kind * RB, src, RB, bar);
-            } else if (p.rows16) {
-              bulk_g2s(st + G * 3 * RB + gg * LS, p.lse + int64_t(node) * p.H, 4 * p.H, bar);
-            }
-          }
-        } else if (r < 4 * G + B) {
-          if (j >= 0) bulk_g2s(kd + b * RB, Kb + int64_t(j) * RB, RB, bar);
-        } else if (r < 4 * G + 2 * B) {
-          if (j >= 0) bulk_g2s(kd + B * RB + b * RB, Vb + int64_t(j) * RB, RB, bar);
+      for (int q4 = 0; q4 < L::QR / 4; ++q4) {
+        bool any = false;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) any |= qrow(4 * q4 + j) != p.N;
+        qmask |= uint32_t(any) << q4;
+      }
+      const uint32_t qset = 3 * L::SET_BYTES + (p.rows16 ? 16 * p.H : 0);
+      fence_proxy_async();
+      mbar_expect_tx(bar, __popc(qmask) * qset + 2 * (B / 4) * L::SET_BYTES);
+#pragma unroll
+      for (int q4 = 0; q4 < L::QR / 4; ++q4)
+        if ((qmask >> q4) & 1) {
+          const int r0 = qrow(4 * q4), r1 = qrow(4 * q4 + 1), r2 = qrow(4 * q4 + 2),
+                    r3 = qrow(4 * q4 + 3);
+          L::gather(st + OQ, 4 * q4, &p.mi0, r0, r1, r2, r3, bar);
+          L::gather(st + ODO, 4 * q4, &p.mi1, r0, r1, r2, r3, bar);
+          L::gather(st + OO, 4 * q4, &p.mi2, r0, r1, r2, r3, bar);
+          if (p.rows16) tma_gather4(st + OL + q4 * L::SSB, &p.ms0, 0, r0, r1, r2, r3, bar);
         }
+#pragma unroll
+      for (int b4 = 0; b4 < B / 4; ++b4) {
+        const int r0 = erow(4 * b4), r1 = erow(4 * b4 + 1), r2 = erow(4 * b4 + 2),
+                  r3 = erow(4 * b4 + 3);
+        L::gather(st + OK, 4 * b4, &p.me0, r0, r1, r2, r3, bar);
+        L::gather(st + OV, 4 * b4, &p.me1, r0, r1, r2, r3, bar);
       }
     }
+    if (!p.rows16) {  // lse rows of starting items by 4-byte copies
+      const int4 dg = lane < G ? dsc[lane] : make_int4(-1, 0, 0, 0);
+      const int fnode = (dsc[0].x != -3 && lane < G && dg.x >= 0 && (dg.z & kFirst)) ? dg.x : -1;
+      copy_stat_rows<L::SSB>(ring.stage_at(s) + OL, p.lse, fnode, G, p.H, lane);
+    }
+    __syncwarp();
     cp_async_commit();
   };
 
@@ -235,10 +253,10 @@ __global__ void __launch_bounds__(CsrShape<T, RB>::THREADS) bwd_csr_kernel(const
       for (int c = 0; c < NC; ++c) {
         float2 o[PP];
         if (first) {
-          const uint8_t* rows = st + g * 3 * RB + (t * NC + c) * 16;
-          PR::load(lds16(rows), q[c]);
-          PR::load(lds16(rows + RB), gq[c]);
-          PR::load(lds16(rows + 2 * RB), o);
+          const int x = L::off(g, (t * NC + c) * 16);
+          PR::load(lds16(st + OQ + x), q[c]);
+          PR::load(lds16(st + ODO + x), gq[c]);
+          PR::load(lds16(st + OO + x), o);
         } else {
 #pragma unroll
           for (int v = 0; v < PP; ++v) o[v] = f2s(0.f);
@@ -250,7 +268,7 @@ __global__ void __launch_bounds__(CsrShape<T, RB>::THREADS) bwd_csr_kernel(const
       }
       head_totals<NC, CPH>(part);
       if (first) {
-        const float* ls = reinterpret_cast<const float*>(st + G * 3 * RB + g * LS);
+        const float* ls = reinterpret_cast<const float*>(st + OL + (g / 4) * L::SSB) + (g % 4) * p.H;
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
           dlt[c] = part[c];
@@ -268,8 +286,8 @@ __global__ void __launch_bounds__(CsrShape<T, RB>::THREADS) bwd_csr_kernel(const
       }
     }
 
-    const uint8_t* ks = st + G * (3 * RB + LS) + g * SE * RB;
-    const uint8_t* vs = ks + B * RB;
+    const uint8_t* ks = st + OK;
+    const uint8_t* vs = st + OV;
     const int kmax = __reduce_max_sync(FULL, cnt);
 #pragma unroll
     for (int k = 0; k < SE; ++k) {
@@ -279,7 +297,7 @@ __global__ void __launch_bounds__(CsrShape<T, RB>::THREADS) bwd_csr_kernel(const
       float2 kf[NC][PP];
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
-        const int off = k * RB + (t * NC + c) * 16;
+        const int off = L::off(g * SE + k, (t * NC + c) * 16);
         float2 vf[PP];
         PR::load(valid ? lds16(ks + off) : make_uint4(0, 0, 0, 0), kf[c]);
         PR::load(valid ? lds16(vs + off) : make_uint4(0, 0, 0, 0), vf);
@@ -390,7 +408,7 @@ __global__ void __launch_bounds__(CsrShape<T, RB>::THREADS) bwd_csr_kernel(const
     // warp -> block -> last block over block partials, all in fixed order
     __syncthreads();  // every warp is done with its ring: reuse shared memory
     float* s_da = reinterpret_cast<float*>(smem);  // [WARPS][HD]
-    __shared__ int s_last;
+    int& s_last = *reinterpret_cast<int*>(smem + Sh::WARPS * HD * 4);
 #pragma unroll
     for (int o = TPR; o < 32; o <<= 1)
 #pragma unroll
@@ -436,7 +454,7 @@ __global__ void __launch_bounds__(CsrShape<T, RB>::THREADS) bwd_csr_kernel(const
 // pass 2: CSC
 // ---------------------------------------------------------------------------
 template <typename T, int RB, int DB, int KIND>
-__global__ void __launch_bounds__(CscShape<T, RB>::THREADS) bwd_csc_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(CscShape<T, RB>::THREADS) bwd_csc_kernel(const __grid_constant__ BwdParams p) {
   using L = Lay<T, RB>;
   using Sh = CscShape<T, RB>;
   using PR = Pairs<T>;
@@ -447,15 +465,11 @@ __global__ void __launch_bounds__(CscShape<T, RB>::THREADS) bwd_csc_kernel(const
   constexpr int CPH = DB / 16;            // 16-byte chunks per head
   constexpr bool GAT = KIND == GATTN_SCORE_GATV2;
   constexpr unsigned FULL = 0xffffffffu;
-  extern __shared__ __align__(16) uint8_t smem[];
+  extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x & 31;
   const int g = lane / TPR, t = lane % TPR;
   Ring<L, Sh::STAGE> ring;
   ring.init(smem + (threadIdx.x >> 5) * Sh::WARP_BYTES, lane);
-  const char* __restrict__ Qb = static_cast<const char*>(p.Q);
-  const char* __restrict__ Kb = static_cast<const char*>(p.K);
-  const char* __restrict__ Vb = static_cast<const char*>(p.V);
-  const char* __restrict__ dOb = static_cast<const char*>(p.dO);
 
   int elem[NC], head[NC];
 #pragma unroll
@@ -477,53 +491,67 @@ __global__ void __launch_bounds__(CscShape<T, RB>::THREADS) bwd_csc_kernel(const
   BundleCursor<G, SE> cur;
   cur.start(p.sorted, p.n_items, p.idx, warp, nwarps, ring.items, lane);
 
-  // stage: [G][K, V rows] [B][Q row] [B][dO row] [B][lse row] [B][Delta row];
-  // rows by TMA bulk copies (stat rows too when they are 16-byte pieces).
-  // Row r: [0,G) K, [G,2G) V, [2G, 2G+B) Q, [2G+B, 2G+2B) dO,
-  // [2G+2B, 2G+3B) lse, [2G+3B, 2G+4B) Delta.
+  // stage: [QR][K row] [QR][V row] [B][Q row] [B][dO row] [B][lse row]
+  // [B][Delta row].  TMA gathers from lane 0 (pad row N in unused slots);
+  // stat rows by gather when they are whole 16-byte pieces, else by 4-byte
+  // cp.async.
+  constexpr int OKI = 0, OVI = L::QR * RB;
+  constexpr int OQE = Sh::OQE, OGE = Sh::OGE, OLS = Sh::OLS, ODL = Sh::ODL;
   auto issue = [&](int s) {
     const int4* dsc = ring.desc_at(s);
-    const int4 dg = lane < G ? dsc[lane] : make_int4(-1, 0, 0, 0);
-    if (__shfl_sync(FULL, dg.x, 0) != -3) {
+    if (lane == 0 && dsc[0].x != -3) {
       uint8_t* st = ring.stage_at(s);
       uint64_t* bar = ring.bar_at(s);
-      const int ge = (lane / SE) & 31;
-      const int cn = __shfl_sync(FULL, dg.x >= 0 ? (dg.z & kCntMask) : 0, ge);
-      const int jv = (lane < B && lane % SE < cn) ? ring.ix_at(s)[lane] : -1;
-      const int fnode = (lane < G && dg.x >= 0 && (dg.z & kFirst)) ? dg.x : -1;
-      const int nq = __popc(__ballot_sync(FULL, fnode >= 0));
-      const int ne = __popc(__ballot_sync(FULL, jv >= 0));
-      const uint32_t bytes =
-          nq * 2 * RB + ne * (2 * RB + (p.rows16 ? 4 * p.H : 0) + (p.delta16 ? 4 * p.H : 0));
-      fence_proxy_async();
-      if (lane == 0) mbar_expect_tx(bar, bytes);
-      __syncwarp();
-      uint8_t* qd = st + G * 2 * RB;
-      uint8_t* gd = qd + B * RB;
-      uint8_t* lsd = gd + B * RB;
-      if (!p.rows16) copy_stat_rows<LS>(lsd, p.lse, jv, B, p.H, false, lane);
-      if (!p.delta16) copy_stat_rows<LS>(lsd + B * LS, p.delta, jv, B, p.H, false, lane);
+      const int* ix = ring.ix_at(s);
+      auto qrow = [&](int gg) {
+        if (gg >= G) return p.N;
+        const int4 dd = dsc[gg];
+        return (dd.x >= 0 && (dd.z & kFirst)) ? dd.x : p.N;
+      };
+      auto erow = [&](int b) {
+        const int4 dd = dsc[b / SE];
+        return (dd.x >= 0 && b % SE < (dd.z & kCntMask)) ? ix[b] : p.N;
+      };
+      uint32_t qmask = 0;
 #pragma unroll
-      for (int r0 = 0; r0 < 2 * G + 4 * B; r0 += 32) {
-        const int r = r0 + lane;
-        const int e = (r - 2 * G) % B;
-        const int node = __shfl_sync(FULL, fnode, (r % G) & 31);
-        const int i2 = __shfl_sync(FULL, jv, (e < 0 ? 0 : e) & 31);
-        if (r < 2 * G) {
-          if (node >= 0)
-            bulk_g2s(st + (r % G) * 2 * RB + (r / G) * RB,
-                     (r < G ? Kb : Vb) + int64_t(node) * RB, RB, bar);
-        } else if (r < 2 * G + 4 * B && i2 >= 0) {
-          const int kind = (r - 2 * G) / B;
-          if (kind == 0) bulk_g2s(qd + e * RB, Qb + int64_t(i2) * RB, RB, bar);
-          else if (kind == 1) bulk_g2s(gd + e * RB, dOb + int64_t(i2) * RB, RB, bar);
-          else if (kind == 2 && p.rows16)
-            bulk_g2s(lsd + e * LS, p.lse + int64_t(i2) * p.H, 4 * p.H, bar);
-          else if (kind == 3 && p.delta16)
-            bulk_g2s(lsd + B * LS + e * LS, p.delta + int64_t(i2) * p.H, 4 * p.H, bar);
+      for (int q4 = 0; q4 < L::QR / 4; ++q4) {
+        bool any = false;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) any |= qrow(4 * q4 + j) != p.N;
+        qmask |= uint32_t(any) << q4;
+      }
+      const uint32_t eset =
+          2 * L::SET_BYTES + (p.rows16 ? 16 * p.H : 0) + (p.delta16 ? 16 * p.H : 0);
+      fence_proxy_async();
+      mbar_expect_tx(bar, __popc(qmask) * 2 * L::SET_BYTES + (B / 4) * eset);
+#pragma unroll
+      for (int q4 = 0; q4 < L::QR / 4; ++q4)
+        if ((qmask >> q4) & 1) {
+          const int r0 = qrow(4 * q4), r1 = qrow(4 * q4 + 1), r2 = qrow(4 * q4 + 2),
+                    r3 = qrow(4 * q4 + 3);
+          L::gather(st + OKI, 4 * q4, &p.mi0, r0, r1, r2, r3, bar);
+          L::gather(st + OVI, 4 * q4, &p.mi1, r0, r1, r2, r3, bar);
         }
+#pragma unroll
+      for (int b4 = 0; b4 < B / 4; ++b4) {
+        const int r0 = erow(4 * b4), r1 = erow(4 * b4 + 1), r2 = erow(4 * b4 + 2),
+                  r3 = erow(4 * b4 + 3);
+        L::gather(st + OQE, 4 * b4, &p.me0, r0, r1, r2, r3, bar);
+        L::gather(st + OGE, 4 * b4, &p.me1, r0, r1, r2, r3, bar);
+        if (p.rows16) tma_gather4(st + OLS + b4 * L::SSB, &p.ms0, 0, r0, r1, r2, r3, bar);
+        if (p.delta16) tma_gather4(st + ODL + b4 * L::SSB, &p.ms1, 0, r0, r1, r2, r3, bar);
       }
     }
+    if (!p.rows16 || !p.delta16) {  // stat rows of the edges by 4-byte copies
+      const int4 dg = lane < G ? dsc[lane] : make_int4(-1, 0, 0, 0);
+      const bool live = dsc[0].x != -3;
+      const int ge = (lane / SE) & 31;
+      const int cn = __shfl_sync(FULL, dg.x >= 0 ? (dg.z & kCntMask) : 0, ge);
+      const int jv = (live && lane < B && lane % SE < cn) ? ring.ix_at(s)[lane] : -1;
+      if (!p.rows16) copy_stat_rows<L::SSB>(ring.stage_at(s) + OLS, p.lse, jv, B, p.H, lane);
+      if (!p.delta16) copy_stat_rows<L::SSB>(ring.stage_at(s) + ODL, p.delta, jv, B, p.H, lane);
+    }
+    __syncwarp();
     cp_async_commit();
   };
 
@@ -554,9 +582,9 @@ __global__ void __launch_bounds__(CscShape<T, RB>::THREADS) bwd_csc_kernel(const
     if (act && (d.z & kFirst)) {
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
-        const uint8_t* rows = st + g * 2 * RB + (t * NC + c) * 16;
-        PR::load(lds16(rows), k[c]);
-        PR::load(lds16(rows + RB), vv[c]);
+        const int x = L::off(g, (t * NC + c) * 16);
+        PR::load(lds16(st + OKI + x), k[c]);
+        PR::load(lds16(st + OVI + x), vv[c]);
 #pragma unroll
         for (int v = 0; v < PP; ++v) {
           if (!GAT) k[c][v] = f2mul(k[c][v], f2s(p.qmul));
@@ -565,10 +593,9 @@ __global__ void __launch_bounds__(CscShape<T, RB>::THREADS) bwd_csc_kernel(const
       }
     }
 
-    const uint8_t* qs = st + G * 2 * RB + g * SE * RB;
-    const uint8_t* gs = qs + B * RB;
-    const float* lss = reinterpret_cast<const float*>(st + G * 2 * RB + 2 * B * RB) + g * SE * (LS / 4);
-    const float* dls = lss + B * (LS / 4);
+    const uint8_t* qs = st + OQE;
+    const uint8_t* gs = st + OGE;
+
     const int kmax = __reduce_max_sync(FULL, cnt);
 #pragma unroll
     for (int e = 0; e < SE; ++e) {
@@ -578,7 +605,7 @@ __global__ void __launch_bounds__(CscShape<T, RB>::THREADS) bwd_csc_kernel(const
       float2 qf[NC][PP], gf[NC][PP];
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
-        const int off = e * RB + (t * NC + c) * 16;
+        const int off = L::off(g * SE + e, (t * NC + c) * 16);
         PR::load(valid ? lds16(qs + off) : make_uint4(0, 0, 0, 0), qf[c]);
         PR::load(valid ? lds16(gs + off) : make_uint4(0, 0, 0, 0), gf[c]);
         float2 s2 = f2s(0.f), p2 = f2s(0.f);
@@ -602,8 +629,9 @@ __global__ void __launch_bounds__(CscShape<T, RB>::THREADS) bwd_csc_kernel(const
       if (act && valid) {
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
-          const float ls = lss[e * (LS / 4) + head[c]];
-          const float dl = dls[e * (LS / 4) + head[c]];
+          const int b = g * SE + e, so = (b / 4) * L::SSB + (b % 4) * 4 * p.H;
+          const float ls = reinterpret_cast<const float*>(st + OLS + so)[head[c]];
+          const float dl = reinterpret_cast<const float*>(st + ODL + so)[head[c]];
           const float pr = ex2((GAT ? sc[c] * kLog2e : sc[c]) - ls * kLog2e);
           const float ds = pr * (dp[c] - dl);
 #pragma unroll

@@ -26,10 +26,12 @@
 namespace gattn {
 
 struct FwdParams {
+  CUtensorMap mq, mk, mv;  // row-gather maps of Q, K, V (tma.cuh)
   const int4* items;   // plan items (w = heavy id of a chunk)
   const int4* sorted;  // items by decreasing length
   int64_t n_items;
   int64_t n_chunks;    // items [0, n_chunks) are heavy chunks
+  int N;               // rows of Q, K, V; row index N is the zero-filled pad row
   const int32_t* indices;
   const void* Q;
   const void* K;
@@ -49,16 +51,16 @@ struct FwdParams {
 template <typename T, int RB>
 struct FwdShape {
   using L = Lay<T, RB>;
-  // Q rows of the G items, then B K rows and B V rows
-  static constexpr int STAGE = RB * (L::G + 2 * L::B);
-  static constexpr int WARP_BYTES = kStages * STAGE + L::META;
+  // Q rows of the G items (QR slots), then B K rows and B V rows
+  static constexpr int STAGE = RB * (L::QR + 2 * L::B);
+  static constexpr int WARP_BYTES = align128(kStages * STAGE + L::META);
   static constexpr int WARPS = WarpsFor<WARP_BYTES>::value;
   static constexpr int THREADS = 32 * WARPS;
   static constexpr int SMEM = WARPS * WARP_BYTES;
 };
 
 template <typename T, int RB, int DB, int KIND>
-__global__ void __launch_bounds__(FwdShape<T, RB>::THREADS) fwd_kernel(const FwdParams p) {
+__global__ void __launch_bounds__(FwdShape<T, RB>::THREADS) fwd_kernel(const __grid_constant__ FwdParams p) {
   using L = Lay<T, RB>;
   using Sh = FwdShape<T, RB>;
   using PR = Pairs<T>;
@@ -69,14 +71,11 @@ __global__ void __launch_bounds__(FwdShape<T, RB>::THREADS) fwd_kernel(const Fwd
   constexpr int CPH = DB / 16;            // 16-byte chunks per head
   constexpr bool GAT = KIND == GATTN_SCORE_GATV2;
   constexpr unsigned FULL = 0xffffffffu;
-  extern __shared__ __align__(16) uint8_t smem[];
+  extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x & 31;
   const int g = lane / TPR, t = lane % TPR;
   Ring<L, Sh::STAGE> ring;
   ring.init(smem + (threadIdx.x >> 5) * Sh::WARP_BYTES, lane);
-  const char* __restrict__ Qb = static_cast<const char*>(p.Q);
-  const char* __restrict__ Kb = static_cast<const char*>(p.K);
-  const char* __restrict__ Vb = static_cast<const char*>(p.V);
 
   // this lane's chunks: global chunk t*NC + c of the row, its head, and
   // whether the lane writes that head's per-head values
@@ -102,38 +101,51 @@ __global__ void __launch_bounds__(FwdShape<T, RB>::THREADS) fwd_kernel(const Fwd
   BundleCursor<G, SE> cur;
   cur.start(p.sorted, p.n_items, p.indices, warp, nwarps, ring.items, lane);
 
-  // rows of stage s into its ring slot: one TMA bulk copy per row, bytes
-  // counted on the slot's barrier.  Row r of the stage: [0, G) Q rows of
-  // items that start here, [G, G+B) K rows, [G+B, G+2B) V rows.
+  // rows of stage s into its ring slot by TMA gathers issued from lane 0:
+  // Q rows of the items that start here (only the 4-row sets that hold one),
+  // then the K rows and the V rows of the stage's edges; unused slots gather
+  // the zero-filled pad row N.  Bytes are counted on the slot's barrier.
   auto issue = [&](int s) {
-    const int4* dsc = ring.desc_at(s);
-    const int4 dg = lane < G ? dsc[lane] : make_int4(-1, 0, 0, 0);
-    if (__shfl_sync(FULL, dg.x, 0) != -3) {
-      uint8_t* st = ring.stage_at(s);
-      uint64_t* bar = ring.bar_at(s);
-      const int ge = (lane / SE) & 31;
-      const int cn = __shfl_sync(FULL, dg.x >= 0 ? (dg.z & kCntMask) : 0, ge);
-      const int jv = (lane < B && lane % SE < cn) ? ring.ix_at(s)[lane] : -1;
-      const int fq = (lane < G && dg.x >= 0 && (dg.z & kFirst)) ? dg.x : -1;
-      const int rows = __popc(__ballot_sync(FULL, fq >= 0)) + 2 * __popc(__ballot_sync(FULL, jv >= 0));
-      fence_proxy_async();
-      if (lane == 0) mbar_expect_tx(bar, rows * RB);
-      __syncwarp();
+    if (lane == 0) {
+      const int4* dsc = ring.desc_at(s);
+      if (dsc[0].x != -3) {
+        uint8_t* st = ring.stage_at(s);
+        uint64_t* bar = ring.bar_at(s);
+        const int* ix = ring.ix_at(s);
+        auto qrow = [&](int gg) {
+          if (gg >= G) return p.N;
+          const int4 dd = dsc[gg];
+          return (dd.x >= 0 && (dd.z & kFirst)) ? dd.x : p.N;
+        };
+        auto erow = [&](int b) {
+          const int4 dd = dsc[b / SE];
+          return (dd.x >= 0 && b % SE < (dd.z & kCntMask)) ? ix[b] : p.N;
+        };
+        uint32_t qmask = 0;
 #pragma unroll
-      for (int r0 = 0; r0 < G + 2 * B; r0 += 32) {
-        const int r = r0 + lane;
-        const int b = r < G + B ? r - G : r - G - B;
-        const int node = __shfl_sync(FULL, fq, r & 31);
-        const int j = __shfl_sync(FULL, jv, b & 31);
-        if (r < G) {
-          if (node >= 0) bulk_g2s(st + r * RB, Qb + int64_t(node) * RB, RB, bar);
-        } else if (r < G + B) {
-          if (j >= 0) bulk_g2s(st + G * RB + b * RB, Kb + int64_t(j) * RB, RB, bar);
-        } else if (r < G + 2 * B) {
-          if (j >= 0) bulk_g2s(st + (G + B) * RB + b * RB, Vb + int64_t(j) * RB, RB, bar);
+        for (int q4 = 0; q4 < L::QR / 4; ++q4) {
+          bool any = false;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) any |= qrow(4 * q4 + j) != p.N;
+          qmask |= uint32_t(any) << q4;
+        }
+        fence_proxy_async();
+        mbar_expect_tx(bar, (__popc(qmask) + 2 * (B / 4)) * L::SET_BYTES);
+#pragma unroll
+        for (int q4 = 0; q4 < L::QR / 4; ++q4)
+          if ((qmask >> q4) & 1)
+            L::gather(st, 4 * q4, &p.mq, qrow(4 * q4), qrow(4 * q4 + 1), qrow(4 * q4 + 2),
+                      qrow(4 * q4 + 3), bar);
+#pragma unroll
+        for (int b4 = 0; b4 < B / 4; ++b4) {
+          const int r0 = erow(4 * b4), r1 = erow(4 * b4 + 1), r2 = erow(4 * b4 + 2),
+                    r3 = erow(4 * b4 + 3);
+          L::gather(st + L::QR * RB, 4 * b4, &p.mk, r0, r1, r2, r3, bar);
+          L::gather(st + (L::QR + B) * RB, 4 * b4, &p.mv, r0, r1, r2, r3, bar);
         }
       }
     }
+    __syncwarp();
     cp_async_commit();  // this iteration's index copies
   };
 
@@ -166,7 +178,7 @@ __global__ void __launch_bounds__(FwdShape<T, RB>::THREADS) fwd_kernel(const Fwd
     if (act && (d.z & kFirst)) {
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
-        PR::load(lds16(st + g * RB + (t * NC + c) * 16), q[c]);
+        PR::load(lds16(st + L::off(g, (t * NC + c) * 16)), q[c]);
         if (!GAT) {
 #pragma unroll
           for (int v = 0; v < PP; ++v) q[c][v] = f2mul(q[c][v], f2s(p.qmul));
@@ -178,7 +190,7 @@ __global__ void __launch_bounds__(FwdShape<T, RB>::THREADS) fwd_kernel(const Fwd
       }
     }
 
-    const uint8_t* ks = st + G * RB + g * SE * RB;
+    const uint8_t* ks = st + L::QR * RB;
     const uint8_t* vs = ks + B * RB;
     const int kmax = __reduce_max_sync(FULL, cnt);  // edges of the warp's longest item here
     float sc[SE][NC];
@@ -187,7 +199,7 @@ __global__ void __launch_bounds__(FwdShape<T, RB>::THREADS) fwd_kernel(const Fwd
       if (k >= kmax) break;
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
-        const uint4 kr = k < cnt ? lds16(ks + k * RB + (t * NC + c) * 16) : make_uint4(0, 0, 0, 0);
+        const uint4 kr = k < cnt ? lds16(ks + L::off(g * SE + k, (t * NC + c) * 16)) : make_uint4(0, 0, 0, 0);
         float2 kf[PP];
         PR::load(kr, kf);
         float2 a2 = f2s(0.f);
@@ -230,7 +242,7 @@ __global__ void __launch_bounds__(FwdShape<T, RB>::THREADS) fwd_kernel(const Fwd
             const float pk = ex2(sc[k][c] - base);
             l[c] += pk;
             float2 vf[PP];
-            PR::load(lds16(vs + k * RB + (t * NC + c) * 16), vf);
+            PR::load(lds16(vs + L::off(g * SE + k, (t * NC + c) * 16)), vf);
 #pragma unroll
             for (int v = 0; v < PP; ++v) acc[c][v] = f2fma(f2s(pk), vf[v], acc[c][v]);
           }

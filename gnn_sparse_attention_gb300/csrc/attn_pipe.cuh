@@ -32,6 +32,7 @@
 #pragma once
 
 #include "gattn_internal.cuh"
+#include "tma.cuh"
 
 namespace gattn {
 
@@ -55,16 +56,41 @@ struct Lay {
   // edges per item per stage: ~4 KB of gathered rows per stage
   static constexpr int SE0 = 4096 / (2 * RB) / G;
   static constexpr int SE1 = SE0 < 1 ? 1 : SE0;
-  static constexpr int SE = SE1 * G > 32 ? 32 / G : SE1;  // at most 32 edges per stage
+  static constexpr int SE2 = SE1 * G > 32 ? 32 / G : SE1;  // at most 32 edges per stage
+  static constexpr int SE = SE2 * G < 4 ? 4 / G : SE2;     // whole 4-row gathers
   static constexpr int B = G * SE;                  // edges per stage
+  static constexpr int QR = (G + 3) / 4 * 4;        // item-row slots per stage
+  // one gather moves 4 rows of BOXE elements; a row is NCOL such pieces
+  static constexpr int HD = RB / (int)sizeof(T);
+  static constexpr int BOXE = HD < kGatherBoxMax ? HD : kGatherBoxMax;
+  static constexpr int NCOL = HD / BOXE;
+  static constexpr int BOXB = BOXE * (int)sizeof(T);
   static constexpr int IDXB = (B * 4 + 15) / 16 * 16;
   // the warp's descriptor ring, index ring, unit buffer and row barriers
   static constexpr int META = kRing * G * 16 + kRing * IDXB + kUnit * 16 + 16 * ((kStages + 1) / 2);
   static_assert(TPR >= 1 && TPR <= 32 && 32 % TPR == 0, "thread layout");
-  static_assert(B <= 32, "stage edges");
-  // shared-memory position (in 16-byte units) of global chunk ch of a row
-  __device__ __forceinline__ static int pos(int ch) { return (ch % NC) * TPR + ch / NC; }
+  static_assert(B <= 32 && B % 4 == 0, "stage edges");
+  // Byte offset of row byte x of row b in a region filled by 4-row gathers:
+  // [b / 4][piece][b % 4][BOXB].
+  __device__ __forceinline__ static int off(int b, int x) {
+    if constexpr (NCOL == 1) return b * RB + x;
+    else return (b / 4) * 4 * RB + (x / BOXB) * 4 * BOXB + (b % 4) * BOXB + x % BOXB;
+  }
+  // Issue the gathers of rows r0..r3 into a region at row slot b0 (multiple of 4).
+  __device__ __forceinline__ static void gather(uint8_t* region, int b0, const CUtensorMap* map,
+                                                int r0, int r1, int r2, int r3, uint64_t* bar) {
+#pragma unroll
+    for (int pc = 0; pc < NCOL; ++pc)
+      tma_gather4(region + b0 * RB + pc * 4 * BOXB, map, pc * BOXE, r0, r1, r2, r3, bar);
+  }
+  static constexpr int SET_BYTES = 4 * RB;  // bytes one 4-row gather set lands
+  // per-node fp32 statistic rows (H <= RB/16 floats) are gathered 4 at a
+  // time into SSB-byte sets (128-byte aligned), 4H bytes per row
+  static constexpr int SSB = RB < 128 ? 128 : RB;
 };
+
+// Offsets are kept 128-byte aligned: tensor copies land on such addresses.
+constexpr int align128(int x) { return (x + 127) / 128 * 128; }
 
 // Warps per block: the count (1..8) that fits the most warps in an SM's
 // shared memory (1 KB per block is reserved by the system); ties go to the
@@ -101,8 +127,11 @@ __device__ __forceinline__ uint4 lds16(const void* p) {
   return *reinterpret_cast<const uint4*>(p);
 }
 
-// mbarrier + TMA bulk copies (global -> this CTA's shared memory)
-constexpr uint32_t kWaitLimit = 1u << 22;  // polls before a wait is declared failed
+// mbarrier + TMA bulk copies (global -> this CTA's shared memory).  A wait
+// suspends the warp in hardware for up to kSuspendNs per poll, so a waiting
+// warp issues almost nothing; kWaitLimit polls bound a wait to about 0.2 s.
+constexpr uint32_t kSuspendNs = 100000;
+constexpr uint32_t kWaitLimit = 2000;
 __device__ __forceinline__ void mbar_init(uint64_t* bar, int count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count)
                : "memory");
@@ -121,10 +150,10 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
       : "memory");
   return ok != 0;
 }
