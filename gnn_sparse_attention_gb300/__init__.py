@@ -7,7 +7,7 @@ not touch the GPU.  The public Python names mirror the C entry points.
 from __future__ import annotations
 
 __all__ = ["Score", "Plan", "GattnError", "gattn_plan_create", "gattn_plan_get_info",
-           "gattn_plan_export", "gattn_workspace_size", "gattn_fwd", "gattn_bwd", "gattn_bwd_dq", "gattn_bwd_dkdv", "gattn_plan_check_errors",
+           "gattn_plan_export", "gattn_workspace_size", "gattn_fwd", "gattn_bwd", "gattn_bwd_dq", "gattn_bwd_dkdv", "gattn_plan_check_errors", "gattn_fwd_noalloc",
            "gattn_version", "load_library"]
 
 

@@ -24,8 +24,8 @@ GATTN_F32, GATTN_BF16 = 0, 1
 GATTN_SCORE_DOT, GATTN_SCORE_GATV2 = 0, 1
 EXPORTED = ("gattn_plan_create", "gattn_plan_destroy", "gattn_plan_get_info",
             "gattn_plan_export", "gattn_workspace_size", "gattn_fwd", "gattn_bwd",
-            "gattn_bwd_dq", "gattn_bwd_dkdv", "gattn_plan_check_errors", "gattn_last_error",
-            "gattn_version")
+            "gattn_bwd_dq", "gattn_bwd_dkdv", "gattn_plan_check_errors", "gattn_fwd_noalloc",
+            "gattn_last_error", "gattn_version")
 
 
 class GattnError(RuntimeError):
@@ -90,7 +90,9 @@ def load_library(path: str | None = None):
         lib.gattn_bwd_dkdv.argtypes = [P, i32, i32, ctypes.c_int, P, P, P,
                                        ctypes.POINTER(_Score), P, P, P, P, P, sz, P]
         lib.gattn_plan_check_errors.argtypes = [P]
-        for name in EXPORTED[:10]:
+        lib.gattn_fwd_noalloc.argtypes = [P, i32, i32, ctypes.c_int, P, P, P,
+                                          ctypes.POINTER(_Score), P, P, P]
+        for name in EXPORTED[:11]:
             getattr(lib, name).restype = st
         lib.gattn_last_error.restype = ctypes.c_char_p
         lib.gattn_last_error.argtypes = []
@@ -315,3 +317,15 @@ def gattn_bwd_dkdv(plan: Plan, Q, K, V, dout, lse, score: Score, dK=None, dV=Non
 def gattn_plan_check_errors(plan: Plan) -> None:
     """Raise GattnError(GATTN_ERR_TIMEOUT) if a kernel gave up a bounded wait."""
     _check(load_library().gattn_plan_check_errors(plan.handle), "gattn_plan_check_errors")
+
+
+def gattn_fwd_noalloc(plan: Plan, Q, K, V, score: Score, out, lse, stream=None):
+    """Forward pass that allocates nothing: ``out`` and ``lse`` must be given,
+    and the heavy-chunk scratch comes from the library's fixed 32 MiB array
+    (for callers that cannot allocate device memory at call time)."""
+    H, D = _shape(Q)
+    sc = score._struct()
+    _check(load_library().gattn_fwd_noalloc(plan.handle, H, D, _dtype_code(Q.dtype), _ptr(Q),
+                                            _ptr(K), _ptr(V), ctypes.byref(sc), _ptr(out),
+                                            _ptr(lse), _stream(stream)), "gattn_fwd_noalloc")
+    return out, lse

@@ -9,10 +9,6 @@
 #include "attn_launch.cuh"
 #include "tma.cuh"
 
-struct gattn_plan {
-  gattn::Plan p;
-};
-
 namespace gattn {
 
 namespace {

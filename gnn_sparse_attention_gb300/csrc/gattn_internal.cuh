@@ -191,3 +191,8 @@ void set_error(const char* fmt, ...);
 int grid_for(const Plan& p, int64_t n_items, int blocks_per_sm);
 
 }  // namespace gattn
+
+// The opaque handle of include/gattn.h.
+struct gattn_plan {
+  gattn::Plan p;
+};

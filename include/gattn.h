@@ -220,6 +220,26 @@ GATTN_API gattn_status gattn_bwd_dkdv(const gattn_plan* plan, int32_t H, int32_t
                                       const float* lse, void* dK, void* dV, void* workspace,
                                       size_t workspace_bytes, gattn_stream_t stream);
 
+/*
+ * gattn_fwd without a workspace argument, for callers that cannot allocate
+ * device memory where they run the layer (inside CUDA graph capture, under
+ * a memory pool they do not own, in plugin hosts that only pass tensors).
+ * The paper has no counterpart to this call.  Same arguments and results as
+ * gattn_fwd; the heavy-chunk scratch comes from one fixed 32 MiB array
+ * compiled into the library, so the call allocates nothing.
+ *   - A plan and head layout whose scratch would exceed 32 MiB are rejected
+ *     with GATTN_ERR_INVALID_ARG (use gattn_fwd with a workspace instead).
+ *   - The first call on a device looks up the array's device address (a
+ *     cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - All calls share the array: calls whose kernels may overlap on the GPU
+ *     (different streams or host threads) race and must be ordered.
+ *   - The array lives on every device that loads the library until exit.
+ */
+GATTN_API gattn_status gattn_fwd_noalloc(const gattn_plan* plan, int32_t H, int32_t D,
+                                         gattn_dtype dtype, const void* Q, const void* K,
+                                         const void* V, const gattn_score* score, void* out,
+                                         float* lse, gattn_stream_t stream);
+
 /* Message of the last failing call on this thread ("" if none).  Never NULL. */
 GATTN_API const char* gattn_last_error(void);
 
