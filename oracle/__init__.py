@@ -66,6 +66,8 @@ def _load():
             lib.oracle_plan.argtypes = [i32, i64, P, P, i32, i32, P, P, P, P, i64, P, P, P, P, P,
                                         P, P, i64, P]
             lib.oracle_plan.restype = ctypes.c_int
+            lib.oracle_tile_plan.argtypes = [i32, i64, P, P, i64, i64, P, P, P, P, P, P]
+            lib.oracle_tile_plan.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -172,6 +174,38 @@ def plan(indptr, indices, heavy_threshold, chunk):
         "outdeg": outdeg, "hist_out": hist_out, "light_src": light_src[:nls],
         "src_chunks": src_chunks[:ncs],
     }
+
+
+TILE = 128  # nodes per tile side
+
+
+def tile_min_count(density: float) -> int:
+    """Edges a 128 x 128 block needs to be a dense tile: ceil(density * 128^2), at least 1."""
+    import math
+    return max(1, int(math.ceil(float(np.float32(density)) * TILE * TILE)))
+
+
+def tile_plan(indptr, indices, min_count):
+    """Oracle dense-tile split: tiles (rb, cb), their bit masks and the residual CSR."""
+    lib = _load()
+    indptr = np.ascontiguousarray(indptr, dtype=np.int32)
+    indices = np.ascontiguousarray(indices, dtype=np.int32)
+    N = len(indptr) - 1
+    M = int(indptr[-1])
+    cap = M // max(int(min_count), 1) + 1
+    tile_rb = np.zeros(cap, np.int32)
+    tile_cb = np.zeros(cap, np.int32)
+    masks = np.zeros((cap, 128, 4), np.uint32)
+    indptr_r = np.zeros(N + 1, np.int32)
+    indices_r = np.zeros(max(M, 1), np.int32)
+    counts = np.zeros(2, np.int64)
+    rc = lib.oracle_tile_plan(N, M, _p(indptr), _p(indices), int(min_count), cap, _p(tile_rb),
+                              _p(tile_cb), _p(masks), _p(indptr_r), _p(indices_r), _p(counts))
+    if rc != 0:
+        raise RuntimeError(f"oracle_tile_plan failed ({rc})")
+    nt, mr = int(counts[0]), int(counts[1])
+    return {"tile_rb": tile_rb[:nt], "tile_cb": tile_cb[:nt], "masks": masks[:nt],
+            "indptr_r": indptr_r, "indices_r": indices_r[:mr]}
 
 
 def rows_subgraph(indptr, indices, rows):

@@ -299,3 +299,96 @@ int oracle_plan(int32_t N, int64_t M, const int32_t* indptr, const int32_t* indi
   counts[3] = ncs;
   return 0;
 }
+
+/*
+ * Dense-tile split of the CSR for the tensor-core path ("On Efficient Scaling
+ * of GNNs via IO-Aware Layers Implementations", zh/ko technical summaries,
+ * "Methodology", attention-based layers, tensor-core optimisation: locally
+ * dense neighbourhoods are packed into block tiles so that their scores and
+ * aggregation run as small dense matrix products; the remaining edges stay
+ * on the CSR path).
+ *
+ * Reading used here: nodes are cut into blocks of 128 consecutive ids; the
+ * block (rb, cb) holds the edges j -> i with i / 128 == rb and j / 128 == cb.
+ * A block with at least min_count edges is a dense tile.  In a tile every
+ * (i, j) pair that occurs exactly once becomes bit (j % 128) of row (i % 128)
+ * of the tile's 128 x 128 mask (4 words of 32 bits per row, bit b of word w
+ * is column 32 w + b); pairs that occur more than once, and every edge of a
+ * block that is not a tile, form the residual CSR, kept in CSR order.  Tiles
+ * are listed in (rb, cb) order.
+ *
+ * Outputs: tile_rb/tile_cb[n_tiles], masks[n_tiles * 512], indptr_r[N + 1],
+ * indices_r[M_res].  counts[0] = n_tiles, counts[1] = M_res.  Returns 0, -1
+ * if more than cap_tiles tiles, -2 on allocation failure.
+ */
+typedef struct { uint64_t key; int64_t e; } orc_edge_key;
+
+static int orc_cmp_key(const void* a, const void* b) {
+  const orc_edge_key* x = (const orc_edge_key*)a;
+  const orc_edge_key* y = (const orc_edge_key*)b;
+  if (x->key != y->key) return x->key < y->key ? -1 : 1;
+  return x->e < y->e ? -1 : (x->e > y->e ? 1 : 0);
+}
+
+int oracle_tile_plan(int32_t N, int64_t M, const int32_t* indptr, const int32_t* indices,
+                     int64_t min_count, int64_t cap_tiles, int32_t* tile_rb, int32_t* tile_cb,
+                     uint32_t* masks, int32_t* indptr_r, int32_t* indices_r, int64_t* counts) {
+  const uint64_t nb = ((uint64_t)N + 127) / 128;
+  orc_edge_key* ek = (orc_edge_key*)malloc((size_t)(M > 0 ? M : 1) * sizeof(orc_edge_key));
+  int32_t* row = (int32_t*)malloc((size_t)(M > 0 ? M : 1) * sizeof(int32_t));
+  unsigned char* in_tile = (unsigned char*)calloc((size_t)(M > 0 ? M : 1), 1);
+  int32_t* pair_count = (int32_t*)malloc(128 * 128 * sizeof(int32_t));
+  if (!ek || !row || !in_tile || !pair_count) {
+    free(ek); free(row); free(in_tile); free(pair_count);
+    return -2;
+  }
+  for (int32_t i = 0; i < N; ++i)
+    for (int64_t e = indptr[i]; e < indptr[i + 1]; ++e) row[e] = i;
+  for (int64_t e = 0; e < M; ++e) {
+    ek[e].key = (uint64_t)(row[e] / 128) * nb + (uint64_t)(indices[e] / 128);
+    ek[e].e = e;
+  }
+  qsort(ek, (size_t)M, sizeof(orc_edge_key), orc_cmp_key);
+
+  int64_t n_tiles = 0;
+  for (int64_t s = 0; s < M;) {
+    int64_t t = s;
+    while (t < M && ek[t].key == ek[s].key) ++t;  /* run [s, t): one block */
+    if (t - s >= min_count) {
+      if (n_tiles >= cap_tiles) {
+        free(ek); free(row); free(in_tile); free(pair_count);
+        return -1;
+      }
+      tile_rb[n_tiles] = (int32_t)(ek[s].key / nb);
+      tile_cb[n_tiles] = (int32_t)(ek[s].key % nb);
+      uint32_t* mk = masks + n_tiles * 512;
+      memset(mk, 0, 512 * sizeof(uint32_t));
+      memset(pair_count, 0, 128 * 128 * sizeof(int32_t));
+      for (int64_t u = s; u < t; ++u) {
+        const int64_t e = ek[u].e;
+        pair_count[(row[e] % 128) * 128 + indices[e] % 128] += 1;
+      }
+      for (int64_t u = s; u < t; ++u) {
+        const int64_t e = ek[u].e;
+        const int r = row[e] % 128, c = indices[e] % 128;
+        if (pair_count[r * 128 + c] == 1) {
+          mk[r * 4 + c / 32] |= 1u << (c % 32);
+          in_tile[e] = 1;
+        }
+      }
+      ++n_tiles;
+    }
+    s = t;
+  }
+  int64_t mr = 0;
+  indptr_r[0] = 0;
+  for (int32_t i = 0; i < N; ++i) {
+    for (int64_t e = indptr[i]; e < indptr[i + 1]; ++e)
+      if (!in_tile[e]) indices_r[mr++] = indices[e];
+    indptr_r[i + 1] = (int32_t)mr;
+  }
+  counts[0] = n_tiles;
+  counts[1] = mr;
+  free(ek); free(row); free(in_tile); free(pair_count);
+  return 0;
+}

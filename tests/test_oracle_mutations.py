@@ -8,6 +8,7 @@ import pytest
 
 import oracle
 from tests import test_oracle_pins as pins
+from tests import test_oracle_tile_pins as tile_pins
 
 MUTANTS = {
     "drop_dot_scale": ("return scale * s;", "return s;"),
@@ -24,6 +25,11 @@ MUTANTS = {
                          "for (int32_t i = N - 1; i >= 0; --i)\n    for (int64_t e = ptr[i];"),
     "chunk_off_by_one": ("if (d <= T) { light[nl++] = i; continue; }",
                          "if (d < T) { light[nl++] = i; continue; }"),
+    "tile_threshold_strict": ("if (t - s >= min_count) {", "if (t - s > min_count) {"),
+    "tile_keeps_duplicates": ("if (pair_count[r * 128 + c] == 1) {",
+                              "if (pair_count[r * 128 + c] >= 1) {"),
+    "tile_mask_column_order": ("mk[r * 4 + c / 32] |= 1u << (c % 32);",
+                               "mk[r * 4 + c % 4] |= 1u << (c / 4);"),
 }
 
 
@@ -40,6 +46,10 @@ def _battery():
         ("fd_gatv2", lambda: pins.test_finite_differences(oracle.GATV2)),
         ("plan", lambda: pins.test_plan_recount(10, 200, 6.0, 8, 4)),
         ("plan_T", lambda: pins.test_plan_recount(11, 500, 20.0, 32, 16)),
+        ("tile_split", lambda: tile_pins.test_tile_split_recount(0, 300, [(0, 0), (1, 2)], 0.3,
+                                                                 400, 30, 1000)),
+        ("tile_threshold", tile_pins.test_tile_threshold_is_inclusive),
+        ("tile_dups", tile_pins.test_tile_duplicates_stay_residual),
     ]
     for name, fn in checks:
         try:
