@@ -25,7 +25,7 @@ GATTN_SCORE_DOT, GATTN_SCORE_GATV2 = 0, 1
 EXPORTED = ("gattn_plan_create", "gattn_plan_destroy", "gattn_plan_get_info",
             "gattn_plan_export", "gattn_workspace_size", "gattn_fwd", "gattn_bwd",
             "gattn_bwd_dq", "gattn_bwd_dkdv", "gattn_plan_check_errors", "gattn_fwd_noalloc",
-            "gattn_last_error", "gattn_version")
+            "gattn_plan_export_tiles", "gattn_last_error", "gattn_version")
 
 
 class GattnError(RuntimeError):
@@ -51,7 +51,9 @@ class _PlanInfo(ctypes.Structure):
                 ("n_chunks", ctypes.c_int64), ("n_light_src", ctypes.c_int64),
                 ("n_heavy_src", ctypes.c_int64), ("n_src_chunks", ctypes.c_int64),
                 ("max_deg", ctypes.c_int32), ("max_outdeg", ctypes.c_int32),
-                ("device_bytes", ctypes.c_size_t)]
+                ("device_bytes", ctypes.c_size_t), ("n_tiles", ctypes.c_int64),
+                ("n_tile_rows", ctypes.c_int64), ("tile_edges", ctypes.c_int64),
+                ("tile_min_edges", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -92,7 +94,8 @@ def load_library(path: str | None = None):
         lib.gattn_plan_check_errors.argtypes = [P]
         lib.gattn_fwd_noalloc.argtypes = [P, i32, i32, ctypes.c_int, P, P, P,
                                           ctypes.POINTER(_Score), P, P, P]
-        for name in EXPORTED[:11]:
+        lib.gattn_plan_export_tiles.argtypes = [P] * 6
+        for name in EXPORTED[:12]:
             getattr(lib, name).restype = st
         lib.gattn_last_error.restype = ctypes.c_char_p
         lib.gattn_last_error.argtypes = []
@@ -193,12 +196,14 @@ def gattn_version() -> str:
 
 
 def gattn_plan_create(indptr: torch.Tensor, indices: torch.Tensor, heavy_threshold: int = 0,
-                      chunk: int = 0, stream=None) -> Plan:
+                      chunk: int = 0, stream=None, tile_enable: bool = False,
+                      tile_density: float = 0.0) -> Plan:
     lib = load_library()
     for t, name in ((indptr, "indptr"), (indices, "indices")):
         if not t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
-    opts = _PlanOpts(int(heavy_threshold), int(chunk), 0, 0.0)
+    opts = _PlanOpts(int(heavy_threshold), int(chunk), int(bool(tile_enable)),
+                     float(tile_density))
     h = ctypes.c_void_p()
     N = indptr.numel() - 1
     _check(lib.gattn_plan_create(_ptr(indptr), _ptr(indices) if indices.numel() else None,
@@ -230,6 +235,21 @@ def gattn_plan_export(plan: Plan) -> dict:
              "hist_out", "light_src", "src_chunks")
     ptrs = [arr[k].ctypes.data_as(ctypes.c_void_p) if arr[k].size else None for k in order]
     _check(load_library().gattn_plan_export(plan.handle, *ptrs), "gattn_plan_export")
+    return arr
+
+
+def gattn_plan_export_tiles(plan: Plan) -> dict:
+    """Dense-tile split of a plan built with tile_enable: tiles, masks, residual CSR."""
+    info = gattn_plan_get_info(plan)
+    nt, N = info["n_tiles"], info["N"]
+    arr = {
+        "tile_rb": np.zeros(nt, np.int32), "tile_cb": np.zeros(nt, np.int32),
+        "masks": np.zeros((nt, 128, 4), np.uint32), "indptr_r": np.zeros(N + 1, np.int32),
+        "indices_r": np.zeros(info["M"] - info["tile_edges"], np.int32),
+    }
+    order = ("tile_rb", "tile_cb", "masks", "indptr_r", "indices_r")
+    ptrs = [arr[k].ctypes.data_as(ctypes.c_void_p) if arr[k].size else None for k in order]
+    _check(load_library().gattn_plan_export_tiles(plan.handle, *ptrs), "gattn_plan_export_tiles")
     return arr
 
 

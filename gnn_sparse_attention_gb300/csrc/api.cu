@@ -7,6 +7,7 @@
 #include <new>
 
 #include "attn_launch.cuh"
+#include "attn_tile.cuh"
 #include "tma.cuh"
 
 namespace gattn {
@@ -64,8 +65,9 @@ Workspace ws_layout(const Plan& p, int H, int D) {
   size_t off = 0;
   w.fwd_part = off;
   const size_t slots = size_t(p.n_chunks + p.n_inner);
+  const size_t slots_res = size_t(p.n_chunks_r + p.n_inner_r);  // residual forward (tiles)
   const size_t slots_src = size_t(p.n_src_chunks + p.n_inner_src);
-  off = align_up(off + slots * w.pstride * 4, 256);
+  off = align_up(off + (slots > slots_res ? slots : slots_res) * w.pstride * 4, 256);
   w.dq_part = off;
   off = align_up(off + slots * HD * 4, 256);
   w.delta = off;
@@ -202,8 +204,16 @@ gattn_status gattn_plan_create(const int32_t* indptr, const int32_t* indices, in
     GATTN_REQUIRE(T <= kMaxItemEdges && C <= kMaxItemEdges, GATTN_ERR_INVALID_ARG,
                   "heavy_threshold and chunk must be at most %d (got %d, %d)", kMaxItemEdges, T,
                   C);
-    GATTN_REQUIRE(opts->tile_enable == 0, GATTN_ERR_UNSUPPORTED,
-                  "the dense-tile path is not available in this build");
+  }
+  int32_t tile_min = 0;
+  if (opts && opts->tile_enable) {
+    GATTN_REQUIRE(N <= (1 << 23), GATTN_ERR_UNSUPPORTED,
+                  "the dense-tile split needs N <= 2^23 (got %d)", N);
+    const float dens = opts->tile_density > 0.f ? opts->tile_density : 0.0625f;
+    GATTN_REQUIRE(dens <= 1.f, GATTN_ERR_INVALID_ARG, "tile_density must be at most 1 (got %g)",
+                  (double)dens);
+    const double need = std::ceil(double(dens) * kTileRows * kTileRows);
+    tile_min = need < 1.0 ? 1 : int32_t(need);
   }
   gattn_plan* h = new (std::nothrow) gattn_plan();
   GATTN_REQUIRE(h != nullptr, GATTN_ERR_OOM, "host allocation failed");
@@ -214,6 +224,7 @@ gattn_status gattn_plan_create(const int32_t* indptr, const int32_t* indices, in
   p.C = C;
   p.device = dev;
   p.num_sms = sms;
+  p.tile_min = tile_min;
   const gattn_status s = plan_build(&p, indptr, indices, reinterpret_cast<cudaStream_t>(stream));
   if (s != GATTN_OK) {
     for (void* q : p.allocs) cudaFree(q);
@@ -255,6 +266,10 @@ gattn_status gattn_plan_get_info(const gattn_plan* plan, gattn_plan_info* info) 
   info->max_deg = p.max_deg;
   info->max_outdeg = p.max_outdeg;
   info->device_bytes = p.device_bytes;
+  info->n_tiles = p.n_tiles;
+  info->n_tile_rows = p.n_trows;
+  info->tile_edges = p.tile_min > 0 ? p.M - p.M_res : 0;
+  info->tile_min_edges = p.tile_min;
   return GATTN_OK;
 }
 
@@ -308,6 +323,22 @@ gattn_status gattn_plan_export(const gattn_plan* plan, int32_t* deg, int32_t* hi
   return GATTN_OK;
 }
 
+gattn_status gattn_plan_export_tiles(const gattn_plan* plan, int32_t* tile_rb, int32_t* tile_cb,
+                                     uint32_t* masks, int32_t* indptr_r, int32_t* indices_r) {
+  GATTN_REQUIRE(plan, GATTN_ERR_INVALID_ARG, "plan is NULL");
+  const Plan& p = plan->p;
+  GATTN_REQUIRE(p.tile_min > 0, GATTN_ERR_INVALID_ARG, "the plan was built without tile_enable");
+  gattn_status s;
+  if ((s = copy_out(tile_rb, p.tile_rb, p.n_tiles)) != GATTN_OK) return s;
+  if ((s = copy_out(tile_cb, p.tile_cb, p.n_tiles)) != GATTN_OK) return s;
+  if ((s = copy_out(reinterpret_cast<int32_t*>(masks), p.tile_mask,
+                    size_t(p.n_tiles) * kTileRows * 4)) != GATTN_OK)
+    return s;
+  if ((s = copy_out(indptr_r, p.indptr_r, size_t(p.N) + 1)) != GATTN_OK) return s;
+  if ((s = copy_out(indices_r, p.indices_r, p.M_res)) != GATTN_OK) return s;
+  return GATTN_OK;
+}
+
 gattn_status gattn_plan_check_errors(const gattn_plan* plan) {
   GATTN_REQUIRE(plan, GATTN_ERR_INVALID_ARG, "plan is NULL");
   cudaError_t e = cudaDeviceSynchronize();
@@ -357,10 +388,13 @@ gattn_status gattn_fwd(const gattn_plan* plan, int32_t H, int32_t D, gattn_dtype
                 GATTN_ERR_INVALID_ARG, "workspace needs %zu bytes (16-byte aligned), got %zu",
                 w.total, workspace_bytes);
   char* ws = static_cast<char*>(workspace);
-  f.items = p.items;
-  f.sorted = p.sorted;
-  f.n_items = p.n_chunks + p.n_light;
-  f.n_chunks = p.n_chunks;
+  // dense tiles on the tensor cores: the CSR pass covers the residual edges
+  const bool tiles = p.tile_min > 0 && p.n_tiles > 0 && dtype == GATTN_BF16 &&
+                     score->kind == GATTN_SCORE_DOT && (D == 64 || D == 128);
+  f.items = tiles ? p.items_r : p.items;
+  f.sorted = tiles ? p.sorted_r : p.sorted;
+  f.n_items = tiles ? p.n_chunks_r + p.n_light_r : p.n_chunks + p.n_light;
+  f.n_chunks = tiles ? p.n_chunks_r : p.n_chunks;
   f.N = p.N;
   {
     const int es = (int)dtype_size(dtype);
@@ -370,7 +404,7 @@ gattn_status gattn_fwd(const gattn_plan* plan, int32_t H, int32_t D, gattn_dtype
         !encode_rows_map(&f.mv, V, es, bf, p.N, HD))
       return GATTN_ERR_CUDA;
   }
-  f.indices = p.indices;
+  f.indices = tiles ? p.indices_r : p.indices;
   f.Q = Q;
   f.K = K;
   f.V = V;
@@ -381,13 +415,31 @@ gattn_status gattn_fwd(const gattn_plan* plan, int32_t H, int32_t D, gattn_dtype
   f.D = D;
   f.part = reinterpret_cast<float*>(ws + w.fwd_part);
   f.pstride = w.pstride;
-  f.tree = Tree{p.parent, p.kids, p.n_chunks, p.cnt_fwd};
+  f.tree = tiles ? Tree{p.parent_r, p.kids_r, p.n_chunks_r, p.cnt_fwd_r}
+                 : Tree{p.parent, p.kids, p.n_chunks, p.cnt_fwd};
   f.err = p.err;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if ((s = launch_fwd(dtype, rb, D * (int)dtype_size(dtype), score->kind, f, p.num_sms, st,
                       nullptr)) != GATTN_OK)
     return s;
-  return launched("forward");
+  if ((s = launched("forward")) != GATTN_OK || !tiles) return s;
+  TileParams tp{};
+  const int64_t HD = int64_t(H) * D;
+  if (!encode_tile_map(&tp.mq, Q, p.N, HD) || !encode_tile_map(&tp.mk, K, p.N, HD) ||
+      !encode_tile_map(&tp.mv, V, p.N, HD))
+    return GATTN_ERR_CUDA;
+  tp.mask = p.tile_mask;
+  tp.tile_cb = p.tile_cb;
+  tp.trow_rb = p.trow_rb;
+  tp.trow_ptr = p.trow_ptr;
+  tp.n_trows = p.n_trows;
+  tp.N = p.N;
+  tp.H = H;
+  tp.qmul = f.qmul;
+  tp.out = out;
+  tp.lse = lse;
+  tp.err = p.err;
+  return launch_tile_fwd(tp, D, st);
 }
 
 static gattn_status bwd_common(const gattn_plan* plan, int32_t H, int32_t D, gattn_dtype dtype,

@@ -126,10 +126,12 @@ __global__ void __launch_bounds__(CsrShape<T, RB>::THREADS) bwd_csr_kernel(const
   using Sh = CsrShape<T, RB>;
   using PR = Pairs<T>;
   constexpr int NC = L::NC, TPR = L::TPR, G = L::G, SE = L::SE, B = L::B;
-  constexpr int NCH = L::NCH, PP = PR::P, S = kStages, LS = Sh::LS;
+  constexpr int PP = PR::P, S = kStages;
   constexpr int HD = RB / (int)sizeof(T);
   constexpr int D = DB / (int)sizeof(T);  // head width
   constexpr int CPH = DB / 16;            // 16-byte chunks per head
+  using LH = LaneHeads<NC, CPH>;
+  constexpr int HL = LH::N;               // heads of this lane
   constexpr bool GAT = KIND == GATTN_SCORE_GATV2;
   constexpr unsigned FULL = 0xffffffffu;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -160,7 +162,7 @@ __global__ void __launch_bounds__(CsrShape<T, RB>::THREADS) bwd_csr_kernel(const
   const int64_t warp = (int64_t(blockIdx.x) * Sh::THREADS + threadIdx.x) >> 5;
   const int64_t nwarps = (int64_t(gridDim.x) * Sh::THREADS) >> 5;
   BundleCursor<G, SE> cur;
-  cur.start(p.sorted, p.n_items, p.idx, warp, nwarps, ring.items, lane);
+  cur.start(p.sorted, p.n_items, p.idx, p.N, warp, nwarps, ring.items, lane);
 
   // stage: [QR][Q row] [QR][dO row] [QR][O row] [QR][lse row] [B][K row]
   // [B][V row].  TMA gathers from lane 0 (item rows only for 4-row sets that
@@ -173,22 +175,13 @@ __global__ void __launch_bounds__(CsrShape<T, RB>::THREADS) bwd_csr_kernel(const
     if (lane == 0 && dsc[0].x != -3) {
       uint8_t* st = ring.stage_at(s);
       uint64_t* bar = ring.bar_at(s);
-      const int* ix = ring.ix_at(s);
-      auto qrow = [&](int gg) {
-        if (gg >= G) return p.N;
-        const int4 dd = dsc[gg];
-        return (dd.x >= 0 && (dd.z & kFirst)) ? dd.x : p.N;
-      };
-      auto erow = [&](int b) {
-        const int4 dd = dsc[b / SE];
-        return (dd.x >= 0 && b % SE < (dd.z & kCntMask)) ? ix[b] : p.N;
-      };
+      int4 qr[L::QR / 4];
       uint32_t qmask = 0;
 #pragma unroll
       for (int q4 = 0; q4 < L::QR / 4; ++q4) {
-        bool any = false;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) any |= qrow(4 * q4 + j) != p.N;
+        qr[q4] = ring.qset(s, q4);
+        const bool any = qr[q4].x != p.N || qr[q4].y != p.N || qr[q4].z != p.N ||
+                         qr[q4].w != p.N;
         qmask |= uint32_t(any) << q4;
       }
       const uint32_t qset = 3 * L::SET_BYTES + (p.rows16 ? 16 * p.H : 0);
@@ -197,19 +190,17 @@ __global__ void __launch_bounds__(CsrShape<T, RB>::THREADS) bwd_csr_kernel(const
 #pragma unroll
       for (int q4 = 0; q4 < L::QR / 4; ++q4)
         if ((qmask >> q4) & 1) {
-          const int r0 = qrow(4 * q4), r1 = qrow(4 * q4 + 1), r2 = qrow(4 * q4 + 2),
-                    r3 = qrow(4 * q4 + 3);
-          L::gather(st + OQ, 4 * q4, &p.mi0, r0, r1, r2, r3, bar);
-          L::gather(st + ODO, 4 * q4, &p.mi1, r0, r1, r2, r3, bar);
-          L::gather(st + OO, 4 * q4, &p.mi2, r0, r1, r2, r3, bar);
-          if (p.rows16) tma_gather4(st + OL + q4 * L::SSB, &p.ms0, 0, r0, r1, r2, r3, bar);
+          const int4 r = qr[q4];
+          L::gather(st + OQ, 4 * q4, &p.mi0, r.x, r.y, r.z, r.w, bar);
+          L::gather(st + ODO, 4 * q4, &p.mi1, r.x, r.y, r.z, r.w, bar);
+          L::gather(st + OO, 4 * q4, &p.mi2, r.x, r.y, r.z, r.w, bar);
+          if (p.rows16) tma_gather4(st + OL + q4 * L::SSB, &p.ms0, 0, r.x, r.y, r.z, r.w, bar);
         }
 #pragma unroll
       for (int b4 = 0; b4 < B / 4; ++b4) {
-        const int r0 = erow(4 * b4), r1 = erow(4 * b4 + 1), r2 = erow(4 * b4 + 2),
-                  r3 = erow(4 * b4 + 3);
-        L::gather(st + OK, 4 * b4, &p.me0, r0, r1, r2, r3, bar);
-        L::gather(st + OV, 4 * b4, &p.me1, r0, r1, r2, r3, bar);
+        const int4 r = ring.eset(s, b4);
+        L::gather(st + OK, 4 * b4, &p.me0, r.x, r.y, r.z, r.w, bar);
+        L::gather(st + OV, 4 * b4, &p.me1, r.x, r.y, r.z, r.w, bar);
       }
     }
     if (!p.rows16) {  // lse rows of starting items by 4-byte copies
@@ -221,19 +212,19 @@ __global__ void __launch_bounds__(CsrShape<T, RB>::THREADS) bwd_csr_kernel(const
     cp_async_commit();
   };
 
-  for (int s = 0; s < S; ++s) cur.generate(ring.desc_at(s), ring.ix_at(s), lane);
+  for (int s = 0; s < S; ++s) ring.generate(cur, s, lane);
   cp_async_commit();
   cp_async_wait<0>();
   __syncwarp();
   for (int s = 0; s < S - 1; ++s) {
-    cur.generate(ring.desc_at(S + s), ring.ix_at(S + s), lane);
+    ring.generate(cur, S + s, lane);
     issue(s);
   }
 
   float2 q[NC][PP], gq[NC][PP], dq[NC][PP];
-  float lse2[NC], dlt[NC];
+  float lse2[HL], dlt[HL];
   for (int i = 0;; ++i) {
-    cur.generate(ring.desc_at(i + 2 * S - 1), ring.ix_at(i + 2 * S - 1), lane);
+    ring.generate(cur, i + 2 * S - 1, lane);
     __syncwarp();
     issue(i + S - 1);
     cp_async_wait<S - 1>();
@@ -247,8 +238,9 @@ __global__ void __launch_bounds__(CsrShape<T, RB>::THREADS) bwd_csr_kernel(const
     const uint8_t* st = ring.stage_at(i);
     const bool first = act && (d.z & kFirst);
 
-    {  // item start: q, dO, Delta = dO . O, lse (every lane joins the head reduction)
-      float part[NC];
+    if (__any_sync(FULL, first)) {
+      // item start: q, dO, Delta = dO . O, lse (every lane joins the head reduction)
+      float part[NC], dsum[HL];
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
         float2 o[PP];
@@ -266,22 +258,26 @@ __global__ void __launch_bounds__(CsrShape<T, RB>::THREADS) bwd_csr_kernel(const
         for (int v = 0; v < PP; ++v) a2 = f2fma(first ? gq[c][v] : f2s(0.f), o[v], a2);
         part[c] = a2.x + a2.y;
       }
-      head_totals<NC, CPH>(part);
+      head_sums<NC, CPH>(part, dsum);
       if (first) {
         const float* ls = reinterpret_cast<const float*>(st + OL + (g / 4) * L::SSB) + (g % 4) * p.H;
 #pragma unroll
+        for (int j = 0; j < HL; ++j) {
+          const int c0 = j * LH::CPL;
+          dlt[j] = dsum[j];
+          lse2[j] = ls[head[c0]] * kLog2e;
+          // every chunk of a heavy node computes the same Delta: duplicate
+          // writes store identical values
+          if (hw[c0]) p.delta[int64_t(d.x) * p.H + head[c0]] = dlt[j];
+        }
+#pragma unroll
         for (int c = 0; c < NC; ++c) {
-          dlt[c] = part[c];
-          lse2[c] = ls[head[c]] * kLog2e;
           if (!GAT) {
 #pragma unroll
             for (int v = 0; v < PP; ++v) q[c][v] = f2mul(q[c][v], f2s(p.qmul));
           }
 #pragma unroll
           for (int v = 0; v < PP; ++v) dq[c][v] = f2s(0.f);
-          // every chunk of a heavy node computes the same Delta: duplicate
-          // writes store identical values
-          if (hw[c]) p.delta[int64_t(d.x) * p.H + head[c]] = dlt[c];
         }
       }
     }
@@ -293,7 +289,7 @@ __global__ void __launch_bounds__(CsrShape<T, RB>::THREADS) bwd_csr_kernel(const
     for (int k = 0; k < SE; ++k) {
       if (k >= kmax) break;
       const bool valid = k < cnt;
-      float sc[NC], dp[NC];
+      float scp[NC], dpp[NC], sc[HL], dp[HL];
       float2 kf[NC][PP];
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
@@ -314,19 +310,24 @@ __global__ void __launch_bounds__(CsrShape<T, RB>::THREADS) bwd_csr_kernel(const
             s2 = f2fma(av[c][v], lr, s2);
           }
         }
-        sc[c] = s2.x + s2.y;
-        dp[c] = p2.x + p2.y;
+        scp[c] = s2.x + s2.y;
+        dpp[c] = p2.x + p2.y;
       }
-      head_totals<NC, CPH>(sc);
-      head_totals<NC, CPH>(dp);
+      head_sums<NC, CPH>(scp, sc);
+      head_sums<NC, CPH>(dpp, dp);
       if (act && valid) {
+        float ds[HL];
+#pragma unroll
+        for (int j = 0; j < HL; ++j) {
+          const float pr = ex2((GAT ? sc[j] * kLog2e : sc[j]) - lse2[j]);
+          ds[j] = pr * (dp[j] - dlt[j]);
+        }
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
-          const float pr = ex2((GAT ? sc[c] * kLog2e : sc[c]) - lse2[c]);
-          const float ds = pr * (dp[c] - dlt[c]);
+          const float dsc_ = ds[LH::of(c)];
           if (!GAT) {
 #pragma unroll
-            for (int v = 0; v < PP; ++v) dq[c][v] = f2fma(f2s(ds), kf[c][v], dq[c][v]);
+            for (int v = 0; v < PP; ++v) dq[c][v] = f2fma(f2s(dsc_), kf[c][v], dq[c][v]);
           } else {
 #pragma unroll
             for (int v = 0; v < PP; ++v) {
@@ -334,8 +335,8 @@ __global__ void __launch_bounds__(CsrShape<T, RB>::THREADS) bwd_csr_kernel(const
               const float2 sg = make_float2(z.x > 0.f ? 1.f : p.slope, z.y > 0.f ? 1.f : p.slope);
               const float2 lr = make_float2(z.x > 0.f ? z.x : p.slope * z.x,
                                             z.y > 0.f ? z.y : p.slope * z.y);
-              dq[c][v] = f2fma(f2mul(f2s(ds), av[c][v]), sg, dq[c][v]);
-              dacc[c][v] = f2fma(f2s(ds), lr, dacc[c][v]);
+              dq[c][v] = f2fma(f2mul(f2s(dsc_), av[c][v]), sg, dq[c][v]);
+              dacc[c][v] = f2fma(f2s(dsc_), lr, dacc[c][v]);
             }
           }
         }
@@ -459,10 +460,12 @@ __global__ void __launch_bounds__(CscShape<T, RB>::THREADS) bwd_csc_kernel(const
   using Sh = CscShape<T, RB>;
   using PR = Pairs<T>;
   constexpr int NC = L::NC, TPR = L::TPR, G = L::G, SE = L::SE, B = L::B;
-  constexpr int NCH = L::NCH, PP = PR::P, S = kStages, LS = Sh::LS;
+  constexpr int PP = PR::P, S = kStages;
   constexpr int HD = RB / (int)sizeof(T);
   constexpr int D = DB / (int)sizeof(T);  // head width
   constexpr int CPH = DB / 16;            // 16-byte chunks per head
+  using LH = LaneHeads<NC, CPH>;
+  constexpr int HL = LH::N;               // heads of this lane
   constexpr bool GAT = KIND == GATTN_SCORE_GATV2;
   constexpr unsigned FULL = 0xffffffffu;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -489,7 +492,7 @@ __global__ void __launch_bounds__(CscShape<T, RB>::THREADS) bwd_csc_kernel(const
   const int64_t warp = (int64_t(blockIdx.x) * Sh::THREADS + threadIdx.x) >> 5;
   const int64_t nwarps = (int64_t(gridDim.x) * Sh::THREADS) >> 5;
   BundleCursor<G, SE> cur;
-  cur.start(p.sorted, p.n_items, p.idx, warp, nwarps, ring.items, lane);
+  cur.start(p.sorted, p.n_items, p.idx, p.N, warp, nwarps, ring.items, lane);
 
   // stage: [QR][K row] [QR][V row] [B][Q row] [B][dO row] [B][lse row]
   // [B][Delta row].  TMA gathers from lane 0 (pad row N in unused slots);
@@ -502,22 +505,13 @@ __global__ void __launch_bounds__(CscShape<T, RB>::THREADS) bwd_csc_kernel(const
     if (lane == 0 && dsc[0].x != -3) {
       uint8_t* st = ring.stage_at(s);
       uint64_t* bar = ring.bar_at(s);
-      const int* ix = ring.ix_at(s);
-      auto qrow = [&](int gg) {
-        if (gg >= G) return p.N;
-        const int4 dd = dsc[gg];
-        return (dd.x >= 0 && (dd.z & kFirst)) ? dd.x : p.N;
-      };
-      auto erow = [&](int b) {
-        const int4 dd = dsc[b / SE];
-        return (dd.x >= 0 && b % SE < (dd.z & kCntMask)) ? ix[b] : p.N;
-      };
+      int4 qr[L::QR / 4];
       uint32_t qmask = 0;
 #pragma unroll
       for (int q4 = 0; q4 < L::QR / 4; ++q4) {
-        bool any = false;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) any |= qrow(4 * q4 + j) != p.N;
+        qr[q4] = ring.qset(s, q4);
+        const bool any = qr[q4].x != p.N || qr[q4].y != p.N || qr[q4].z != p.N ||
+                         qr[q4].w != p.N;
         qmask |= uint32_t(any) << q4;
       }
       const uint32_t eset =
@@ -527,19 +521,17 @@ __global__ void __launch_bounds__(CscShape<T, RB>::THREADS) bwd_csc_kernel(const
 #pragma unroll
       for (int q4 = 0; q4 < L::QR / 4; ++q4)
         if ((qmask >> q4) & 1) {
-          const int r0 = qrow(4 * q4), r1 = qrow(4 * q4 + 1), r2 = qrow(4 * q4 + 2),
-                    r3 = qrow(4 * q4 + 3);
-          L::gather(st + OKI, 4 * q4, &p.mi0, r0, r1, r2, r3, bar);
-          L::gather(st + OVI, 4 * q4, &p.mi1, r0, r1, r2, r3, bar);
+          const int4 r = qr[q4];
+          L::gather(st + OKI, 4 * q4, &p.mi0, r.x, r.y, r.z, r.w, bar);
+          L::gather(st + OVI, 4 * q4, &p.mi1, r.x, r.y, r.z, r.w, bar);
         }
 #pragma unroll
       for (int b4 = 0; b4 < B / 4; ++b4) {
-        const int r0 = erow(4 * b4), r1 = erow(4 * b4 + 1), r2 = erow(4 * b4 + 2),
-                  r3 = erow(4 * b4 + 3);
-        L::gather(st + OQE, 4 * b4, &p.me0, r0, r1, r2, r3, bar);
-        L::gather(st + OGE, 4 * b4, &p.me1, r0, r1, r2, r3, bar);
-        if (p.rows16) tma_gather4(st + OLS + b4 * L::SSB, &p.ms0, 0, r0, r1, r2, r3, bar);
-        if (p.delta16) tma_gather4(st + ODL + b4 * L::SSB, &p.ms1, 0, r0, r1, r2, r3, bar);
+        const int4 r = ring.eset(s, b4);
+        L::gather(st + OQE, 4 * b4, &p.me0, r.x, r.y, r.z, r.w, bar);
+        L::gather(st + OGE, 4 * b4, &p.me1, r.x, r.y, r.z, r.w, bar);
+        if (p.rows16) tma_gather4(st + OLS + b4 * L::SSB, &p.ms0, 0, r.x, r.y, r.z, r.w, bar);
+        if (p.delta16) tma_gather4(st + ODL + b4 * L::SSB, &p.ms1, 0, r.x, r.y, r.z, r.w, bar);
       }
     }
     if (!p.rows16 || !p.delta16) {  // stat rows of the edges by 4-byte copies
@@ -555,18 +547,18 @@ __global__ void __launch_bounds__(CscShape<T, RB>::THREADS) bwd_csc_kernel(const
     cp_async_commit();
   };
 
-  for (int s = 0; s < S; ++s) cur.generate(ring.desc_at(s), ring.ix_at(s), lane);
+  for (int s = 0; s < S; ++s) ring.generate(cur, s, lane);
   cp_async_commit();
   cp_async_wait<0>();
   __syncwarp();
   for (int s = 0; s < S - 1; ++s) {
-    cur.generate(ring.desc_at(S + s), ring.ix_at(S + s), lane);
+    ring.generate(cur, S + s, lane);
     issue(s);
   }
 
   float2 k[NC][PP], vv[NC][PP], dk[NC][PP], dv[NC][PP];
   for (int i = 0;; ++i) {
-    cur.generate(ring.desc_at(i + 2 * S - 1), ring.ix_at(i + 2 * S - 1), lane);
+    ring.generate(cur, i + 2 * S - 1, lane);
     __syncwarp();
     issue(i + S - 1);
     cp_async_wait<S - 1>();
@@ -601,7 +593,7 @@ __global__ void __launch_bounds__(CscShape<T, RB>::THREADS) bwd_csc_kernel(const
     for (int e = 0; e < SE; ++e) {
       if (e >= kmax) break;
       const bool valid = e < cnt;
-      float sc[NC], dp[NC];
+      float scp[NC], dpp[NC], sc[HL], dp[HL];
       float2 qf[NC][PP], gf[NC][PP];
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
@@ -621,30 +613,36 @@ __global__ void __launch_bounds__(CscShape<T, RB>::THREADS) bwd_csc_kernel(const
             s2 = f2fma(av[c][v], lr, s2);
           }
         }
-        sc[c] = s2.x + s2.y;
-        dp[c] = p2.x + p2.y;
+        scp[c] = s2.x + s2.y;
+        dpp[c] = p2.x + p2.y;
       }
-      head_totals<NC, CPH>(sc);
-      head_totals<NC, CPH>(dp);
+      head_sums<NC, CPH>(scp, sc);
+      head_sums<NC, CPH>(dpp, dp);
       if (act && valid) {
+        const int b = g * SE + e, so = (b / 4) * L::SSB + (b % 4) * 4 * p.H;
+        float pr[HL], ds[HL];
+#pragma unroll
+        for (int j = 0; j < HL; ++j) {
+          const int hh = head[j * LH::CPL];
+          const float ls = reinterpret_cast<const float*>(st + OLS + so)[hh];
+          const float dl = reinterpret_cast<const float*>(st + ODL + so)[hh];
+          pr[j] = ex2((GAT ? sc[j] * kLog2e : sc[j]) - ls * kLog2e);
+          ds[j] = pr[j] * (dp[j] - dl);
+        }
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
-          const int b = g * SE + e, so = (b / 4) * L::SSB + (b % 4) * 4 * p.H;
-          const float ls = reinterpret_cast<const float*>(st + OLS + so)[head[c]];
-          const float dl = reinterpret_cast<const float*>(st + ODL + so)[head[c]];
-          const float pr = ex2((GAT ? sc[c] * kLog2e : sc[c]) - ls * kLog2e);
-          const float ds = pr * (dp[c] - dl);
+          const float prc = pr[LH::of(c)], dsc_ = ds[LH::of(c)];
 #pragma unroll
-          for (int v = 0; v < PP; ++v) dv[c][v] = f2fma(f2s(pr), gf[c][v], dv[c][v]);
+          for (int v = 0; v < PP; ++v) dv[c][v] = f2fma(f2s(prc), gf[c][v], dv[c][v]);
           if (!GAT) {
 #pragma unroll
-            for (int v = 0; v < PP; ++v) dk[c][v] = f2fma(f2s(ds), qf[c][v], dk[c][v]);
+            for (int v = 0; v < PP; ++v) dk[c][v] = f2fma(f2s(dsc_), qf[c][v], dk[c][v]);
           } else {
 #pragma unroll
             for (int v = 0; v < PP; ++v) {
               const float2 z = make_float2(qf[c][v].x + k[c][v].x, qf[c][v].y + k[c][v].y);
               const float2 sg = make_float2(z.x > 0.f ? 1.f : p.slope, z.y > 0.f ? 1.f : p.slope);
-              dk[c][v] = f2fma(f2mul(f2s(ds), av[c][v]), sg, dk[c][v]);
+              dk[c][v] = f2fma(f2mul(f2s(dsc_), av[c][v]), sg, dk[c][v]);
             }
           }
         }
@@ -655,7 +653,6 @@ __global__ void __launch_bounds__(CscShape<T, RB>::THREADS) bwd_csc_kernel(const
     const bool heavy = fin && d.y < p.n_chunks;
     bool write = fin && !heavy;
     if (heavy) {
-      constexpr int HD = RB / (int)sizeof(T);
       auto store = [&](int slot) {
         float* pb = p.part + int64_t(slot) * (2 * HD);
 #pragma unroll

@@ -65,10 +65,12 @@ __global__ void __launch_bounds__(FwdShape<T, RB>::THREADS) fwd_kernel(const __g
   using Sh = FwdShape<T, RB>;
   using PR = Pairs<T>;
   constexpr int NC = L::NC, TPR = L::TPR, G = L::G, SE = L::SE, B = L::B;
-  constexpr int NCH = L::NCH, PP = PR::P, S = kStages;
+  constexpr int PP = PR::P, S = kStages;
   constexpr int HD = RB / (int)sizeof(T);
   constexpr int D = DB / (int)sizeof(T);  // head width
   constexpr int CPH = DB / 16;            // 16-byte chunks per head
+  using LH = LaneHeads<NC, CPH>;
+  constexpr int HL = LH::N;               // heads of this lane
   constexpr bool GAT = KIND == GATTN_SCORE_GATV2;
   constexpr unsigned FULL = 0xffffffffu;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -99,7 +101,7 @@ __global__ void __launch_bounds__(FwdShape<T, RB>::THREADS) fwd_kernel(const __g
   const int64_t warp = (int64_t(blockIdx.x) * Sh::THREADS + threadIdx.x) >> 5;
   const int64_t nwarps = (int64_t(gridDim.x) * Sh::THREADS) >> 5;
   BundleCursor<G, SE> cur;
-  cur.start(p.sorted, p.n_items, p.indices, warp, nwarps, ring.items, lane);
+  cur.start(p.sorted, p.n_items, p.indices, p.N, warp, nwarps, ring.items, lane);
 
   // rows of stage s into its ring slot by TMA gathers issued from lane 0:
   // Q rows of the items that start here (only the 4-row sets that hold one),
@@ -111,22 +113,13 @@ __global__ void __launch_bounds__(FwdShape<T, RB>::THREADS) fwd_kernel(const __g
       if (dsc[0].x != -3) {
         uint8_t* st = ring.stage_at(s);
         uint64_t* bar = ring.bar_at(s);
-        const int* ix = ring.ix_at(s);
-        auto qrow = [&](int gg) {
-          if (gg >= G) return p.N;
-          const int4 dd = dsc[gg];
-          return (dd.x >= 0 && (dd.z & kFirst)) ? dd.x : p.N;
-        };
-        auto erow = [&](int b) {
-          const int4 dd = dsc[b / SE];
-          return (dd.x >= 0 && b % SE < (dd.z & kCntMask)) ? ix[b] : p.N;
-        };
+        int4 qr[L::QR / 4];
         uint32_t qmask = 0;
 #pragma unroll
         for (int q4 = 0; q4 < L::QR / 4; ++q4) {
-          bool any = false;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) any |= qrow(4 * q4 + j) != p.N;
+          qr[q4] = ring.qset(s, q4);
+          const bool any = qr[q4].x != p.N || qr[q4].y != p.N || qr[q4].z != p.N ||
+                           qr[q4].w != p.N;
           qmask |= uint32_t(any) << q4;
         }
         fence_proxy_async();
@@ -134,14 +127,12 @@ __global__ void __launch_bounds__(FwdShape<T, RB>::THREADS) fwd_kernel(const __g
 #pragma unroll
         for (int q4 = 0; q4 < L::QR / 4; ++q4)
           if ((qmask >> q4) & 1)
-            L::gather(st, 4 * q4, &p.mq, qrow(4 * q4), qrow(4 * q4 + 1), qrow(4 * q4 + 2),
-                      qrow(4 * q4 + 3), bar);
+            L::gather(st, 4 * q4, &p.mq, qr[q4].x, qr[q4].y, qr[q4].z, qr[q4].w, bar);
 #pragma unroll
         for (int b4 = 0; b4 < B / 4; ++b4) {
-          const int r0 = erow(4 * b4), r1 = erow(4 * b4 + 1), r2 = erow(4 * b4 + 2),
-                    r3 = erow(4 * b4 + 3);
-          L::gather(st + L::QR * RB, 4 * b4, &p.mk, r0, r1, r2, r3, bar);
-          L::gather(st + (L::QR + B) * RB, 4 * b4, &p.mv, r0, r1, r2, r3, bar);
+          const int4 r = ring.eset(s, b4);
+          L::gather(st + L::QR * RB, 4 * b4, &p.mk, r.x, r.y, r.z, r.w, bar);
+          L::gather(st + (L::QR + B) * RB, 4 * b4, &p.mv, r.x, r.y, r.z, r.w, bar);
         }
       }
     }
@@ -150,19 +141,19 @@ __global__ void __launch_bounds__(FwdShape<T, RB>::THREADS) fwd_kernel(const __g
   };
 
   // prologue: indices of stages 0..S-1, then rows of stages 0..S-2
-  for (int s = 0; s < S; ++s) cur.generate(ring.desc_at(s), ring.ix_at(s), lane);
+  for (int s = 0; s < S; ++s) ring.generate(cur, s, lane);
   cp_async_commit();
   cp_async_wait<0>();
   __syncwarp();
   for (int s = 0; s < S - 1; ++s) {
-    cur.generate(ring.desc_at(S + s), ring.ix_at(S + s), lane);
+    ring.generate(cur, S + s, lane);
     issue(s);
   }
 
   float2 q[NC][PP], acc[NC][PP];
-  float m[NC], l[NC];
+  float m[HL], l[HL];
   for (int i = 0;; ++i) {
-    cur.generate(ring.desc_at(i + 2 * S - 1), ring.ix_at(i + 2 * S - 1), lane);
+    ring.generate(cur, i + 2 * S - 1, lane);
     __syncwarp();
     issue(i + S - 1);
     cp_async_wait<S - 1>();
@@ -183,20 +174,24 @@ __global__ void __launch_bounds__(FwdShape<T, RB>::THREADS) fwd_kernel(const __g
 #pragma unroll
           for (int v = 0; v < PP; ++v) q[c][v] = f2mul(q[c][v], f2s(p.qmul));
         }
-        m[c] = neg_inf();
-        l[c] = 0.f;
 #pragma unroll
         for (int v = 0; v < PP; ++v) acc[c][v] = f2s(0.f);
+      }
+#pragma unroll
+      for (int j = 0; j < HL; ++j) {
+        m[j] = neg_inf();
+        l[j] = 0.f;
       }
     }
 
     const uint8_t* ks = st + L::QR * RB;
     const uint8_t* vs = ks + B * RB;
     const int kmax = __reduce_max_sync(FULL, cnt);  // edges of the warp's longest item here
-    float sc[SE][NC];
+    float sc[SE][HL];
 #pragma unroll
     for (int k = 0; k < SE; ++k) {
       if (k >= kmax) break;
+      float part[NC];
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
         const uint4 kr = k < cnt ? lds16(ks + L::off(g * SE + k, (t * NC + c) * 16)) : make_uint4(0, 0, 0, 0);
@@ -215,39 +210,49 @@ __global__ void __launch_bounds__(FwdShape<T, RB>::THREADS) fwd_kernel(const __g
             a2 = f2fma(av[c][v], lr, a2);
           }
         }
-        sc[k][c] = a2.x + a2.y;
+        part[c] = a2.x + a2.y;
       }
-      head_totals<NC, CPH>(sc[k]);
+      head_sums<NC, CPH>(part, sc[k]);
 #pragma unroll
-      for (int c = 0; c < NC; ++c) {
-        if (GAT) sc[k][c] *= kLog2e;
-        if (k >= cnt) sc[k][c] = neg_inf();
+      for (int j = 0; j < HL; ++j) {
+        if (GAT) sc[k][j] *= kLog2e;
+        if (k >= cnt) sc[k][j] = neg_inf();
       }
     }
     if (act) {
+      float corr[HL], base[HL];
 #pragma unroll
-      for (int c = 0; c < NC; ++c) {
-        float mx = m[c];
+      for (int j = 0; j < HL; ++j) {
+        float mx = m[j];
 #pragma unroll
         for (int k = 0; k < SE; ++k)
-          if (k < cnt) mx = fmaxf(mx, sc[k][c]);
-        const float base = mx == neg_inf() ? 0.f : mx;
-        const float corr = ex2(m[c] - base);
-        l[c] *= corr;
+          if (k < cnt) mx = fmaxf(mx, sc[k][j]);
+        base[j] = mx == neg_inf() ? 0.f : mx;
+        corr[j] = ex2(m[j] - base[j]);
+        l[j] *= corr[j];
+        m[j] = mx;
+      }
 #pragma unroll
-        for (int v = 0; v < PP; ++v) acc[c][v] = f2mul(acc[c][v], f2s(corr));
+      for (int c = 0; c < NC; ++c)
 #pragma unroll
-        for (int k = 0; k < SE; ++k) {
-          if (k < cnt) {
-            const float pk = ex2(sc[k][c] - base);
-            l[c] += pk;
+        for (int v = 0; v < PP; ++v) acc[c][v] = f2mul(acc[c][v], f2s(corr[LH::of(c)]));
+#pragma unroll
+      for (int k = 0; k < SE; ++k) {
+        if (k < cnt) {
+          float pk[HL];
+#pragma unroll
+          for (int j = 0; j < HL; ++j) {
+            pk[j] = ex2(sc[k][j] - base[j]);
+            l[j] += pk[j];
+          }
+#pragma unroll
+          for (int c = 0; c < NC; ++c) {
             float2 vf[PP];
             PR::load(lds16(vs + L::off(g * SE + k, (t * NC + c) * 16)), vf);
 #pragma unroll
-            for (int v = 0; v < PP; ++v) acc[c][v] = f2fma(f2s(pk), vf[v], acc[c][v]);
+            for (int v = 0; v < PP; ++v) acc[c][v] = f2fma(f2s(pk[LH::of(c)]), vf[v], acc[c][v]);
           }
         }
-        m[c] = mx;
       }
     }
 
@@ -264,53 +269,65 @@ __global__ void __launch_bounds__(FwdShape<T, RB>::THREADS) fwd_kernel(const __g
           for (int v = 0; v < PP; v += 2)
             *reinterpret_cast<float4*>(pb + elem[c] + 2 * v) =
                 make_float4(acc[c][v].x, acc[c][v].y, acc[c][v + 1].x, acc[c][v + 1].y);
-          if (hw[c]) {
-            pb[HD + head[c]] = m[c];
-            pb[HD + p.H + head[c]] = l[c];
-          }
         }
+#pragma unroll
+        for (int j = 0; j < HL; ++j)
+          if (hw[j * LH::CPL]) {
+            pb[HD + head[j * LH::CPL]] = m[j];
+            pb[HD + p.H + head[j * LH::CPL]] = l[j];
+          }
       };
       auto merge = [&](int c0, int cn) {
 #pragma unroll
-        for (int c = 0; c < NC; ++c) {
-          m[c] = neg_inf();
-          l[c] = 0.f;
+        for (int c = 0; c < NC; ++c)
 #pragma unroll
           for (int v = 0; v < PP; ++v) acc[c][v] = f2s(0.f);
+#pragma unroll
+        for (int j = 0; j < HL; ++j) {
+          m[j] = neg_inf();
+          l[j] = 0.f;
         }
         for (int kk = 0; kk < cn; kk += 4) {  // four children's loads in flight at a time
-          float mo[4][NC], lo[4][NC];
+          float mo[4][HL], lo[4][HL];
           float4 f[4][NC][PP / 2];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const bool ok = kk + j < cn;
-            const float* pc = p.part + int64_t(c0 + (ok ? kk + j : 0)) * p.pstride;
+          for (int jj = 0; jj < 4; ++jj) {
+            const bool ok = kk + jj < cn;
+            const float* pc = p.part + int64_t(c0 + (ok ? kk + jj : 0)) * p.pstride;
 #pragma unroll
-            for (int c = 0; c < NC; ++c) {
-              mo[j][c] = ok ? __ldcg(pc + HD + head[c]) : neg_inf();
-              lo[j][c] = ok ? __ldcg(pc + HD + p.H + head[c]) : 0.f;
+            for (int j = 0; j < HL; ++j) {
+              mo[jj][j] = ok ? __ldcg(pc + HD + head[j * LH::CPL]) : neg_inf();
+              lo[jj][j] = ok ? __ldcg(pc + HD + p.H + head[j * LH::CPL]) : 0.f;
+            }
+#pragma unroll
+            for (int c = 0; c < NC; ++c)
 #pragma unroll
               for (int v = 0; v < PP / 2; ++v)
-                f[j][c][v] = ok ? __ldcg(reinterpret_cast<const float4*>(pc + elem[c] + 4 * v))
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+                f[jj][c][v] = ok ? __ldcg(reinterpret_cast<const float4*>(pc + elem[c] + 4 * v))
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
           }
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
+          for (int jj = 0; jj < 4; ++jj) {
+            float c1[HL], c2[HL];
+#pragma unroll
+            for (int j = 0; j < HL; ++j) {
+              const float mn = fmaxf(m[j], mo[jj][j]);
+              const float base = mn == neg_inf() ? 0.f : mn;
+              c1[j] = ex2(m[j] - base);
+              c2[j] = ex2(mo[jj][j] - base);
+              l[j] = l[j] * c1[j] + lo[jj][j] * c2[j];
+              m[j] = mn;
+            }
 #pragma unroll
             for (int c = 0; c < NC; ++c) {
-              const float mn = fmaxf(m[c], mo[j][c]);
-              const float base = mn == neg_inf() ? 0.f : mn;
-              const float c1 = ex2(m[c] - base), c2 = ex2(mo[j][c] - base);
-              l[c] = l[c] * c1 + lo[j][c] * c2;
+              const float a1 = c1[LH::of(c)], a2 = c2[LH::of(c)];
 #pragma unroll
               for (int v = 0; v < PP / 2; ++v) {
-                acc[c][2 * v] = f2fma(acc[c][2 * v], f2s(c1),
-                                      f2mul(make_float2(f[j][c][v].x, f[j][c][v].y), f2s(c2)));
-                acc[c][2 * v + 1] = f2fma(acc[c][2 * v + 1], f2s(c1),
-                                          f2mul(make_float2(f[j][c][v].z, f[j][c][v].w), f2s(c2)));
+                acc[c][2 * v] = f2fma(acc[c][2 * v], f2s(a1),
+                                      f2mul(make_float2(f[jj][c][v].x, f[jj][c][v].y), f2s(a2)));
+                acc[c][2 * v + 1] = f2fma(acc[c][2 * v + 1], f2s(a1),
+                                          f2mul(make_float2(f[jj][c][v].z, f[jj][c][v].w), f2s(a2)));
               }
-              m[c] = mn;
             }
           }
         }
@@ -319,15 +336,20 @@ __global__ void __launch_bounds__(FwdShape<T, RB>::THREADS) fwd_kernel(const __g
     }
     if (write) {
       char* ob = static_cast<char*>(p.out) + int64_t(d.x) * RB;
+      float inv[HL];
+#pragma unroll
+      for (int j = 0; j < HL; ++j) {
+        inv[j] = l[j] > 0.f ? 1.f / l[j] : 0.f;
+        if (hw[j * LH::CPL])
+          p.lse[int64_t(d.x) * p.H + head[j * LH::CPL]] =
+              l[j] > 0.f ? (m[j] + lg2(l[j])) * kLn2 : neg_inf();
+      }
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
-        const float inv = l[c] > 0.f ? 1.f / l[c] : 0.f;
         float2 o[PP];
 #pragma unroll
-        for (int v = 0; v < PP; ++v) o[v] = f2mul(acc[c][v], f2s(inv));
+        for (int v = 0; v < PP; ++v) o[v] = f2mul(acc[c][v], f2s(inv[LH::of(c)]));
         *reinterpret_cast<uint4*>(ob + (t * NC + c) * 16) = PR::store(o);
-        if (hw[c])
-          p.lse[int64_t(d.x) * p.H + head[c]] = l[c] > 0.f ? (m[c] + lg2(l[c])) * kLn2 : neg_inf();
       }
     }
     __syncwarp();

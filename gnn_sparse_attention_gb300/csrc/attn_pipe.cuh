@@ -15,16 +15,16 @@
 // groups run in lockstep.
 //
 // Pipeline (one per warp, three levels, no inter-warp waits):
-//   units  : 32 consecutive sorted items; the NEXT unit of the warp is loaded
-//            into registers (one item per lane) when the current one starts,
+//   items  : the warp's next block of 32 / G bundles (one sorted item per
+//            lane) is loaded into registers when the current block starts,
 //            and stored to shared memory when it becomes current;
 //   indices: stage t's descriptors (one per group: node, item, edge count,
 //            FIRST/LAST flags) are generated and its source indices copied
 //            (cp.async) 2S - 1 stages before t is computed;
-//   rows   : stage t's rows (Q/K/V or their gradients' operands) are copied
-//            by the TMA engine, one cp.async.bulk per row issued by one lane,
-//            S - 1 stages before t is computed; completion is counted in
-//            bytes on the stage slot's mbarrier.
+//   rows   : stage t's rows (Q/K/V or their gradients' operands) are fetched
+//            by the TMA engine S - 1 stages before t is computed, four rows
+//            per tile::gather4 copy issued by one lane; completion is counted
+//            in bytes on the stage slot's mbarrier.
 // A stage holds SE edges of each of the G items.  Index copies complete
 // through cp.async.wait_group (a hardware wait on the thread's own copies);
 // the row barriers are polled with mbarrier.try_wait under an iteration
@@ -38,7 +38,7 @@ namespace gattn {
 
 constexpr int kStages = 3;           // row stages in flight + 1
 constexpr int kRing = 2 * kStages;   // descriptor / index ring entries
-constexpr int kUnit = 32;            // items per unit
+constexpr int kUnit = 32;            // items per block of bundles
 constexpr int kFirst = 1 << 29;
 constexpr int kLast = 1 << 30;
 constexpr int kCntMask = 0xffff;
@@ -66,8 +66,10 @@ struct Lay {
   static constexpr int NCOL = HD / BOXE;
   static constexpr int BOXB = BOXE * (int)sizeof(T);
   static constexpr int IDXB = (B * 4 + 15) / 16 * 16;
-  // the warp's descriptor ring, index ring, unit buffer and row barriers
-  static constexpr int META = kRing * G * 16 + kRing * IDXB + kUnit * 16 + 16 * ((kStages + 1) / 2);
+  // the warp's descriptor ring, index ring, item-row ring, unit buffer and
+  // row barriers
+  static constexpr int META =
+      kRing * G * 16 + kRing * IDXB + kRing * QR * 4 + kUnit * 16 + 16 * ((kStages + 1) / 2);
   static_assert(TPR >= 1 && TPR <= 32 && 32 % TPR == 0, "thread layout");
   static_assert(B <= 32 && B % 4 == 0, "stage edges");
   // Byte offset of row byte x of row b in a region filled by 4-row gathers:
@@ -216,31 +218,34 @@ __device__ __forceinline__ float2 f2fma(float2 a, float2 b, float2 c) { return _
 __device__ __forceinline__ float2 f2mul(float2 a, float2 b) { return __fmul2_rn(a, b); }
 __device__ __forceinline__ float2 f2s(float s) { return make_float2(s, s); }
 
-// Combine per-chunk partial sums into per-head totals.  CPH = 16-byte chunks
-// per head.  Chunks of one thread that share a head are summed in-thread;
-// heads wider than a thread (CPH > NC) reduce over CPH / NC lanes.  Every
-// lane of the warp must call this (it may shuffle).
+// The heads a lane's NC chunks belong to: NC / CPH of them when a head is
+// narrower than the lane's slice, else one (the lane holds part of a head).
+// Per-head quantities (running max, sum, probabilities) are kept once per
+// lane head, not once per chunk.
 template <int NC, int CPH>
-__device__ __forceinline__ void head_totals(float* x) {
-  if constexpr (CPH == 1) {
-    return;
-  } else if constexpr (CPH >= NC) {
-    float s = 0.f;
+struct LaneHeads {
+  static constexpr int N = CPH >= NC ? 1 : NC / CPH;  // heads per lane
+  static constexpr int CPL = NC / N;                  // chunks per lane head
+  __device__ __forceinline__ static constexpr int of(int c) { return c / CPL; }
+};
+
+// Per-lane-head totals y[LaneHeads::N] of per-chunk partial sums x[NC]: the
+// chunks of a lane head are summed in-thread, and heads wider than a lane
+// reduce over CPH / NC lanes.  Every lane of the warp must call this (it may
+// shuffle).
+template <int NC, int CPH>
+__device__ __forceinline__ void head_sums(const float* x, float* y) {
+  using LH = LaneHeads<NC, CPH>;
 #pragma unroll
-    for (int c = 0; c < NC; ++c) s += x[c];
+  for (int j = 0; j < LH::N; ++j) {
+    float s = x[j * LH::CPL];
 #pragma unroll
-    for (int o = 1; o < CPH / NC; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    for (int c = 1; c < LH::CPL; ++c) s += x[j * LH::CPL + c];
+    y[j] = s;
+  }
+  if constexpr (CPH > NC) {
 #pragma unroll
-    for (int c = 0; c < NC; ++c) x[c] = s;
-  } else {  // 1 < CPH < NC: in-thread groups of CPH chunks
-#pragma unroll
-    for (int c0 = 0; c0 < NC; c0 += CPH) {
-      float s = 0.f;
-#pragma unroll
-      for (int c = 0; c < CPH; ++c) s += x[c0 + c];
-#pragma unroll
-      for (int c = 0; c < CPH; ++c) x[c0 + c] = s;
-    }
+    for (int o = 1; o < CPH / NC; o <<= 1) y[0] += __shfl_xor_sync(0xffffffffu, y[0], o);
   }
 }
 
@@ -260,6 +265,7 @@ struct BundleCursor {
   static constexpr int R = kUnit / G;  // bundles per block
   const int4* sorted;     // items by decreasing length: (node, e0, e1, item index)
   const int32_t* idx;     // CSR sources (or CSC destinations)
+  int pad;                // row index of unused gather slots (zero-filled)
   int64_t n_items, n_bundles, W, w, r_next;
   int4* s_items;          // [kUnit] current block of bundles, shared memory
   int4 pf;                // next block's item of this lane
@@ -288,9 +294,11 @@ struct BundleCursor {
     if (live) maxlen = s_items[0].z - s_items[0].y;
   }
   __device__ __forceinline__ void start(const int4* sorted_, int64_t n_items_, const int32_t* idx_,
-                                        int64_t warp, int64_t nwarps, int4* s_items_, int lane) {
+                                        int pad_, int64_t warp, int64_t nwarps, int4* s_items_,
+                                        int lane) {
     sorted = sorted_;
     idx = idx_;
+    pad = pad_;
     n_items = n_items_;
     n_bundles = (n_items_ + G - 1) / G;
     W = nwarps;
@@ -301,10 +309,13 @@ struct BundleCursor {
     advance(lane);
   }
 
-  // Generate the next stage into ring slot (desc[G], ix[B]): lane g < G
-  // writes group g's descriptor {node (-1 idle, -3 end), item, count|flags,
-  // first edge}; lanes b < B copy the stage's source indices.
-  __device__ __forceinline__ void generate(int4* desc, int* ix, int lane) {
+  // Generate the next stage into ring slot (desc[G], ix[B], qix[QR]): lane
+  // g < G writes group g's descriptor {node (-1 idle, -3 end), item,
+  // count|flags, first edge}; lanes b < B copy the stage's source indices
+  // (pad in unused slots); qix[g] is the node of an item that starts here,
+  // else pad.  The issuing lane then reads whole 4-row sets from ix / qix.
+  template <int QR>
+  __device__ __forceinline__ void generate(int4* desc, int* ix, int* qix, int lane) {
     constexpr unsigned FULL = 0xffffffffu;
     int4 d = make_int4(-1, 0, 0, 0);
     if (!live) {
@@ -321,10 +332,14 @@ struct BundleCursor {
       }
       desc[lane] = d;
     }
+    if (lane < QR) qix[lane] = (d.x >= 0 && (d.z & kFirst)) ? d.x : pad;
     const int g = (lane / SE) & 31, k = lane % SE;
     const int es = __shfl_sync(FULL, d.w, g);
     const int cn = __shfl_sync(FULL, d.x >= 0 ? (d.z & kCntMask) : 0, g);
-    if (lane < B && k < cn) cp_async4(ix + lane, idx + es + k);
+    if (lane < B) {
+      if (k < cn) cp_async4(ix + lane, idx + es + k);
+      else ix[lane] = pad;
+    }
     off += SE;
     if (off >= maxlen) {
       bi += G;
@@ -387,13 +402,15 @@ struct Ring {
   uint8_t* data;  // [kStages][STAGE]
   int4* desc;     // [kRing][G]
   uint8_t* ix;    // [kRing][IDXB]
+  int* qix;       // [kRing][QR]
   int4* items;    // [kUnit]
   uint64_t* bar;  // [kStages] row barriers
   __device__ __forceinline__ void init(uint8_t* base, int lane) {
     data = base;
     desc = reinterpret_cast<int4*>(base + kStages * STAGE);
     ix = reinterpret_cast<uint8_t*>(desc + kRing * L::G);
-    items = reinterpret_cast<int4*>(ix + kRing * L::IDXB);
+    qix = reinterpret_cast<int*>(ix + kRing * L::IDXB);
+    items = reinterpret_cast<int4*>(qix + kRing * L::QR);
     bar = reinterpret_cast<uint64_t*>(items + kUnit);
     if (lane == 0) {
       for (int k = 0; k < kStages; ++k) mbar_init(bar + k, 1);
@@ -421,6 +438,19 @@ struct Ring {
   __device__ __forceinline__ int4* desc_at(int t) { return desc + (t % kRing) * L::G; }
   __device__ __forceinline__ int* ix_at(int t) {
     return reinterpret_cast<int*>(ix + (t % kRing) * L::IDXB);
+  }
+  __device__ __forceinline__ int* qix_at(int t) { return qix + (t % kRing) * L::QR; }
+  // rows of 4-row set q4 of stage t's items / e4 of its edges
+  __device__ __forceinline__ int4 qset(int t, int q4) {
+    return reinterpret_cast<const int4*>(qix_at(t))[q4];
+  }
+  __device__ __forceinline__ int4 eset(int t, int e4) {
+    return reinterpret_cast<const int4*>(ix_at(t))[e4];
+  }
+  // Generate stage t with the cursor.
+  template <class Cursor>
+  __device__ __forceinline__ void generate(Cursor& cur, int t, int lane) {
+    cur.template generate<L::QR>(desc_at(t), ix_at(t), qix_at(t), lane);
   }
   __device__ __forceinline__ uint8_t* stage_at(int t) { return data + (t % kStages) * STAGE; }
 };

@@ -129,40 +129,6 @@ __global__ void k_fill_items(const int32_t* __restrict__ ptr, int32_t N, int32_t
 }
 
 // Item edge counts (for the unit segmentation).
-__global__ void k_item_edges(const int4* __restrict__ items, int64_t n, int32_t* __restrict__ len) {
-  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i <= n; i += stride)
-    len[i] = i < n ? items[i].z - items[i].y : 0;
-}
-
-// Unit starts: item 0, every multiple of kUnitItems, a new kUnitBucket edge
-// bucket of the exclusive edge prefix, or a gap in the edge ranges.
-__global__ void k_unit_flags(const int4* __restrict__ items, int64_t n,
-                             const int32_t* __restrict__ epre, int32_t* __restrict__ flag) {
-  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i <= n; i += stride) {
-    if (i == n) {
-      flag[n] = 0;
-      continue;
-    }
-    bool f = i == 0 || (i % kUnitItems) == 0 || epre[i] / kUnitBucket != epre[i - 1] / kUnitBucket ||
-             items[i].y != items[i - 1].z;
-    flag[i] = f ? 1 : 0;
-  }
-}
-
-__global__ void k_fill_units(const int4* __restrict__ items, int64_t n,
-                             const int32_t* __restrict__ flag, const int32_t* __restrict__ upos,
-                             int4* __restrict__ units) {
-  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
-    if (!flag[i]) continue;
-    int64_t e = i + 1;
-    while (e < n && !flag[e]) ++e;  // at most kUnitItems - 1 steps
-    units[upos[i]] = make_int4((int)i, (int)e, items[i].y, items[e - 1].z);
-  }
-}
-
 // Merge trees over the chunks of every heavy node (fan-in kTreeFanIn).
 __device__ __forceinline__ int32_t tree_inner(int32_t n) {
   int32_t total = 0;
@@ -404,16 +370,169 @@ __global__ void k_edge_rows(const int32_t* __restrict__ indptr, int32_t N,
   }
 }
 
+// ---------------------------------------------------------------------------
+// dense tiles ("Methodology", attention-based layers, tensor-core
+// optimisation: locally dense neighbourhoods packed into block tiles)
+// ---------------------------------------------------------------------------
+// Block key of every edge, (row block) * nb + (column block) as an unsigned
+// bit pattern, the edge id, and the edge's row for the mask pass.
+__global__ void k_block_keys(const int32_t* __restrict__ indptr, int32_t N,
+                             const int32_t* __restrict__ indices, int64_t M, uint32_t nb,
+                             int32_t* __restrict__ key, int32_t* __restrict__ eid,
+                             int32_t* __restrict__ row) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < M; e += stride) {
+    int32_t lo = 0, hi = N;  // invariant: indptr[lo] <= e < indptr[hi]
+    while (hi - lo > 1) {
+      const int32_t mid = lo + (hi - lo) / 2;
+      if (indptr[mid] <= e) lo = mid;
+      else hi = mid;
+    }
+    row[e] = lo;
+    eid[e] = (int32_t)e;
+    key[e] = (int32_t)(uint32_t(lo / kTileRows) * nb + uint32_t(indices[e] / kTileRows));
+  }
+}
+
+// head[p] = 1 where the sorted keys start a new block (head[n] = 0)
+__global__ void k_run_heads(const int32_t* __restrict__ key, int64_t n, int32_t* __restrict__ head) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i <= n; i += stride)
+    head[i] = i < n && (i == 0 || key[i] != key[i - 1]) ? 1 : 0;
+}
+
+// start[pos[i]] = i at every head; start[n_runs] = n
+__global__ void k_run_starts(const int32_t* __restrict__ head, const int32_t* __restrict__ pos,
+                             int64_t n, int32_t* __restrict__ start) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i <= n; i += stride)
+    if (i == n) start[pos[n]] = (int32_t)n;
+    else if (head[i]) start[pos[i]] = (int32_t)i;
+}
+
+// dense[r] = 1 for runs (blocks) of at least tile_min edges (dense[n_runs] = 0)
+__global__ void k_run_dense(const int32_t* __restrict__ start, int64_t n_runs, int32_t tile_min,
+                            int32_t* __restrict__ dense) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t r = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; r <= n_runs; r += stride)
+    dense[r] = r < n_runs && start[r + 1] - start[r] >= tile_min ? 1 : 0;
+}
+
+__global__ void k_tile_meta(const int32_t* __restrict__ start, const int32_t* __restrict__ dense,
+                            const int32_t* __restrict__ tpos, int64_t n_runs,
+                            const int32_t* __restrict__ key, uint32_t nb,
+                            int32_t* __restrict__ tile_rb, int32_t* __restrict__ tile_cb,
+                            int32_t* __restrict__ tbeg, int32_t* __restrict__ tend) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t r = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; r < n_runs; r += stride) {
+    if (!dense[r]) continue;
+    const int32_t t = tpos[r];
+    const uint32_t k = uint32_t(key[start[r]]);
+    tile_rb[t] = int32_t(k / nb);
+    tile_cb[t] = int32_t(k % nb);
+    tbeg[t] = start[r];
+    tend[t] = start[r + 1];
+  }
+}
+
+// One block per tile: set the bits of the tile's (row, column) pairs in
+// shared memory, drop the pairs seen more than once, publish the mask and
+// flag the edges it covers.
+__global__ void k_tile_masks(const int32_t* __restrict__ tbeg, const int32_t* __restrict__ tend,
+                             const int32_t* __restrict__ seid, const int32_t* __restrict__ row,
+                             const int32_t* __restrict__ indices, uint32_t* __restrict__ mask,
+                             uint8_t* __restrict__ in_tile) {
+  __shared__ uint32_t s_seen[kTileRows * 4], s_dup[kTileRows * 4];
+  const int64_t t = blockIdx.x;
+  for (int w = threadIdx.x; w < kTileRows * 4; w += blockDim.x) s_seen[w] = s_dup[w] = 0;
+  __syncthreads();
+  const int32_t b = tbeg[t], e1 = tend[t];
+  for (int32_t p = b + threadIdx.x; p < e1; p += blockDim.x) {
+    const int32_t e = seid[p];
+    const int r = row[e] % kTileRows, c = indices[e] % kTileRows;
+    const uint32_t bit = 1u << (c % 32);
+    if (atomicOr(&s_seen[r * 4 + c / 32], bit) & bit) atomicOr(&s_dup[r * 4 + c / 32], bit);
+  }
+  __syncthreads();
+  for (int w = threadIdx.x; w < kTileRows * 4; w += blockDim.x) {
+    const uint32_t m = s_seen[w] & ~s_dup[w];
+    mask[t * kTileRows * 4 + w] = m;
+    s_seen[w] = m;
+  }
+  __syncthreads();
+  for (int32_t p = b + threadIdx.x; p < e1; p += blockDim.x) {
+    const int32_t e = seid[p];
+    const int r = row[e] % kTileRows, c = indices[e] % kTileRows;
+    if ((s_seen[r * 4 + c / 32] >> (c % 32)) & 1u) in_tile[e] = 1;
+  }
+}
+
+// Residual CSR: a warp per row counts (then copies, in CSR order) the edges
+// outside the tiles.
+__global__ void k_res_count(const int32_t* __restrict__ indptr, int32_t N,
+                            const uint8_t* __restrict__ in_tile, int32_t* __restrict__ cnt) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t i = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; i <= N; i += warps) {
+    if (i == N) {
+      if (lane == 0) cnt[N] = 0;
+      continue;
+    }
+    int32_t c = 0;
+    for (int32_t e = indptr[i] + lane; e < indptr[i + 1]; e += 32) c += in_tile[e] ? 0 : 1;
+    c = __reduce_add_sync(0xffffffffu, c);
+    if (lane == 0) cnt[i] = c;
+  }
+}
+
+__global__ void k_res_fill(const int32_t* __restrict__ indptr, int32_t N,
+                           const int32_t* __restrict__ indices, const uint8_t* __restrict__ in_tile,
+                           const int32_t* __restrict__ ptr_r, int32_t* __restrict__ idx_r) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t i = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; i < N; i += warps) {
+    int32_t out = ptr_r[i];
+    const int32_t e1 = indptr[i + 1];
+    for (int32_t e0 = indptr[i]; e0 < e1; e0 += 32) {
+      const int32_t e = e0 + lane;
+      const bool keep = e < e1 && !in_tile[e];
+      const unsigned bal = __ballot_sync(0xffffffffu, keep);
+      if (keep) idx_r[out + __popc(bal & ((1u << lane) - 1u))] = indices[e];
+      out += __popc(bal);
+    }
+  }
+}
+
+// Row blocks that have tiles (tiles are in row-block order).
+__global__ void k_trow_heads(const int32_t* __restrict__ tile_rb, int64_t n, int32_t* __restrict__ head) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t t = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; t <= n; t += stride)
+    head[t] = t < n && (t == 0 || tile_rb[t] != tile_rb[t - 1]) ? 1 : 0;
+}
+
+__global__ void k_trow_fill(const int32_t* __restrict__ tile_rb, const int32_t* __restrict__ head,
+                            const int32_t* __restrict__ pos, int64_t n, int32_t* __restrict__ trow_rb,
+                            int32_t* __restrict__ trow_ptr) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t t = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; t <= n; t += stride)
+    if (t == n) trow_ptr[pos[n]] = (int32_t)n;
+    else if (head[t]) {
+      trow_rb[pos[t]] = tile_rb[t];
+      trow_ptr[pos[t]] = (int32_t)t;
+    }
+}
+
 int grid_1d(int64_t n, int num_sms) {
   const int64_t want = (n + kThreads - 1) / kThreads;
   const int64_t cap = int64_t(num_sms) * 8;
   return (int)(want < 1 ? 1 : (want > cap ? cap : want));
 }
 
-// Stable LSD radix sort of (key, value) pairs, keys in [0, 2^bits); the
-// sorted values end in *vout_final (one of the scratch buffers).
+// Stable LSD radix sort of (key, value) pairs, keys in [0, 2^bits) (bit
+// patterns of unsigned keys, bits <= 32); the sorted values end in
+// *vout_final and the sorted keys in *kout_final (scratch buffers).
 gattn_status radix_sort(int32_t* keys, int32_t* vals, int64_t n, int bits, Scratch& scr,
-                        cudaStream_t st, int32_t** vout_final) {
+                        cudaStream_t st, int32_t** vout_final, int32_t** kout_final = nullptr) {
   int32_t *kb, *vb, *hist, *offs;
   const int64_t tiles = (n + kTile - 1) / kTile;
   GATTN_CUDA(scr.get(&kb, n));
@@ -439,6 +558,7 @@ gattn_status radix_sort(int32_t* keys, int32_t* vals, int64_t n, int bits, Scrat
     vout = t;
   }
   *vout_final = vin;
+  if (kout_final) *kout_final = kin;
   return GATTN_OK;
 }
 
@@ -446,9 +566,9 @@ gattn_status radix_sort(int32_t* keys, int32_t* vals, int64_t n, int bits, Scrat
 // scans, item list.  Allocates its outputs in the plan.
 struct Side {
   int32_t *deg, *hist, *maxdeg, *light_list, *hfirst, *parent;
-  int4 *items, *units, *sorted;
+  int4 *items, *sorted;
   int2* kids;
-  int64_t n_light, n_heavy, n_chunks, n_units, n_inner;
+  int64_t n_light, n_heavy, n_chunks, n_inner;
 };
 
 template <typename T>
@@ -499,28 +619,7 @@ gattn_status build_side(Plan* p, const int32_t* ptr, Scratch& scr, cudaStream_t 
                                                             s->n_chunks, s->n_heavy, s->light_list,
                                                             s->items, s->hfirst);
   GATTN_CUDA(cudaGetLastError());
-  // work units over the item list
   const int64_t n_items = s->n_light + s->n_chunks;
-  int32_t *len, *epre, *flag, *upos;
-  GATTN_CUDA(scr.get(&len, n_items + 1));
-  GATTN_CUDA(scr.get(&epre, n_items + 1));
-  GATTN_CUDA(scr.get(&flag, n_items + 1));
-  GATTN_CUDA(scr.get(&upos, n_items + 1));
-  k_item_edges<<<grid_1d(n_items + 1, p->num_sms), kThreads, 0, st>>>(s->items, n_items, len);
-  GATTN_CUDA(cudaGetLastError());
-  if ((r = exclusive_scan(len, epre, n_items + 1, scr, st)) != GATTN_OK) return r;
-  k_unit_flags<<<grid_1d(n_items + 1, p->num_sms), kThreads, 0, st>>>(s->items, n_items, epre,
-                                                                      flag);
-  GATTN_CUDA(cudaGetLastError());
-  if ((r = exclusive_scan(flag, upos, n_items + 1, scr, st)) != GATTN_OK) return r;
-  int32_t nu = 0;
-  GATTN_CUDA(cudaMemcpyAsync(&nu, upos + n_items, 4, cudaMemcpyDeviceToHost, st));
-  GATTN_CUDA(cudaStreamSynchronize(st));
-  s->n_units = nu;
-  GATTN_CUDA(plan_alloc(p, &s->units, s->n_units));
-  k_fill_units<<<grid_1d(n_items, p->num_sms), kThreads, 0, st>>>(s->items, n_items, flag, upos,
-                                                                  s->units);
-  GATTN_CUDA(cudaGetLastError());
   // merge trees over the heavy nodes' chunks
   {
     int32_t *inner, *ipos;
@@ -555,6 +654,116 @@ gattn_status build_side(Plan* p, const int32_t* ptr, Scratch& scr, cudaStream_t 
                                                                        s->sorted);
     GATTN_CUDA(cudaGetLastError());
   }
+  return GATTN_OK;
+}
+
+// Dense tiles and the residual CSR with its forward split (plan fields
+// tile_*, trow_*, *_r).  Needs p->tile_min > 0.
+gattn_status tile_build(Plan* p, Scratch& scr, cudaStream_t st) {
+  const int32_t N = p->N;
+  const int64_t M = p->M;
+  const uint32_t nb = uint32_t((int64_t(N) + kTileRows - 1) / kTileRows);
+  int32_t *key, *eid, *row, *seid, *skey;
+  uint8_t* in_tile;
+  GATTN_CUDA(scr.get(&key, M));
+  GATTN_CUDA(scr.get(&eid, M));
+  GATTN_CUDA(scr.get(&row, M));
+  GATTN_CUDA(scr.get(&in_tile, M));
+  GATTN_CUDA(cudaMemsetAsync(in_tile, 0, M ? M : 1, st));
+  gattn_status r;
+  int32_t n_runs = 0, n_tiles = 0;
+  int32_t *start = nullptr, *dense = nullptr, *tpos = nullptr;
+  if (M) {
+    k_block_keys<<<grid_1d(M, p->num_sms), kThreads, 0, st>>>(p->indptr, N, p->indices, M, nb, key,
+                                                              eid, row);
+    GATTN_CUDA(cudaGetLastError());
+    const uint64_t nkeys = uint64_t(nb) * nb;
+    int bits = 1;
+    while (bits < 32 && (uint64_t(1) << bits) < nkeys) ++bits;
+    if ((r = radix_sort(key, eid, M, bits, scr, st, &seid, &skey)) != GATTN_OK) return r;
+    int32_t *head, *pos;
+    GATTN_CUDA(scr.get(&head, M + 1));
+    GATTN_CUDA(scr.get(&pos, M + 1));
+    k_run_heads<<<grid_1d(M + 1, p->num_sms), kThreads, 0, st>>>(skey, M, head);
+    GATTN_CUDA(cudaGetLastError());
+    if ((r = exclusive_scan(head, pos, M + 1, scr, st)) != GATTN_OK) return r;
+    GATTN_CUDA(cudaMemcpyAsync(&n_runs, pos + M, 4, cudaMemcpyDeviceToHost, st));
+    GATTN_CUDA(cudaStreamSynchronize(st));
+    GATTN_CUDA(scr.get(&start, int64_t(n_runs) + 1));
+    GATTN_CUDA(scr.get(&dense, int64_t(n_runs) + 1));
+    GATTN_CUDA(scr.get(&tpos, int64_t(n_runs) + 1));
+    k_run_starts<<<grid_1d(M + 1, p->num_sms), kThreads, 0, st>>>(head, pos, M, start);
+    GATTN_CUDA(cudaGetLastError());
+    k_run_dense<<<grid_1d(int64_t(n_runs) + 1, p->num_sms), kThreads, 0, st>>>(start, n_runs,
+                                                                              p->tile_min, dense);
+    GATTN_CUDA(cudaGetLastError());
+    if ((r = exclusive_scan(dense, tpos, int64_t(n_runs) + 1, scr, st)) != GATTN_OK) return r;
+    GATTN_CUDA(cudaMemcpyAsync(&n_tiles, tpos + n_runs, 4, cudaMemcpyDeviceToHost, st));
+    GATTN_CUDA(cudaStreamSynchronize(st));
+  }
+  p->n_tiles = n_tiles;
+  GATTN_CUDA(plan_alloc(p, &p->tile_rb, n_tiles));
+  GATTN_CUDA(plan_alloc(p, &p->tile_cb, n_tiles));
+  GATTN_CUDA(plan_alloc(p, &p->tile_mask, int64_t(n_tiles) * kTileRows * 4));
+  if (n_tiles > 0) {
+    int32_t *tbeg, *tend;
+    GATTN_CUDA(scr.get(&tbeg, n_tiles));
+    GATTN_CUDA(scr.get(&tend, n_tiles));
+    k_tile_meta<<<grid_1d(n_runs, p->num_sms), kThreads, 0, st>>>(start, dense, tpos, n_runs, skey,
+                                                                 nb, p->tile_rb, p->tile_cb, tbeg,
+                                                                 tend);
+    GATTN_CUDA(cudaGetLastError());
+    k_tile_masks<<<(unsigned)n_tiles, kThreads, 0, st>>>(tbeg, tend, seid, row, p->indices,
+                                                        p->tile_mask, in_tile);
+    GATTN_CUDA(cudaGetLastError());
+  }
+  // residual CSR
+  int32_t* cnt;
+  GATTN_CUDA(scr.get(&cnt, int64_t(N) + 1));
+  GATTN_CUDA(plan_alloc(p, &p->indptr_r, int64_t(N) + 1));
+  const int warp_grid = grid_1d((int64_t(N) + 1) * 32, p->num_sms);
+  k_res_count<<<warp_grid, kThreads, 0, st>>>(p->indptr, N, in_tile, cnt);
+  GATTN_CUDA(cudaGetLastError());
+  if ((r = exclusive_scan(cnt, p->indptr_r, int64_t(N) + 1, scr, st)) != GATTN_OK) return r;
+  int32_t mres = 0;
+  GATTN_CUDA(cudaMemcpyAsync(&mres, p->indptr_r + N, 4, cudaMemcpyDeviceToHost, st));
+  GATTN_CUDA(cudaStreamSynchronize(st));
+  p->M_res = mres;
+  GATTN_CUDA(plan_alloc(p, &p->indices_r, mres));
+  k_res_fill<<<warp_grid, kThreads, 0, st>>>(p->indptr, N, p->indices, in_tile, p->indptr_r,
+                                            p->indices_r);
+  GATTN_CUDA(cudaGetLastError());
+  // row blocks with tiles
+  int32_t n_trows = 0;
+  {
+    int32_t *head, *pos;
+    GATTN_CUDA(scr.get(&head, int64_t(n_tiles) + 1));
+    GATTN_CUDA(scr.get(&pos, int64_t(n_tiles) + 1));
+    k_trow_heads<<<grid_1d(int64_t(n_tiles) + 1, p->num_sms), kThreads, 0, st>>>(p->tile_rb,
+                                                                                n_tiles, head);
+    GATTN_CUDA(cudaGetLastError());
+    if ((r = exclusive_scan(head, pos, int64_t(n_tiles) + 1, scr, st)) != GATTN_OK) return r;
+    GATTN_CUDA(cudaMemcpyAsync(&n_trows, pos + n_tiles, 4, cudaMemcpyDeviceToHost, st));
+    GATTN_CUDA(cudaStreamSynchronize(st));
+    p->n_trows = n_trows;
+    GATTN_CUDA(plan_alloc(p, &p->trow_rb, n_trows));
+    GATTN_CUDA(plan_alloc(p, &p->trow_ptr, int64_t(n_trows) + 1));
+    k_trow_fill<<<grid_1d(int64_t(n_tiles) + 1, p->num_sms), kThreads, 0, st>>>(
+        p->tile_rb, head, pos, n_tiles, p->trow_rb, p->trow_ptr);
+    GATTN_CUDA(cudaGetLastError());
+  }
+  // forward split of the residual CSR
+  Side rs{};
+  if ((r = build_side(p, p->indptr_r, scr, st, &rs)) != GATTN_OK) return r;
+  p->items_r = rs.items;
+  p->sorted_r = rs.sorted;
+  p->parent_r = rs.parent;
+  p->kids_r = rs.kids;
+  p->n_light_r = rs.n_light;
+  p->n_chunks_r = rs.n_chunks;
+  p->n_inner_r = rs.n_inner;
+  GATTN_CUDA(plan_alloc(p, &p->cnt_fwd_r, rs.n_inner));
+  GATTN_CUDA(cudaMemsetAsync(p->cnt_fwd_r, 0, (rs.n_inner ? rs.n_inner : 1) * 4, st));
   return GATTN_OK;
 }
 
@@ -642,8 +851,6 @@ gattn_status plan_build(Plan* p, const int32_t* indptr, const int32_t* indices, 
   p->light = d.light_list;
   p->items = d.items;
   p->hfirst = d.hfirst;
-  p->units = d.units;
-  p->n_units = d.n_units;
   p->sorted = d.sorted;
   p->parent = d.parent;
   p->kids = d.kids;
@@ -656,8 +863,6 @@ gattn_status plan_build(Plan* p, const int32_t* indptr, const int32_t* indices, 
   p->light_src = s.light_list;
   p->items_src = s.items;
   p->hfirst_src = s.hfirst;
-  p->units_src = s.units;
-  p->n_units_src = s.n_units;
   p->sorted_src = s.sorted;
   p->parent_src = s.parent;
   p->kids_src = s.kids;
@@ -667,6 +872,8 @@ gattn_status plan_build(Plan* p, const int32_t* indptr, const int32_t* indices, 
   p->n_src_chunks = s.n_chunks;
   p->max_deg = mx[0];
   p->max_outdeg = mx[1];
+  // 7. dense tiles and the residual CSR
+  if (p->tile_min > 0 && (r = tile_build(p, scr, st)) != GATTN_OK) return r;
   return GATTN_OK;
 }
 

@@ -87,8 +87,9 @@ typedef struct {
   int32_t heavy_threshold; /* node is heavy when its degree > this (max 256); <= 0: chosen
                               from the graph size, a power of two in [32, 256] */
   int32_t chunk;           /* edges per heavy-node chunk (max 256); <= 0: the threshold */
-  int32_t tile_enable;     /* reserved for the dense-tile path; must be 0 */
-  float tile_density;      /* reserved */
+  int32_t tile_enable;     /* nonzero: also build the dense-tile split (needs N <= 2^23) */
+  float tile_density;      /* a 128 x 128 block of (destination, source) ids with at least
+                              ceil(tile_density * 16384) edges becomes a tile; <= 0: 1/16 */
 } gattn_plan_opts;
 
 /* Sizes of a built plan (host struct filled by gattn_plan_get_info). */
@@ -106,6 +107,10 @@ typedef struct {
   int32_t max_deg;
   int32_t max_outdeg;
   size_t device_bytes;  /* device memory held by the plan */
+  int64_t n_tiles;      /* dense tiles (0 unless tile_enable) */
+  int64_t n_tile_rows;  /* 128-node row blocks that have tiles */
+  int64_t tile_edges;   /* edges covered by the tiles' masks */
+  int32_t tile_min_edges; /* edges that made a block a tile */
 } gattn_plan_info;
 
 typedef struct gattn_plan gattn_plan;
@@ -151,6 +156,23 @@ GATTN_API gattn_status gattn_plan_export(const gattn_plan* plan, int32_t* deg, i
                                int32_t* hist_out, int32_t* light_src, int32_t* src_chunks);
 
 /*
+ * Copy the dense-tile split to HOST buffers (each nullable; synchronous).
+ * Nodes are cut into blocks of 128 ids; the block (rb, cb) holds the edges
+ * j -> i with i / 128 == rb, j / 128 == cb.  A block with at least
+ * tile_min_edges edges is a tile; tiles are listed in (rb, cb) order.
+ *   tile_rb[n_tiles], tile_cb[n_tiles]
+ *   masks[n_tiles * 512] : per tile 128 rows of 4 words; bit b of word w of
+ *                          row r is set when the pair (i = 128 rb + r,
+ *                          j = 128 cb + 32 w + b) occurs exactly once
+ *   indptr_r[N+1], indices_r[M - tile_edges] : the residual CSR, every edge
+ *                          not covered by a mask bit, in CSR order
+ * Returns GATTN_ERR_INVALID_ARG for a plan built without tile_enable.
+ */
+GATTN_API gattn_status gattn_plan_export_tiles(const gattn_plan* plan, int32_t* tile_rb,
+                                               int32_t* tile_cb, uint32_t* masks,
+                                               int32_t* indptr_r, int32_t* indices_r);
+
+/*
  * Synchronise the device and report whether any kernel run with this plan
  * since the last check gave up a bounded wait for its asynchronous copies
  * (every wait in the kernels has an iteration limit; on expiry the kernel
@@ -179,6 +201,11 @@ GATTN_API gattn_status gattn_workspace_size(const gattn_plan* plan, int32_t H, i
  *   workspace : device, >= gattn_workspace_size bytes, 16-byte aligned;
  *               its contents need no initialisation.
  * Calls that share a plan or a workspace must not overlap on the device.
+ * With a plan built with tile_enable, the DOT score, bf16 and D = 64 or
+ * 128, the forward runs in two launches ("Methodology", attention-based
+ * layers, tensor-core optimisation): the CSR pass over the residual edges,
+ * then the tiles on the tensor cores, merged per node; otherwise the CSR
+ * pass covers every edge.  Both give the same softmax attention.
  */
 GATTN_API gattn_status gattn_fwd(const gattn_plan* plan, int32_t H, int32_t D, gattn_dtype dtype,
                        const void* Q, const void* K, const void* V, const gattn_score* score,
