@@ -40,6 +40,7 @@ KERNEL_SOURCES = ("attn_fwd.cuh", "attn_bwd.cuh", "attn_pipe.cuh", "tma.cuh", "g
                   "attn_launch.cuh")
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
+CPU_SAMPLE_EDGES = 2_000_000
 
 
 # ----------------------------------------------------------------------------
@@ -188,10 +189,19 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+GRAPH_TEXT = {
+    "powerlaw170k": "power-law graph (1.2M Zipf(2.1) in-edges capped at 13000 + N self-loops)",
+    "er1k": "directed Erdos-Renyi graph (avg in-degree 8 + self-loops)",
+    "lognormal233k": "lognormal in-degrees (mu 5.5, sigma 1.2)",
+    "gatv2_powerlaw2m4": "power-law graph (62M Zipf(2.3) in-edges)",
+    "sbm1m": "stochastic block model (64-node communities, p_in 0.5, 4N inter edges)",
+}
+
+
 def workload_config(w, N, M, extra=None):
     cfg = {
-        "workload": (f"{w.name}: power-law graph N={N}, M={M} (1.2M Zipf(2.1) in-edges capped "
-                     f"at 13000 + {N} self-loops), dot score, H={w.H}, D={w.D}, bf16 I/O"),
+        "workload": (f"{w.name}: {GRAPH_TEXT.get(w.name, w.graph)} N={N}, M={M}, "
+                     f"{w.score} score, H={w.H}, D={w.D}, {w.dtype} I/O"),
         "N": N, "M": M, "H": w.H, "D": w.D, "io_dtype": w.dtype, "score": w.score,
         "seed": 0,
     }
@@ -199,21 +209,39 @@ def workload_config(w, N, M, extra=None):
     return cfg
 
 
-def oracle_sample_step(indptr, indices, f64, rows):
+def oracle_sample_step(indptr, indices, f64, rows, w):
     """One oracle fwd+bwd over a row subset; returns (edges, seconds)."""
     import oracle
+    kind = oracle.GATV2 if w.score == "gatv2" else oracle.DOT
+    a = f64.get("a")
     rp, col, rid = oracle.rows_subgraph(indptr, indices, rows)
     t0 = time.perf_counter()
-    oracle.forward(rp, col, f64["Q"], f64["K"], f64["V"], rows=rid)
-    oracle.backward(rp, col, f64["Q"], f64["K"], f64["V"], f64["dO"][rows], rows=rid)
+    oracle.forward(rp, col, f64["Q"], f64["K"], f64["V"], kind=kind, a=a, rows=rid)
+    oracle.backward(rp, col, f64["Q"], f64["K"], f64["V"], f64["dO"][rows], kind=kind, a=a,
+                    rows=rid)
     return int(rp[-1]), time.perf_counter() - t0
 
 
-def decoded_inputs(f):
-    """The bf16 inputs decoded exactly to fp64 (what the GPU path computes on)."""
+def sample_rows(indptr, edges, rng):
+    """A block of consecutive destination rows holding about ``edges`` edges."""
+    import numpy as np
+    N, M = len(indptr) - 1, int(indptr[-1])
+    if M <= edges:
+        return np.arange(N)
+    e0 = int(rng.integers(0, M - edges))
+    r0 = int(np.searchsorted(indptr, e0, side="right")) - 1
+    r1 = int(np.searchsorted(indptr, int(indptr[r0]) + edges, side="left"))
+    return np.arange(r0, max(r1, r0 + 1))
+
+
+def decoded_inputs(f, w):
+    """The inputs decoded exactly to fp64 (what the GPU path computes on)."""
     import torch
-    return {k: torch.from_numpy(f[k]).to(torch.bfloat16).double().numpy()
-            for k in ("Q", "K", "V", "dO")}
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    out = {k: torch.from_numpy(f[k]).to(tdt).double().numpy() for k in ("Q", "K", "V", "dO")}
+    if "a" in f:
+        out["a"] = f["a"].astype("float64")
+    return out
 
 
 # ----------------------------------------------------------------------------
@@ -230,17 +258,19 @@ def run_cuda(args):
     dist = init_group(world)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = synth.WORKLOADS[WORKLOAD]
+    w = synth.WORKLOADS[args.workload]
     indptr, indices = synth.make_graph(w, seed=0)
     f = synth.make_features(w, seed=0)
     N, M = len(indptr) - 1, int(indptr[-1])
-    H, D, s = w.H, w.D, 2
-    tdt = torch.bfloat16
+    H, D = w.H, w.D
+    s = 2 if w.dtype == "bf16" else 4
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     Q, K, V, G = (torch.from_numpy(f[k]).to(dev, tdt) for k in ("Q", "K", "V", "dO"))
     plan = gb.gattn_plan_create(torch.from_numpy(indptr).to(dev),
-                                torch.from_numpy(indices).to(dev))
+                                torch.from_numpy(indices).to(dev), tile_enable=args.tile)
     info = plan.info()
-    score = gb.Score("dot")
+    a = torch.from_numpy(f["a"]).to(dev) if w.score == "gatv2" else None
+    score = gb.Score(w.score, a=a)
     out = torch.empty_like(Q)
     lse = torch.empty((N, H), dtype=torch.float32, device=dev)
     dQ, dK, dV = (torch.empty_like(Q) for _ in range(3))
@@ -331,16 +361,19 @@ def run_cuda(args):
     # oracle timed on the host cores on a bounded sample (rank 0, N = 1 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        f64 = decoded_inputs(f)
-        rows = np.arange(N)
+        f64 = decoded_inputs(f, w)
+        rng = np.random.default_rng(1)
         edges, sec, passes = 0, 0.0, 0
-        while sec < 10.0 and passes < 20:       # whole-graph passes, ~10 s of CPU work
-            e, t = oracle_sample_step(indptr, indices, f64, rows)
+        while sec < 10.0 and passes < 20:       # ~10 s of CPU work
+            rows = sample_rows(indptr, CPU_SAMPLE_EDGES, rng)
+            e, t = oracle_sample_step(indptr, indices, f64, rows, w)
             edges, sec, passes = edges + e, sec + t, passes + 1
+        what = (f"the whole {w.name} graph" if M <= CPU_SAMPLE_EDGES else
+                f"blocks of consecutive destination rows of {w.name} (~{CPU_SAMPLE_EDGES} "
+                "edges each, random offsets)")
         cpu = {"value": edges / sec, "unit": "edges/s", "cores": 1, "kind": "oracle",
-               "sample": f"{passes} fp64 oracle fwd+bwd passes over the whole {WORKLOAD} "
-                         f"graph ({edges} edges, {sec:.1f} s, serial C, bf16 inputs decoded "
-                         "exactly)"}
+               "sample": f"{passes} fp64 oracle fwd+bwd passes over {what} ({edges} edges, "
+                         f"{sec:.1f} s, serial C, inputs decoded exactly)"}
 
     res = {
         "metric": METRIC, "value": value, "unit": "edges/s", "n_gpus": world,
@@ -356,7 +389,7 @@ def run_cuda(args):
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
                      "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
-                     "traffic": dram_traffic(dom, WORKLOAD)},
+                     "traffic": dram_traffic(dom, w.name)},
         "step_gbs": round(step_bytes / (statistics.mean(step_ms) / 1e3) / 1e9, 1),
         "kernels": kernels,
         "e2e": {"value": e2e_value, "unit": "edges/s",
@@ -383,23 +416,23 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    w = synth.WORKLOADS[WORKLOAD]
+    w = synth.WORKLOADS[args.workload]
     indptr, indices = synth.make_graph(w, seed=0)
     f = synth.make_features(w, seed=0)
     N, M = len(indptr) - 1, int(indptr[-1])
-    f64 = decoded_inputs(f)
-    n_rows = N // 16
+    f64 = decoded_inputs(f, w)
     edges_tot, sec_tot = 0, 0.0
     r = np.random.default_rng(1)
+    step_edges = min(M // 16, CPU_SAMPLE_EDGES)
     for k in range(args.warmup + args.steps):
-        start = int(r.integers(0, N - n_rows))
-        e, sec = oracle_sample_step(indptr, indices, f64, np.arange(start, start + n_rows))
+        rows = sample_rows(indptr, step_edges, r)
+        e, sec = oracle_sample_step(indptr, indices, f64, rows, w)
         if k >= args.warmup:
             edges_tot += e
             sec_tot += sec
     value = edges_tot / sec_tot
-    sample = (f"per step: one fp64 oracle fwd+bwd over {n_rows} consecutive destination rows "
-              f"of {WORKLOAD} at a random offset ({edges_tot // max(args.steps, 1)} edges "
+    sample = (f"per step: one fp64 oracle fwd+bwd over a block of consecutive destination rows "
+              f"of {w.name} at a random offset ({edges_tot // max(args.steps, 1)} edges "
               "on average), serial C")
     res = {
         "metric": METRIC, "value": value, "unit": "edges/s", "n_gpus": world,
@@ -422,6 +455,10 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("cuda", "reference"), default="cuda")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="synthetic workload (default: the power-law graph the metric is quoted on)")
+    ap.add_argument("--tile", action="store_true",
+                    help="build the plan with the dense-tile split (tensor-core forward)")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the oracle timing (profiling runs)")
     args = ap.parse_args(argv)

@@ -36,7 +36,7 @@
 
 namespace gattn {
 
-constexpr int kStages = 3;           // row stages in flight + 1
+constexpr int kStages = 2;           // row stages in flight + 1
 constexpr int kRing = 2 * kStages;   // descriptor / index ring entries
 constexpr int kUnit = 32;            // items per block of bundles
 constexpr int kFirst = 1 << 29;
@@ -53,8 +53,8 @@ struct Lay {
   static constexpr int TPR = RB / PT;               // threads per row
   static constexpr int G = 32 / TPR;                // groups (items) per warp
   static constexpr int NCH = RB / 16;               // chunks per row
-  // edges per item per stage: ~4 KB of gathered rows per stage
-  static constexpr int SE0 = 4096 / (2 * RB) / G;
+  // edges per item per stage: ~8 KB of gathered rows per stage
+  static constexpr int SE0 = 8192 / (2 * RB) / G;
   static constexpr int SE1 = SE0 < 1 ? 1 : SE0;
   static constexpr int SE2 = SE1 * G > 32 ? 32 / G : SE1;  // at most 32 edges per stage
   static constexpr int SE = SE2 * G < 4 ? 4 / G : SE2;     // whole 4-row gathers

@@ -24,9 +24,9 @@
 // After the head's last tile each thread merges its row with the residual
 // CSR pass (which ran first and wrote out / lse over the edges outside the
 // tiles): lse = log(e^lse_t + e^lse_r), out = the two halves weighted by
-// their share of the softmax mass.  The normaliser sums the bf16-rounded
-// weights that the MMA multiplies, so each row stays an exact convex
-// combination of its values.
+// their share of the softmax mass.  The MMA multiplies the weights rounded
+// to bf16 while the normaliser (and so lse, which the backward reuses) sums
+// them in fp32, as in FlashAttention.
 //
 // Every mbarrier wait is bounded; a wait that gives up is reported through
 // the plan's error word, the block drains what it issued (again bounded),
@@ -278,7 +278,7 @@ __global__ void __launch_bounds__(kThreadsTile) tile_fwd_kernel(const __grid_con
             const float p0 = ((mw[j / 32] >> (j % 32)) & 1u) ? ex2(s[j] - base) : 0.f;
             const float p1 = ((mw[(j + 1) / 32] >> ((j + 1) % 32)) & 1u) ? ex2(s[j + 1] - base) : 0.f;
             w[q] = bf16x2_bits(p0, p1);
-            sum += __uint_as_float(w[q] << 16) + __uint_as_float(w[q] & 0xffff0000u);
+            sum += p0 + p1;
           }
           // K-major 128-byte swizzle: 16-byte chunk ch of row r sits at chunk ch ^ (r % 8)
           uint8_t* dst = sP + kb * kTileBytes + tid * 128 + ((ch ^ (tid & 7)) * 16);

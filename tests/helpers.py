@@ -59,7 +59,8 @@ def graph_with_source_hub(seed, N, avg, hub_src=1, frac=0.7, **kw):
 class GpuCase:
     """Inputs on the GPU (in the I/O dtype) and their exact fp64 decodes."""
 
-    def __init__(self, indptr, indices, H, D, dtype, kind, seed=0, T=0, C=0, feats=None):
+    def __init__(self, indptr, indices, H, D, dtype, kind, seed=0, T=0, C=0, feats=None,
+                 tile=False, density=0.0):
         import torch
         from gnn_sparse_attention_gb300 import binding as gb
         self.indptr, self.indices = indptr, indices
@@ -75,7 +76,8 @@ class GpuCase:
         self.a = torch.from_numpy(f["a"]).to(dev) if kind == "gatv2" else None
         self.score = gb.Score(kind, a=self.a)
         self.plan = gb.gattn_plan_create(torch.from_numpy(indptr).to(dev),
-                                         torch.from_numpy(indices).to(dev), T, C)
+                                         torch.from_numpy(indices).to(dev), T, C,
+                                         tile_enable=tile, tile_density=density)
         self.okind = oracle.DOT if kind == "dot" else oracle.GATV2
 
     def host64(self, name, rows=None):
