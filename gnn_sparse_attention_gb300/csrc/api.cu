@@ -125,34 +125,35 @@ gattn_status launched(const char* what) {
 
 }  // namespace
 
-#define GATTN_ROW_CASE(PASS_NAME, PT, TNAME, RB_) \
-  case RB_:                                      \
-    return launch_##PASS_NAME##_##TNAME##_##RB_(db, kind, p, num_sms, st, g);
+// switch key of a (row bytes, stage bytes) pair
+#define GATTN_ROW_CASE(PASS_NAME, PT, TNAME, RB_, SB_) \
+  case RB_ * 16 + SB_ / 4096:                          \
+    return launch_##PASS_NAME##_##TNAME##_##RB_##_##SB_(db, kind, p, num_sms, st, g);
 
-gattn_status launch_fwd(gattn_dtype dt, int rb, int db, int kind, const FwdParams& p, int num_sms,
-                        cudaStream_t st, int* g) {
+gattn_status launch_fwd(gattn_dtype dt, int rb, int db, int kind, int sb, const FwdParams& p,
+                        int num_sms, cudaStream_t st, int* g) {
   if (dt == GATTN_F32) {
-    switch (rb) { GATTN_FOR_ROWS(GATTN_ROW_CASE, fwd, FwdParams, f32) }
+    switch (rb * 16 + sb / 4096) { GATTN_FOR_ROWS(GATTN_ROW_CASE, fwd, FwdParams, f32) }
   } else {
-    switch (rb) { GATTN_FOR_ROWS(GATTN_ROW_CASE, fwd, FwdParams, bf16) }
+    switch (rb * 16 + sb / 4096) { GATTN_FOR_ROWS(GATTN_ROW_CASE, fwd, FwdParams, bf16) }
   }
   return GATTN_ERR_UNSUPPORTED;
 }
-gattn_status launch_bwd_csr(gattn_dtype dt, int rb, int db, int kind, const BwdParams& p,
+gattn_status launch_bwd_csr(gattn_dtype dt, int rb, int db, int kind, int sb, const BwdParams& p,
                             int num_sms, cudaStream_t st, int* g) {
   if (dt == GATTN_F32) {
-    switch (rb) { GATTN_FOR_ROWS(GATTN_ROW_CASE, csr, BwdParams, f32) }
+    switch (rb * 16 + sb / 4096) { GATTN_FOR_ROWS(GATTN_ROW_CASE, csr, BwdParams, f32) }
   } else {
-    switch (rb) { GATTN_FOR_ROWS(GATTN_ROW_CASE, csr, BwdParams, bf16) }
+    switch (rb * 16 + sb / 4096) { GATTN_FOR_ROWS(GATTN_ROW_CASE, csr, BwdParams, bf16) }
   }
   return GATTN_ERR_UNSUPPORTED;
 }
-gattn_status launch_bwd_csc(gattn_dtype dt, int rb, int db, int kind, const BwdParams& p,
+gattn_status launch_bwd_csc(gattn_dtype dt, int rb, int db, int kind, int sb, const BwdParams& p,
                             int num_sms, cudaStream_t st, int* g) {
   if (dt == GATTN_F32) {
-    switch (rb) { GATTN_FOR_ROWS(GATTN_ROW_CASE, csc, BwdParams, f32) }
+    switch (rb * 16 + sb / 4096) { GATTN_FOR_ROWS(GATTN_ROW_CASE, csc, BwdParams, f32) }
   } else {
-    switch (rb) { GATTN_FOR_ROWS(GATTN_ROW_CASE, csc, BwdParams, bf16) }
+    switch (rb * 16 + sb / 4096) { GATTN_FOR_ROWS(GATTN_ROW_CASE, csc, BwdParams, bf16) }
   }
   return GATTN_ERR_UNSUPPORTED;
 }
@@ -419,7 +420,9 @@ gattn_status gattn_fwd(const gattn_plan* plan, int32_t H, int32_t D, gattn_dtype
                  : Tree{p.parent, p.kids, p.n_chunks, p.cnt_fwd};
   f.err = p.err;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if ((s = launch_fwd(dtype, rb, D * (int)dtype_size(dtype), score->kind, f, p.num_sms, st,
+  const int sb = tiles ? stage_bytes(p.M_res, p.n_chunks_r + p.n_light_r)
+                       : stage_bytes(p.M, p.n_chunks + p.n_light);
+  if ((s = launch_fwd(dtype, rb, D * (int)dtype_size(dtype), score->kind, sb, f, p.num_sms, st,
                       nullptr)) != GATTN_OK)
     return s;
   if ((s = launched("forward")) != GATTN_OK || !tiles) return s;
@@ -524,7 +527,8 @@ gattn_status gattn_bwd_dq(const gattn_plan* plan, int32_t H, int32_t D, gattn_dt
   b.da = gat ? da : nullptr;
   b.part = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.dq_part);
   b.tree = Tree{p.parent, p.kids, p.n_chunks, p.cnt_dq};
-  if ((s = launch_bwd_csr(dtype, rb, D * (int)dtype_size(dtype), score->kind, b, p.num_sms,
+  if ((s = launch_bwd_csr(dtype, rb, D * (int)dtype_size(dtype), score->kind,
+                          stage_bytes(p.M, p.n_chunks + p.n_light), b, p.num_sms,
                           st, nullptr)) != GATTN_OK)
     return s;
   return launched("backward (CSR pass)");
@@ -566,7 +570,8 @@ gattn_status gattn_bwd_dkdv(const gattn_plan* plan, int32_t H, int32_t D, gattn_
   b.da = nullptr;
   b.part = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.dkv_part);
   b.tree = Tree{p.parent_src, p.kids_src, p.n_src_chunks, p.cnt_dkv};
-  if ((s = launch_bwd_csc(dtype, rb, D * (int)dtype_size(dtype), score->kind, b, p.num_sms,
+  if ((s = launch_bwd_csc(dtype, rb, D * (int)dtype_size(dtype), score->kind,
+                          stage_bytes(p.M, p.n_src_chunks + p.n_light_src), b, p.num_sms,
                           reinterpret_cast<cudaStream_t>(stream), nullptr)) != GATTN_OK)
     return s;
   return launched("backward (CSC pass)");

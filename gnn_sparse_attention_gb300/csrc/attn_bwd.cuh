@@ -68,9 +68,9 @@ struct StatBytes {
   static constexpr int value = RB / 4 < 16 ? 16 : RB / 4;
 };
 
-template <typename T, int RB>
+template <typename T, int RB, int SB>
 struct CsrShape {
-  using L = Lay<T, RB>;
+  using L = Lay<T, RB, SB>;
   static constexpr int LS = StatBytes<RB>::value;
   // per item slot: Q, dO, O rows and the lse row; per edge: K row, V row
   static constexpr int OL = 3 * L::QR * RB;             // lse sets
@@ -83,9 +83,9 @@ struct CsrShape {
   static constexpr int SMEM = WARPS * WARP_BYTES;
 };
 
-template <typename T, int RB>
+template <typename T, int RB, int SB>
 struct CscShape {
-  using L = Lay<T, RB>;
+  using L = Lay<T, RB, SB>;
   static constexpr int LS = StatBytes<RB>::value;
   // per item slot: K, V rows; per edge: Q row, dO row, lse row, Delta row
   static constexpr int OQE = 2 * L::QR * RB;            // Q rows of the edges
@@ -120,10 +120,10 @@ __device__ __forceinline__ void copy_stat_rows(uint8_t* dst, const float* src, i
 // ---------------------------------------------------------------------------
 // pass 1: CSR
 // ---------------------------------------------------------------------------
-template <typename T, int RB, int DB, int KIND>
-__global__ void __launch_bounds__(CsrShape<T, RB>::THREADS) bwd_csr_kernel(const __grid_constant__ BwdParams p) {
-  using L = Lay<T, RB>;
-  using Sh = CsrShape<T, RB>;
+template <typename T, int RB, int DB, int KIND, int SB>
+__global__ void __launch_bounds__(CsrShape<T, RB, SB>::THREADS) bwd_csr_kernel(const __grid_constant__ BwdParams p) {
+  using L = Lay<T, RB, SB>;
+  using Sh = CsrShape<T, RB, SB>;
   using PR = Pairs<T>;
   constexpr int NC = L::NC, TPR = L::TPR, G = L::G, SE = L::SE, B = L::B;
   constexpr int PP = PR::P, S = kStages;
@@ -454,10 +454,10 @@ __global__ void __launch_bounds__(CsrShape<T, RB>::THREADS) bwd_csr_kernel(const
 // ---------------------------------------------------------------------------
 // pass 2: CSC
 // ---------------------------------------------------------------------------
-template <typename T, int RB, int DB, int KIND>
-__global__ void __launch_bounds__(CscShape<T, RB>::THREADS) bwd_csc_kernel(const __grid_constant__ BwdParams p) {
-  using L = Lay<T, RB>;
-  using Sh = CscShape<T, RB>;
+template <typename T, int RB, int DB, int KIND, int SB>
+__global__ void __launch_bounds__(CscShape<T, RB, SB>::THREADS) bwd_csc_kernel(const __grid_constant__ BwdParams p) {
+  using L = Lay<T, RB, SB>;
+  using Sh = CscShape<T, RB, SB>;
   using PR = Pairs<T>;
   constexpr int NC = L::NC, TPR = L::TPR, G = L::G, SE = L::SE, B = L::B;
   constexpr int PP = PR::P, S = kStages;

@@ -48,9 +48,9 @@ struct FwdParams {
   int32_t* err;        // set when a wait gives up
 };
 
-template <typename T, int RB>
+template <typename T, int RB, int SB>
 struct FwdShape {
-  using L = Lay<T, RB>;
+  using L = Lay<T, RB, SB>;
   // Q rows of the G items (QR slots), then B K rows and B V rows
   static constexpr int STAGE = RB * (L::QR + 2 * L::B);
   static constexpr int WARP_BYTES = align128(kStages * STAGE + L::META);
@@ -59,10 +59,10 @@ struct FwdShape {
   static constexpr int SMEM = WARPS * WARP_BYTES;
 };
 
-template <typename T, int RB, int DB, int KIND>
-__global__ void __launch_bounds__(FwdShape<T, RB>::THREADS) fwd_kernel(const __grid_constant__ FwdParams p) {
-  using L = Lay<T, RB>;
-  using Sh = FwdShape<T, RB>;
+template <typename T, int RB, int DB, int KIND, int SB>
+__global__ void __launch_bounds__(FwdShape<T, RB, SB>::THREADS) fwd_kernel(const __grid_constant__ FwdParams p) {
+  using L = Lay<T, RB, SB>;
+  using Sh = FwdShape<T, RB, SB>;
   using PR = Pairs<T>;
   constexpr int NC = L::NC, TPR = L::TPR, G = L::G, SE = L::SE, B = L::B;
   constexpr int PP = PR::P, S = kStages;

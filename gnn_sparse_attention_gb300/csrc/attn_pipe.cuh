@@ -44,7 +44,9 @@ constexpr int kLast = 1 << 30;
 constexpr int kCntMask = 0xffff;
 constexpr int kSmemPerSm = 227 * 1024;
 
-template <typename T, int RB>
+// SB: target bytes of gathered rows per stage (4 KB or 8 KB; the launcher
+// picks by the plan's mean item length).
+template <typename T, int RB, int SB>
 struct Lay {
   static constexpr int VEC = 16 / (int)sizeof(T);  // elements per 16-byte chunk
   static constexpr int PT = RB <= 1024 ? 32 : RB / 32;
@@ -53,8 +55,8 @@ struct Lay {
   static constexpr int TPR = RB / PT;               // threads per row
   static constexpr int G = 32 / TPR;                // groups (items) per warp
   static constexpr int NCH = RB / 16;               // chunks per row
-  // edges per item per stage: ~8 KB of gathered rows per stage
-  static constexpr int SE0 = 8192 / (2 * RB) / G;
+  // edges per item per stage: ~SB bytes of gathered rows per stage
+  static constexpr int SE0 = SB / (2 * RB) / G;
   static constexpr int SE1 = SE0 < 1 ? 1 : SE0;
   static constexpr int SE2 = SE1 * G > 32 ? 32 / G : SE1;  // at most 32 edges per stage
   static constexpr int SE = SE2 * G < 4 ? 4 / G : SE2;     // whole 4-row gathers

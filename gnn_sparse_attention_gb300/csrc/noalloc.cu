@@ -143,7 +143,8 @@ extern "C" gattn_status gattn_fwd_noalloc(const gattn_plan* plan, int32_t H, int
   f.tree = Tree{p.parent, p.kids, p.n_chunks, p.cnt_fwd};
   f.err = p.err;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if ((s = launch_fwd(dtype, int(rb), int(db), score->kind, f, p.num_sms, st, nullptr)) !=
+  if ((s = launch_fwd(dtype, int(rb), int(db), score->kind, stage_bytes(p.M, f.n_items), f,
+                      p.num_sms, st, nullptr)) !=
       GATTN_OK)
     return s;
   const cudaError_t e = cudaGetLastError();
