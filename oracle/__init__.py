@@ -68,6 +68,10 @@ def _load():
             lib.oracle_plan.restype = ctypes.c_int
             lib.oracle_tile_plan.argtypes = [i32, i64, P, P, i64, i64, P, P, P, P, P, P]
             lib.oracle_tile_plan.restype = ctypes.c_int
+            lib.oracle_reorder.argtypes = [i32, i64, P, P, ctypes.c_int, P]
+            lib.oracle_reorder.restype = ctypes.c_int
+            lib.oracle_permute_csr.argtypes = [i32, i64, P, P, P, P, P]
+            lib.oracle_permute_csr.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -174,6 +178,39 @@ def plan(indptr, indices, heavy_threshold, chunk):
         "outdeg": outdeg, "hist_out": hist_out, "light_src": light_src[:nls],
         "src_chunks": src_chunks[:ncs],
     }
+
+
+REORDER_DEGREE = 0
+REORDER_RCM = 1
+
+
+def reorder(indptr, indices, method):
+    """Oracle relabelling: perm[new] = old (degree order or reverse Cuthill-McKee)."""
+    lib = _load()
+    indptr = np.ascontiguousarray(indptr, dtype=np.int32)
+    indices = np.ascontiguousarray(indices, dtype=np.int32)
+    N = len(indptr) - 1
+    perm = np.zeros(max(N, 1), np.int32)
+    rc = lib.oracle_reorder(N, int(indptr[-1]), _p(indptr), _p(indices), int(method), _p(perm))
+    if rc != 0:
+        raise RuntimeError(f"oracle_reorder failed ({rc})")
+    return perm[:N]
+
+
+def permute_csr(indptr, indices, perm):
+    """Oracle relabelled graph: row i = old row perm[i], sources renamed and sorted."""
+    lib = _load()
+    indptr = np.ascontiguousarray(indptr, dtype=np.int32)
+    indices = np.ascontiguousarray(indices, dtype=np.int32)
+    perm = np.ascontiguousarray(perm, dtype=np.int32)
+    N = len(indptr) - 1
+    M = int(indptr[-1])
+    ptr = np.zeros(N + 1, np.int32)
+    idx = np.zeros(max(M, 1), np.int32)
+    rc = lib.oracle_permute_csr(N, M, _p(indptr), _p(indices), _p(perm), _p(ptr), _p(idx))
+    if rc != 0:
+        raise RuntimeError(f"oracle_permute_csr failed ({rc})")
+    return ptr, idx[:M]
 
 
 TILE = 128  # nodes per tile side

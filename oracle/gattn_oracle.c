@@ -392,3 +392,138 @@ int oracle_tile_plan(int32_t N, int64_t M, const int32_t* indptr, const int32_t*
   free(ek); free(row); free(in_tile); free(pair_count);
   return 0;
 }
+
+/*
+ * Node relabelling for gather locality ("On Efficient Scaling of GNNs via
+ * IO-Aware Layers Implementations", zh/ko technical summaries,
+ * "Methodology" and results: graph reordering, which the pages find helps
+ * neighbour-parallel (gather-dominated) kernels on high-degree graphs).  The
+ * pages name no method; two textbook ones are provided.  perm[new] = old.
+ *   method 0, degree : nodes by decreasing total degree (in + out, every
+ *                      edge counted), ties by increasing id.
+ *   method 1, RCM    : reverse Cuthill-McKee on the undirected simple graph
+ *                      (j -> i and i -> j merged, self-loops and repeats
+ *                      dropped).  While nodes are unvisited, the unvisited
+ *                      node of least degree (smallest id on ties) starts a
+ *                      breadth-first search that appends each dequeued
+ *                      node's unvisited neighbours in increasing (degree, id)
+ *                      order; the final order is reversed.
+ * Returns 0, -1 for an unknown method, -2 on allocation failure.
+ */
+typedef struct { int64_t key; int32_t id; } orc_node_key;
+
+static int orc_cmp_node(const void* a, const void* b) {
+  const orc_node_key* x = (const orc_node_key*)a;
+  const orc_node_key* y = (const orc_node_key*)b;
+  if (x->key != y->key) return x->key < y->key ? -1 : 1;
+  return x->id < y->id ? -1 : (x->id > y->id ? 1 : 0);
+}
+
+static int orc_cmp_i32(const void* a, const void* b) {
+  const int32_t x = *(const int32_t*)a, y = *(const int32_t*)b;
+  return x < y ? -1 : (x > y ? 1 : 0);
+}
+
+int oracle_reorder(int32_t N, int64_t M, const int32_t* indptr, const int32_t* indices,
+                   int method, int32_t* perm) {
+  if (method != 0 && method != 1) return -1;
+  orc_node_key* nk = (orc_node_key*)malloc(((size_t)N + 1) * sizeof(orc_node_key));
+  if (!nk) return -2;
+  if (method == 0) {
+    int64_t* deg = (int64_t*)calloc((size_t)N + 1, sizeof(int64_t));
+    if (!deg) { free(nk); return -2; }
+    for (int32_t i = 0; i < N; ++i) {
+      deg[i] += indptr[i + 1] - indptr[i];
+      for (int64_t e = indptr[i]; e < indptr[i + 1]; ++e) deg[indices[e]] += 1;
+    }
+    for (int32_t i = 0; i < N; ++i) { nk[i].key = -deg[i]; nk[i].id = i; }
+    qsort(nk, (size_t)N, sizeof(orc_node_key), orc_cmp_node);
+    for (int32_t i = 0; i < N; ++i) perm[i] = nk[i].id;
+    free(deg);
+    free(nk);
+    return 0;
+  }
+  /* undirected simple adjacency: both directions, then sort + unique per node */
+  int64_t* cnt = (int64_t*)calloc((size_t)N + 1, sizeof(int64_t));
+  int64_t* start = (int64_t*)malloc(((size_t)N + 1) * sizeof(int64_t));
+  int32_t* adj = (int32_t*)malloc((size_t)(2 * M > 0 ? 2 * M : 1) * sizeof(int32_t));
+  int64_t* fill = (int64_t*)malloc(((size_t)N + 1) * sizeof(int64_t));
+  int64_t* deg = (int64_t*)malloc(((size_t)N + 1) * sizeof(int64_t));
+  unsigned char* seen = (unsigned char*)calloc((size_t)N + 1, 1);
+  int32_t* order = (int32_t*)malloc(((size_t)N + 1) * sizeof(int32_t));
+  orc_node_key* nb = (orc_node_key*)malloc(((size_t)N + 1) * sizeof(orc_node_key));
+  if (!cnt || !start || !adj || !fill || !deg || !seen || !order || !nb) {
+    free(nk); free(cnt); free(start); free(adj); free(fill); free(deg); free(seen); free(order);
+    free(nb);
+    return -2;
+  }
+  for (int32_t i = 0; i < N; ++i)
+    for (int64_t e = indptr[i]; e < indptr[i + 1]; ++e)
+      if (indices[e] != i) { cnt[i] += 1; cnt[indices[e]] += 1; }
+  start[0] = 0;
+  for (int32_t i = 0; i < N; ++i) { start[i + 1] = start[i] + cnt[i]; fill[i] = start[i]; }
+  for (int32_t i = 0; i < N; ++i)
+    for (int64_t e = indptr[i]; e < indptr[i + 1]; ++e) {
+      const int32_t j = indices[e];
+      if (j == i) continue;
+      adj[fill[i]++] = j;
+      adj[fill[j]++] = i;
+    }
+  for (int32_t i = 0; i < N; ++i) {
+    int32_t* a = adj + start[i];
+    const int64_t n = start[i + 1] - start[i];
+    qsort(a, (size_t)n, sizeof(int32_t), orc_cmp_i32);
+    int64_t u = 0;
+    for (int64_t k = 0; k < n; ++k)
+      if (k == 0 || a[k] != a[k - 1]) a[u++] = a[k];
+    deg[i] = u;
+  }
+  /* roots in (degree, id) order */
+  for (int32_t i = 0; i < N; ++i) { nk[i].key = deg[i]; nk[i].id = i; }
+  qsort(nk, (size_t)N, sizeof(orc_node_key), orc_cmp_node);
+  int64_t head = 0, tail = 0, next_root = 0;
+  while (tail < N) {
+    while (seen[nk[next_root].id]) ++next_root;
+    const int32_t r = nk[next_root].id;
+    seen[r] = 1;
+    order[tail++] = r;
+    while (head < tail) {
+      const int32_t v = order[head++];
+      int64_t m = 0;
+      for (int64_t k = 0; k < deg[v]; ++k) {
+        const int32_t w = adj[start[v] + k];
+        if (!seen[w]) { nb[m].key = deg[w]; nb[m].id = w; ++m; }
+      }
+      qsort(nb, (size_t)m, sizeof(orc_node_key), orc_cmp_node);
+      for (int64_t k = 0; k < m; ++k) { seen[nb[k].id] = 1; order[tail++] = nb[k].id; }
+    }
+  }
+  for (int32_t i = 0; i < N; ++i) perm[i] = order[N - 1 - i];
+  free(nk); free(cnt); free(start); free(adj); free(fill); free(deg); free(seen); free(order);
+  free(nb);
+  return 0;
+}
+
+/*
+ * The graph under a relabelling perm (perm[new] = old): row i of the result
+ * is old row perm[i], its sources mapped to their new ids and sorted
+ * ascending (repeated sources kept).
+ */
+int oracle_permute_csr(int32_t N, int64_t M, const int32_t* indptr, const int32_t* indices,
+                       const int32_t* perm, int32_t* indptr_out, int32_t* indices_out) {
+  int32_t* inv = (int32_t*)malloc(((size_t)N + 1) * sizeof(int32_t));
+  if (!inv) return -2;
+  for (int32_t i = 0; i < N; ++i) inv[perm[i]] = i;
+  int64_t o = 0;
+  indptr_out[0] = 0;
+  for (int32_t i = 0; i < N; ++i) {
+    const int32_t old = perm[i];
+    const int64_t r0 = o;
+    for (int64_t e = indptr[old]; e < indptr[old + 1]; ++e) indices_out[o++] = inv[indices[e]];
+    qsort(indices_out + r0, (size_t)(o - r0), sizeof(int32_t), orc_cmp_i32);
+    indptr_out[i + 1] = (int32_t)o;
+  }
+  (void)M;
+  free(inv);
+  return 0;
+}

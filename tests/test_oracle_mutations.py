@@ -8,6 +8,7 @@ import pytest
 
 import oracle
 from tests import test_oracle_pins as pins
+from tests import test_oracle_reorder_pins as reorder_pins
 from tests import test_oracle_tile_pins as tile_pins
 
 MUTANTS = {
@@ -30,6 +31,14 @@ MUTANTS = {
                               "if (pair_count[r * 128 + c] >= 1) {"),
     "tile_mask_column_order": ("mk[r * 4 + c / 32] |= 1u << (c % 32);",
                                "mk[r * 4 + c % 4] |= 1u << (c / 4);"),
+    "rcm_not_reversed": ("for (int32_t i = 0; i < N; ++i) perm[i] = order[N - 1 - i];",
+                         "for (int32_t i = 0; i < N; ++i) perm[i] = order[i];"),
+    "rcm_neighbours_by_id": ("if (!seen[w]) { nb[m].key = deg[w]; nb[m].id = w; ++m; }",
+                             "if (!seen[w]) { nb[m].key = 0; nb[m].id = w; ++m; }"),
+    "degree_order_in_only": ("deg[i] += indptr[i + 1] - indptr[i];\n      for (int64_t e = indptr[i]; e < indptr[i + 1]; ++e) deg[indices[e]] += 1;",
+                             "deg[i] += indptr[i + 1] - indptr[i];"),
+    "permute_keeps_old_ids": ("indices_out[o++] = inv[indices[e]];",
+                              "indices_out[o++] = indices[e];"),
 }
 
 
@@ -50,6 +59,10 @@ def _battery():
                                                                  400, 30, 1000)),
         ("tile_threshold", tile_pins.test_tile_threshold_is_inclusive),
         ("tile_dups", tile_pins.test_tile_duplicates_stay_residual),
+        ("rcm_small", reorder_pins.test_rcm_path_and_star),
+        ("rcm_order", lambda: reorder_pins.test_rcm_is_a_cuthill_mckee_order(2, 150, 8.0)),
+        ("degree", reorder_pins.test_degree_order),
+        ("permute", reorder_pins.test_permuted_csr_is_the_relabelled_graph),
     ]
     for name, fn in checks:
         try:
