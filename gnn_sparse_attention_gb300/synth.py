@@ -57,6 +57,9 @@ WORKLOADS = {
     # Stochastic block model, 64-node communities ordered by community.
     "sbm1m": Workload("sbm1m", "sbm", 1 << 20, 8, 64, "bf16", "dot", False,
                       {"block": 64, "p_in": 0.5, "inter_per_node": 4}),
+    # The same block model on a quarter of the nodes (profiling-sized case).
+    "sbm256k": Workload("sbm256k", "sbm", 1 << 18, 8, 64, "bf16", "dot", False,
+                        {"block": 64, "p_in": 0.5, "inter_per_node": 4}),
 }
 
 
