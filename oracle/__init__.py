@@ -68,6 +68,10 @@ def _load():
             lib.oracle_plan.restype = ctypes.c_int
             lib.oracle_tile_plan.argtypes = [i32, i64, P, P, i64, i64, P, P, P, P, P, P]
             lib.oracle_tile_plan.restype = ctypes.c_int
+            lib.oracle_reduce_forward.argtypes = [i64, P, P, i64, ctypes.c_int, P, P, P]
+            lib.oracle_reduce_forward.restype = ctypes.c_int
+            lib.oracle_reduce_backward.argtypes = [i64, i64, i64, P, P, P]
+            lib.oracle_reduce_backward.restype = ctypes.c_int
             lib.oracle_reorder.argtypes = [i32, i64, P, P, ctypes.c_int, P]
             lib.oracle_reorder.restype = ctypes.c_int
             lib.oracle_permute_csr.argtypes = [i32, i64, P, P, P, P, P]
@@ -178,6 +182,40 @@ def plan(indptr, indices, heavy_threshold, chunk):
         "outdeg": outdeg, "hist_out": hist_out, "light_src": light_src[:nls],
         "src_chunks": src_chunks[:ncs],
     }
+
+
+MAX = 0
+MIN = 1
+
+
+def reduce_forward(indptr, indices, X, op=MAX, rows=None):
+    """Max / min pooling of source rows over each row's edges: (out [R, F] fp64, arg [R, F] int32).
+
+    X is [N, ...] (flattened to F features per node); ``rows`` as for forward().
+    """
+    lib = _load()
+    X = _f64(X)
+    N = X.shape[0]
+    F = int(np.prod(X.shape[1:])) if X.ndim > 1 else 1
+    n_rows, row_ids, row_ptr, col = _rows_args(indptr, indices, rows)
+    out = np.zeros((n_rows, F), np.float64)
+    arg = np.zeros((n_rows, F), np.int32)
+    rc = lib.oracle_reduce_forward(n_rows, _p(row_ptr), _p(col), F, int(op), _p(X), _p(out),
+                                   _p(arg))
+    if rc != 0:
+        raise RuntimeError(f"oracle_reduce_forward failed ({rc})")
+    return out, arg
+
+
+def reduce_backward(arg, dout, N):
+    """dx [N, F] of max / min pooling: each row's gradient goes to its arg source."""
+    lib = _load()
+    arg = np.ascontiguousarray(arg, dtype=np.int32)
+    dout = _f64(dout).reshape(arg.shape)
+    F = arg.shape[1]
+    dx = np.zeros((N, F), np.float64)
+    lib.oracle_reduce_backward(arg.shape[0], N, F, _p(arg), _p(dout), _p(dx))
+    return dx
 
 
 REORDER_DEGREE = 0

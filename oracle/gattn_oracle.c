@@ -527,3 +527,48 @@ int oracle_permute_csr(int32_t N, int64_t M, const int32_t* indptr, const int32_
   free(inv);
   return 0;
 }
+
+/*
+ * Max / min pooling over the in-neighbours ("On Efficient Scaling of GNNs
+ * via IO-Aware Layers Implementations", zh/ko technical summaries,
+ * "Methodology", reduction-based layers: a per-edge message followed by a
+ * reduction over the neighbourhood such as max or min pooling; here the
+ * message of edge j -> i is the source row x[j]).
+ *   op 0 (max) / 1 (min):
+ *     out[r][f] = max (min) over the edges e of row r of x[col[e]][f]
+ *     arg[r][f] = the smallest source id that attains it
+ *   a row without edges gets out 0 and arg -1.
+ * Backward of L = sum out * dout: dx[j][f] = sum of dout[r][f] over the rows
+ * r with arg[r][f] == j (dx is [N, F] by node id, overwritten).
+ * Row subsets work as for the attention oracle (row r is a row position).
+ */
+int oracle_reduce_forward(int64_t n_rows, const int64_t* row_ptr, const int32_t* col, int64_t F,
+                          int op, const double* x, double* out, int32_t* arg) {
+  if (op != 0 && op != 1) return -1;
+  for (int64_t r = 0; r < n_rows; ++r) {
+    for (int64_t f = 0; f < F; ++f) {
+      double best = 0.0;
+      int32_t who = -1;
+      for (int64_t e = row_ptr[r]; e < row_ptr[r + 1]; ++e) {
+        const int32_t j = col[e];
+        const double v = x[(int64_t)j * F + f];
+        const int better = who < 0 || (op == 0 ? v > best : v < best) || (v == best && j < who);
+        if (better) { best = v; who = j; }
+      }
+      out[r * F + f] = best;
+      arg[r * F + f] = who;
+    }
+  }
+  return 0;
+}
+
+int oracle_reduce_backward(int64_t n_rows, int64_t N, int64_t F, const int32_t* arg,
+                           const double* dout, double* dx) {
+  memset(dx, 0, (size_t)(N * F) * sizeof(double));
+  for (int64_t r = 0; r < n_rows; ++r)
+    for (int64_t f = 0; f < F; ++f) {
+      const int32_t j = arg[r * F + f];
+      if (j >= 0) dx[(int64_t)j * F + f] += dout[r * F + f];
+    }
+  return 0;
+}

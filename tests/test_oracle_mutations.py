@@ -8,6 +8,7 @@ import pytest
 
 import oracle
 from tests import test_oracle_pins as pins
+from tests import test_oracle_reduce_pins as reduce_pins
 from tests import test_oracle_reorder_pins as reorder_pins
 from tests import test_oracle_tile_pins as tile_pins
 
@@ -39,6 +40,10 @@ MUTANTS = {
                              "deg[i] += indptr[i + 1] - indptr[i];"),
     "permute_keeps_old_ids": ("indices_out[o++] = inv[indices[e]];",
                               "indices_out[o++] = indices[e];"),
+    "pool_tie_largest_id": ("(v == best && j < who);", "(v == best && j > who);"),
+    "pool_min_as_max": ("(op == 0 ? v > best : v < best)", "(v > best)"),
+    "pool_grad_to_row": ("if (j >= 0) dx[(int64_t)j * F + f] += dout[r * F + f];",
+                         "if (j >= 0) dx[r * F + f] += dout[r * F + f];"),
 }
 
 
@@ -63,6 +68,9 @@ def _battery():
         ("rcm_order", lambda: reorder_pins.test_rcm_is_a_cuthill_mckee_order(2, 150, 8.0)),
         ("degree", reorder_pins.test_degree_order),
         ("permute", reorder_pins.test_permuted_csr_is_the_relabelled_graph),
+        ("pool_ties", reduce_pins.test_pooling_ties_pick_the_smallest_source),
+        ("pool_brute", lambda: reduce_pins.test_pooling_brute_force(oracle.MIN, 0, 50, 4.0, 8)),
+        ("pool_fd", lambda: reduce_pins.test_pooling_backward_finite_differences(oracle.MAX)),
     ]
     for name, fn in checks:
         try:
