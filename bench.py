@@ -262,6 +262,17 @@ def run_cuda(args):
     w = synth.WORKLOADS[args.workload]
     indptr, indices = synth.make_graph(w, seed=0)
     f = synth.make_features(w, seed=0)
+    reorder = None
+    if args.reorder != "none":                    # relabel graph and feature rows once
+        t_r = time.perf_counter()
+        for kind in args.reorder.split(","):      # e.g. "random,rcm": scramble, then restore
+            if kind == "random":
+                perm = np.random.default_rng(7).permutation(len(indptr) - 1).astype(np.int32)
+            else:
+                perm = gb.gattn_reorder(indptr, indices, kind)
+            indptr, indices = gb.gattn_permute_csr(indptr, indices, perm)
+            f = {k: (v[perm] if v.shape[0] == len(perm) else v) for k, v in f.items()}
+        reorder = {"kind": args.reorder, "host_seconds": round(time.perf_counter() - t_r, 2)}
     N, M = len(indptr) - 1, int(indptr[-1])
     H, D = w.H, w.D
     s = 2 if w.dtype == "bf16" else 4
@@ -414,13 +425,15 @@ def run_cuda(args):
         "config": workload_config(w, N, M, {
             "parallelism": "replicas" if world > 1 else "single",
             "l2": "flushed before every timed step (256 MB write, outside the timed region)",
+            "reorder": reorder,
             "plan": {"heavy_threshold": info["heavy_threshold"], "chunk": info["chunk"],
                      "n_heavy": info["n_heavy"], "n_chunks": info["n_chunks"],
                      "n_heavy_src": info["n_heavy_src"]}}),
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
                      "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
-                     "traffic": dram_traffic(dom, w.name)},
+                     "traffic": (dram_traffic(dom, w.name) if reorder is None and not args.tile
+                                 else None)},
         "step_gbs": round(step_bytes / (statistics.mean(step_ms) / 1e3) / 1e9, 1),
         "kernels": kernels,
         "e2e": {"value": e2e_value, "unit": "edges/s",
@@ -492,9 +505,14 @@ def main(argv=None):
                     help="synthetic workload (default: the power-law graph the metric is quoted on)")
     ap.add_argument("--tile", action="store_true",
                     help="build the plan with the dense-tile split (tensor-core forward)")
+    ap.add_argument("--reorder", default="none",
+                    help="relabel the graph (and feature rows) before timing: none, degree, rcm, "
+                         "random (a seeded shuffle), or a comma list applied in order")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the oracle timing (profiling runs)")
     args = ap.parse_args(argv)
+    if not all(k in ("none", "degree", "rcm", "random") for k in args.reorder.split(",")):
+        ap.error(f"unknown --reorder {args.reorder}")
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":

@@ -25,7 +25,9 @@ GATTN_SCORE_DOT, GATTN_SCORE_GATV2 = 0, 1
 EXPORTED = ("gattn_plan_create", "gattn_plan_destroy", "gattn_plan_get_info",
             "gattn_plan_export", "gattn_workspace_size", "gattn_fwd", "gattn_bwd",
             "gattn_bwd_dq", "gattn_bwd_dkdv", "gattn_plan_check_errors", "gattn_fwd_noalloc",
-            "gattn_plan_export_tiles", "gattn_last_error", "gattn_version")
+            "gattn_plan_export_tiles", "gattn_reorder", "gattn_permute_csr",
+            "gattn_permute_rows", "gattn_pool_workspace_size", "gattn_pool_fwd",
+            "gattn_pool_bwd", "gattn_last_error", "gattn_version")
 
 
 class GattnError(RuntimeError):
@@ -95,7 +97,13 @@ def load_library(path: str | None = None):
         lib.gattn_fwd_noalloc.argtypes = [P, i32, i32, ctypes.c_int, P, P, P,
                                           ctypes.POINTER(_Score), P, P, P]
         lib.gattn_plan_export_tiles.argtypes = [P] * 6
-        for name in EXPORTED[:12]:
+        lib.gattn_reorder.argtypes = [P, P, i32, i64, i32, P]
+        lib.gattn_permute_csr.argtypes = [P, P, i32, i64, P, P, P]
+        lib.gattn_permute_rows.argtypes = [P, P, P, i32, i64, i32, P]
+        lib.gattn_pool_workspace_size.argtypes = [P, i32, ctypes.c_int, ctypes.POINTER(sz)]
+        lib.gattn_pool_fwd.argtypes = [P, i32, ctypes.c_int, i32, P, P, P, P, sz, P]
+        lib.gattn_pool_bwd.argtypes = [P, i32, ctypes.c_int, P, P, P, P, sz, P]
+        for name in EXPORTED[:18]:
             getattr(lib, name).restype = st
         lib.gattn_last_error.restype = ctypes.c_char_p
         lib.gattn_last_error.argtypes = []
@@ -251,6 +259,95 @@ def gattn_plan_export_tiles(plan: Plan) -> dict:
     ptrs = [arr[k].ctypes.data_as(ctypes.c_void_p) if arr[k].size else None for k in order]
     _check(load_library().gattn_plan_export_tiles(plan.handle, *ptrs), "gattn_plan_export_tiles")
     return arr
+
+
+REORDER = {"degree": 0, "rcm": 1}
+
+
+def gattn_reorder(indptr: np.ndarray, indices: np.ndarray, kind: str = "rcm") -> np.ndarray:
+    """Relabelling of a host CSR graph: perm[new] = old (host call)."""
+    indptr = np.ascontiguousarray(indptr, dtype=np.int32)
+    indices = np.ascontiguousarray(indices, dtype=np.int32)
+    N = len(indptr) - 1
+    perm = np.zeros(max(N, 1), np.int32)
+    _check(load_library().gattn_reorder(indptr.ctypes.data, indices.ctypes.data if indices.size
+                                        else None, N, int(indptr[-1]), REORDER[kind],
+                                        perm.ctypes.data), "gattn_reorder")
+    return perm[:N]
+
+
+def gattn_permute_csr(indptr: np.ndarray, indices: np.ndarray, perm: np.ndarray):
+    """The host CSR graph under a relabelling: (indptr, indices) with sorted rows."""
+    indptr = np.ascontiguousarray(indptr, dtype=np.int32)
+    indices = np.ascontiguousarray(indices, dtype=np.int32)
+    perm = np.ascontiguousarray(perm, dtype=np.int32)
+    N, M = len(indptr) - 1, int(indptr[-1])
+    ptr = np.zeros(N + 1, np.int32)
+    idx = np.zeros(max(M, 1), np.int32)
+    _check(load_library().gattn_permute_csr(indptr.ctypes.data, indices.ctypes.data if M else None,
+                                            N, M, perm.ctypes.data if N else None, ptr.ctypes.data,
+                                            idx.ctypes.data), "gattn_permute_csr")
+    return ptr, idx[:M]
+
+
+def gattn_permute_rows(x: torch.Tensor, perm: torch.Tensor, inverse: bool = False, out=None,
+                       stream=None) -> torch.Tensor:
+    """Rows of a CUDA tensor under perm: out[i] = x[perm[i]] (or out[perm[i]] = x[i])."""
+    if not x.is_cuda or not x.is_contiguous() or perm.dtype != torch.int32 or not perm.is_cuda:
+        raise ValueError("x must be a contiguous CUDA tensor and perm a CUDA int32 tensor")
+    out = torch.empty_like(x) if out is None else out
+    N = x.shape[0]
+    row_bytes = x[0].numel() * x.element_size() if N else 16
+    _check(load_library().gattn_permute_rows(_ptr(x), _ptr(out), _ptr(perm), N, row_bytes,
+                                             int(bool(inverse)), _stream(stream)),
+           "gattn_permute_rows")
+    return out
+
+
+POOL = {"max": 0, "min": 1}
+
+
+def gattn_pool_workspace_size(plan: Plan, F: int, dtype) -> int:
+    n = ctypes.c_size_t()
+    _check(load_library().gattn_pool_workspace_size(plan.handle, F, _dtype_code(dtype),
+                                                     ctypes.byref(n)), "gattn_pool_workspace_size")
+    return n.value
+
+
+def _pool_ws(plan: Plan, F: int, dtype, device, workspace):
+    if workspace is not None:
+        return workspace
+    return torch.empty(gattn_pool_workspace_size(plan, F, dtype), dtype=torch.uint8,
+                       device=device)
+
+
+def gattn_pool_fwd(plan: Plan, x: torch.Tensor, op: str = "max", out=None, arg=None,
+                   workspace=None, stream=None):
+    """Max / min pooling of source rows: returns (out [N, F] in x's dtype, arg int32 [N, F])."""
+    if not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA tensor [N, F]")
+    x2 = x.reshape(x.shape[0], -1)
+    F = x2.shape[1]
+    out = torch.empty_like(x2) if out is None else out
+    arg = torch.empty(x2.shape, dtype=torch.int32, device=x.device) if arg is None else arg
+    ws = _pool_ws(plan, F, x.dtype, x.device, workspace)
+    _check(load_library().gattn_pool_fwd(plan.handle, F, _dtype_code(x.dtype), POOL[op], _ptr(x2),
+                                         _ptr(out), _ptr(arg), _ptr(ws), ws.numel(),
+                                         _stream(stream)), "gattn_pool_fwd")
+    return out.view(x.shape), arg.view(x.shape)
+
+
+def gattn_pool_bwd(plan: Plan, arg: torch.Tensor, dout: torch.Tensor, dx=None, workspace=None,
+                   stream=None):
+    """Gradient of pooling: dx[j] collects dout[i] wherever arg[i] == j."""
+    d2 = dout.contiguous().reshape(dout.shape[0], -1)
+    F = d2.shape[1]
+    dx = torch.empty_like(d2) if dx is None else dx
+    ws = _pool_ws(plan, F, dout.dtype, dout.device, workspace)
+    _check(load_library().gattn_pool_bwd(plan.handle, F, _dtype_code(dout.dtype),
+                                         _ptr(arg.contiguous()), _ptr(d2), _ptr(dx), _ptr(ws),
+                                         ws.numel(), _stream(stream)), "gattn_pool_bwd")
+    return dx.view(dout.shape)
 
 
 def gattn_workspace_size(plan: Plan, H: int, D: int, dtype) -> int:

@@ -74,6 +74,10 @@ typedef enum { GATTN_F32 = 0, GATTN_BF16 = 1 } gattn_dtype;
 
 typedef enum { GATTN_SCORE_DOT = 0, GATTN_SCORE_GATV2 = 1 } gattn_score_kind;
 
+typedef enum { GATTN_REORDER_DEGREE = 0, GATTN_REORDER_RCM = 1 } gattn_reorder_kind;
+
+typedef enum { GATTN_POOL_MAX = 0, GATTN_POOL_MIN = 1 } gattn_pool_op;
+
 /* Score parameters.  Host struct; `a` is a device pointer. */
 typedef struct {
   int32_t kind;    /* gattn_score_kind */
@@ -272,6 +276,76 @@ GATTN_API const char* gattn_last_error(void);
 
 /* Library version string, e.g. "gattn 0.1.0 sm_103a". */
 GATTN_API const char* gattn_version(void);
+
+/*
+ * Max / min pooling over the in-neighbours ("Methodology", reduction-based
+ * layers: a per-edge message -- here the source row -- reduced over the
+ * neighbourhood; light nodes in one pass, heavy nodes over edge chunks merged
+ * by atomics on packed (value, index) pairs), on the same plan.
+ *   x[N, F], out[N, F] : device, I/O dtype; F * sizeof(dtype) a power of two
+ *                        in [32, 2048] bytes (else GATTN_ERR_UNSUPPORTED).
+ *   op                 : GATTN_POOL_MAX or GATTN_POOL_MIN.
+ *   out[i][f] = max (min) over the sources j of i of x[j][f] (exact: a copy of
+ *   an input value); arg[i][f] (device int32 [N, F]) = the smallest such j;
+ *   a node without in-edges gets out 0 and arg -1.  NaN inputs are not
+ *   supported.
+ *   workspace          : device, gattn_pool_workspace_size bytes, 16-byte
+ *                        aligned; cleared by the calls themselves.
+ * Backward: dx[j][f] = sum of dout[i][f] over the nodes i with arg[i][f] == j
+ * (fp32 accumulation in the workspace, rounded once to the I/O dtype; the
+ * order of the additions is not fixed, so the last bits may vary between
+ * runs).  Asynchronous on `stream`.
+ */
+GATTN_API gattn_status gattn_pool_workspace_size(const gattn_plan* plan, int32_t F,
+                                                 gattn_dtype dtype, size_t* bytes);
+GATTN_API gattn_status gattn_pool_fwd(const gattn_plan* plan, int32_t F, gattn_dtype dtype,
+                                      int32_t op, const void* x, void* out, int32_t* arg,
+                                      void* workspace, size_t workspace_bytes,
+                                      gattn_stream_t stream);
+GATTN_API gattn_status gattn_pool_bwd(const gattn_plan* plan, int32_t F, gattn_dtype dtype,
+                                      const int32_t* arg, const void* dout, void* dx,
+                                      void* workspace, size_t workspace_bytes,
+                                      gattn_stream_t stream);
+
+/*
+ * Node relabelling for gather locality ("Methodology" and results: graph
+ * reordering helps gather-dominated kernels on high-degree graphs; the
+ * pages name no method).  HOST pointers, synchronous, no device work.
+ *   kind GATTN_REORDER_DEGREE : nodes by decreasing total degree (in + out,
+ *        every edge counted), ties by increasing id.
+ *   kind GATTN_REORDER_RCM    : reverse Cuthill-McKee on the undirected
+ *        simple graph (j -> i and i -> j merged, self-loops and repeats
+ *        dropped): while nodes are unvisited, the unvisited node of least
+ *        degree (smallest id on ties) roots a breadth-first search that
+ *        appends each dequeued node's unvisited neighbours in increasing
+ *        (degree, id) order; the final order is reversed.
+ *   perm[N] : receives perm[new id] = old id.
+ * Returns GATTN_ERR_BAD_GRAPH for an invalid CSR.
+ */
+GATTN_API gattn_status gattn_reorder(const int32_t* indptr, const int32_t* indices, int32_t N,
+                                     int64_t M, int32_t kind, int32_t* perm);
+
+/*
+ * The graph under a relabelling (HOST pointers, synchronous): row i of the
+ * output is old row perm[i], its sources renamed to their new ids and sorted
+ * ascending (repeated sources kept).  indptr_out[N+1], indices_out[M].
+ * Returns GATTN_ERR_INVALID_ARG when perm is not a permutation of [0, N).
+ */
+GATTN_API gattn_status gattn_permute_csr(const int32_t* indptr, const int32_t* indices,
+                                         int32_t N, int64_t M, const int32_t* perm,
+                                         int32_t* indptr_out, int32_t* indices_out);
+
+/*
+ * Permute the rows of a dense device tensor of N rows of row_bytes bytes (a
+ * multiple of 16; src and dst distinct, 16-byte aligned device pointers;
+ * perm a device int32 permutation of [0, N)): inverse = 0 gathers, dst row i
+ * = src row perm[i] (features into the new labelling); inverse = 1
+ * scatters, dst row perm[i] = src row i (results back to the old one).
+ * Asynchronous on `stream`; entries of perm outside [0, N) are skipped.
+ */
+GATTN_API gattn_status gattn_permute_rows(const void* src, void* dst, const int32_t* perm,
+                                          int32_t N, int64_t row_bytes, int32_t inverse,
+                                          gattn_stream_t stream);
 
 #ifdef __cplusplus
 }
