@@ -68,6 +68,8 @@ def _load():
             lib.oracle_plan.restype = ctypes.c_int
             lib.oracle_tile_plan.argtypes = [i32, i64, P, P, i64, i64, P, P, P, P, P, P]
             lib.oracle_tile_plan.restype = ctypes.c_int
+            lib.oracle_spmm.argtypes = [i64, P, P, P, i64, P, P]
+            lib.oracle_spmm.restype = ctypes.c_int
             lib.oracle_reduce_forward.argtypes = [i64, P, P, i64, ctypes.c_int, P, P, P]
             lib.oracle_reduce_forward.restype = ctypes.c_int
             lib.oracle_reduce_backward.argtypes = [i64, i64, i64, P, P, P]
@@ -182,6 +184,20 @@ def plan(indptr, indices, heavy_threshold, chunk):
         "outdeg": outdeg, "hist_out": hist_out, "light_src": light_src[:nls],
         "src_chunks": src_chunks[:ncs],
     }
+
+
+def spmm(indptr, indices, w, X):
+    """y = A x with A the weighted adjacency (w[e] per CSR edge): [N, F] fp64."""
+    lib = _load()
+    X = _f64(X)
+    F = int(np.prod(X.shape[1:])) if X.ndim > 1 else 1
+    row_ptr = np.ascontiguousarray(indptr, dtype=np.int64)
+    col = np.ascontiguousarray(indices, dtype=np.int32)
+    w = _f64(w)
+    n_rows = len(row_ptr) - 1
+    y = np.zeros((n_rows, F), np.float64)
+    lib.oracle_spmm(n_rows, _p(row_ptr), _p(col), _p(w), F, _p(X), _p(y))
+    return y
 
 
 MAX = 0

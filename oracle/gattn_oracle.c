@@ -572,3 +572,24 @@ int oracle_reduce_backward(int64_t n_rows, int64_t N, int64_t F, const int32_t* 
     }
   return 0;
 }
+
+/*
+ * Sparse-dense product of the weighted adjacency with node features
+ * ("On Efficient Scaling of GNNs via IO-Aware Layers Implementations", zh/ko
+ * technical summaries, "Methodology", SpMM-based convolutions such as GCN:
+ * H' = A H W, where the SpMM A H aggregates neighbour rows with the edge
+ * weights): y[r][f] = sum over the edges e of row r of w[e] * x[col[e]][f].
+ * A row without edges gets 0.  w holds one weight per edge in CSR order.
+ */
+int oracle_spmm(int64_t n_rows, const int64_t* row_ptr, const int32_t* col, const double* w,
+                int64_t F, const double* x, double* y) {
+  for (int64_t r = 0; r < n_rows; ++r) {
+    double* yr = y + r * F;
+    for (int64_t f = 0; f < F; ++f) yr[f] = 0.0;
+    for (int64_t e = row_ptr[r]; e < row_ptr[r + 1]; ++e) {
+      const double* xj = x + (int64_t)col[e] * F;
+      for (int64_t f = 0; f < F; ++f) yr[f] += w[e] * xj[f];
+    }
+  }
+  return 0;
+}

@@ -9,6 +9,7 @@ import pytest
 import oracle
 from tests import test_oracle_pins as pins
 from tests import test_oracle_reduce_pins as reduce_pins
+from tests import test_oracle_spmm_pins as spmm_pins
 from tests import test_oracle_reorder_pins as reorder_pins
 from tests import test_oracle_tile_pins as tile_pins
 
@@ -44,6 +45,10 @@ MUTANTS = {
     "pool_min_as_max": ("(op == 0 ? v > best : v < best)", "(v > best)"),
     "pool_grad_to_row": ("if (j >= 0) dx[(int64_t)j * F + f] += dout[r * F + f];",
                          "if (j >= 0) dx[r * F + f] += dout[r * F + f];"),
+    "spmm_drops_weight": ("for (int64_t f = 0; f < F; ++f) yr[f] += w[e] * xj[f];",
+                          "for (int64_t f = 0; f < F; ++f) yr[f] += xj[f];"),
+    "spmm_row_gather": ("const double* xj = x + (int64_t)col[e] * F;",
+                        "const double* xj = x + r * F;"),
 }
 
 
@@ -71,6 +76,8 @@ def _battery():
         ("pool_ties", reduce_pins.test_pooling_ties_pick_the_smallest_source),
         ("pool_brute", lambda: reduce_pins.test_pooling_brute_force(oracle.MIN, 0, 50, 4.0, 8)),
         ("pool_fd", lambda: reduce_pins.test_pooling_backward_finite_differences(oracle.MAX)),
+        ("spmm_hand", spmm_pins.test_spmm_hand_example),
+        ("spmm_scipy", lambda: spmm_pins.test_spmm_equals_scipy(0, 300, 6.0, 16)),
     ]
     for name, fn in checks:
         try:
