@@ -27,7 +27,8 @@ EXPORTED = ("gattn_plan_create", "gattn_plan_destroy", "gattn_plan_get_info",
             "gattn_bwd_dq", "gattn_bwd_dkdv", "gattn_plan_check_errors", "gattn_fwd_noalloc",
             "gattn_plan_export_tiles", "gattn_reorder", "gattn_permute_csr",
             "gattn_permute_rows", "gattn_pool_workspace_size", "gattn_pool_fwd",
-            "gattn_pool_bwd", "gattn_last_error", "gattn_version")
+            "gattn_pool_bwd", "gattn_spmm_workspace_size", "gattn_spmm", "gattn_last_error",
+            "gattn_version")
 
 
 class GattnError(RuntimeError):
@@ -103,7 +104,9 @@ def load_library(path: str | None = None):
         lib.gattn_pool_workspace_size.argtypes = [P, i32, ctypes.c_int, ctypes.POINTER(sz)]
         lib.gattn_pool_fwd.argtypes = [P, i32, ctypes.c_int, i32, P, P, P, P, sz, P]
         lib.gattn_pool_bwd.argtypes = [P, i32, ctypes.c_int, P, P, P, P, sz, P]
-        for name in EXPORTED[:18]:
+        lib.gattn_spmm_workspace_size.argtypes = [P, i32, ctypes.c_int, ctypes.POINTER(sz)]
+        lib.gattn_spmm.argtypes = [P, i32, ctypes.c_int, P, P, P, i32, P, sz, P]
+        for name in EXPORTED[:20]:
             getattr(lib, name).restype = st
         lib.gattn_last_error.restype = ctypes.c_char_p
         lib.gattn_last_error.argtypes = []
@@ -348,6 +351,31 @@ def gattn_pool_bwd(plan: Plan, arg: torch.Tensor, dout: torch.Tensor, dx=None, w
                                          _ptr(arg.contiguous()), _ptr(d2), _ptr(dx), _ptr(ws),
                                          ws.numel(), _stream(stream)), "gattn_pool_bwd")
     return dx.view(dout.shape)
+
+
+def gattn_spmm_workspace_size(plan: Plan, F: int, dtype) -> int:
+    n = ctypes.c_size_t()
+    _check(load_library().gattn_spmm_workspace_size(plan.handle, F, _dtype_code(dtype),
+                                                     ctypes.byref(n)), "gattn_spmm_workspace_size")
+    return n.value
+
+
+def gattn_spmm(plan: Plan, w: torch.Tensor, x: torch.Tensor, transpose: bool = False, y=None,
+               workspace=None, stream=None) -> torch.Tensor:
+    """y = A x (or A^T x) with edge weights w (fp32 [M], the plan's CSR order)."""
+    if not x.is_cuda or not x.is_contiguous() or w.dtype != torch.float32 or not w.is_cuda:
+        raise ValueError("x must be a contiguous CUDA tensor and w a CUDA fp32 tensor")
+    x2 = x.reshape(x.shape[0], -1)
+    F = x2.shape[1]
+    y = torch.empty_like(x2) if y is None else y
+    ws = workspace
+    if ws is None:
+        ws = torch.empty(gattn_spmm_workspace_size(plan, F, x.dtype), dtype=torch.uint8,
+                         device=x.device)
+    _check(load_library().gattn_spmm(plan.handle, F, _dtype_code(x.dtype), _ptr(w.contiguous()),
+                                     _ptr(x2), _ptr(y), int(bool(transpose)), _ptr(ws), ws.numel(),
+                                     _stream(stream)), "gattn_spmm")
+    return y.view(x.shape)
 
 
 def gattn_workspace_size(plan: Plan, H: int, D: int, dtype) -> int:

@@ -73,6 +73,9 @@ struct Plan {
   int32_t* trow_ptr = nullptr;    // [n_trows + 1] their tiles: [trow_ptr[r], trow_ptr[r+1])
   int32_t* indptr_r = nullptr;    // [N+1] residual CSR
   int32_t* indices_r = nullptr;   // [M_res]
+  int32_t* res_eid = nullptr;     // [M_res] CSR edge id of each residual edge
+  int32_t* tile_slot = nullptr;   // [M] t*16384 + (i%128)*128 + j%128 for tile edges, else -1
+                                  // (weighted tiles need n_tiles * 16384 < 2^31)
   int64_t n_light_r = 0, n_chunks_r = 0, n_inner_r = 0;
   int4* items_r = nullptr;
   int4* sorted_r = nullptr;

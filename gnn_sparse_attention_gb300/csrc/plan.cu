@@ -441,7 +441,7 @@ __global__ void k_tile_meta(const int32_t* __restrict__ start, const int32_t* __
 __global__ void k_tile_masks(const int32_t* __restrict__ tbeg, const int32_t* __restrict__ tend,
                              const int32_t* __restrict__ seid, const int32_t* __restrict__ row,
                              const int32_t* __restrict__ indices, uint32_t* __restrict__ mask,
-                             uint8_t* __restrict__ in_tile) {
+                             uint8_t* __restrict__ in_tile, int32_t* __restrict__ slot) {
   __shared__ uint32_t s_seen[kTileRows * 4], s_dup[kTileRows * 4];
   const int64_t t = blockIdx.x;
   for (int w = threadIdx.x; w < kTileRows * 4; w += blockDim.x) s_seen[w] = s_dup[w] = 0;
@@ -463,7 +463,11 @@ __global__ void k_tile_masks(const int32_t* __restrict__ tbeg, const int32_t* __
   for (int32_t p = b + threadIdx.x; p < e1; p += blockDim.x) {
     const int32_t e = seid[p];
     const int r = row[e] % kTileRows, c = indices[e] % kTileRows;
-    if ((s_seen[r * 4 + c / 32] >> (c % 32)) & 1u) in_tile[e] = 1;
+    if ((s_seen[r * 4 + c / 32] >> (c % 32)) & 1u) {
+      in_tile[e] = 1;
+      const int64_t sl = t * kTileRows * kTileRows + r * kTileRows + c;
+      if (sl < INT32_MAX) slot[e] = int32_t(sl);  // tiles beyond 2^31 weights: no WSB slot
+    }
   }
 }
 
@@ -487,7 +491,8 @@ __global__ void k_res_count(const int32_t* __restrict__ indptr, int32_t N,
 
 __global__ void k_res_fill(const int32_t* __restrict__ indptr, int32_t N,
                            const int32_t* __restrict__ indices, const uint8_t* __restrict__ in_tile,
-                           const int32_t* __restrict__ ptr_r, int32_t* __restrict__ idx_r) {
+                           const int32_t* __restrict__ ptr_r, int32_t* __restrict__ idx_r,
+                           int32_t* __restrict__ eid_r) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t(gridDim.x) * blockDim.x) >> 5;
   for (int64_t i = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; i < N; i += warps) {
@@ -497,7 +502,11 @@ __global__ void k_res_fill(const int32_t* __restrict__ indptr, int32_t N,
       const int32_t e = e0 + lane;
       const bool keep = e < e1 && !in_tile[e];
       const unsigned bal = __ballot_sync(0xffffffffu, keep);
-      if (keep) idx_r[out + __popc(bal & ((1u << lane) - 1u))] = indices[e];
+      if (keep) {
+        const int32_t o = out + __popc(bal & ((1u << lane) - 1u));
+        idx_r[o] = indices[e];
+        eid_r[o] = e;
+      }
       out += __popc(bal);
     }
   }
@@ -705,6 +714,8 @@ gattn_status tile_build(Plan* p, Scratch& scr, cudaStream_t st) {
   GATTN_CUDA(plan_alloc(p, &p->tile_rb, n_tiles));
   GATTN_CUDA(plan_alloc(p, &p->tile_cb, n_tiles));
   GATTN_CUDA(plan_alloc(p, &p->tile_mask, int64_t(n_tiles) * kTileRows * 4));
+  GATTN_CUDA(plan_alloc(p, &p->tile_slot, M));
+  GATTN_CUDA(cudaMemsetAsync(p->tile_slot, 0xff, (M ? M : 1) * sizeof(int32_t), st));
   if (n_tiles > 0) {
     int32_t *tbeg, *tend;
     GATTN_CUDA(scr.get(&tbeg, n_tiles));
@@ -714,7 +725,7 @@ gattn_status tile_build(Plan* p, Scratch& scr, cudaStream_t st) {
                                                                  tend);
     GATTN_CUDA(cudaGetLastError());
     k_tile_masks<<<(unsigned)n_tiles, kThreads, 0, st>>>(tbeg, tend, seid, row, p->indices,
-                                                        p->tile_mask, in_tile);
+                                                        p->tile_mask, in_tile, p->tile_slot);
     GATTN_CUDA(cudaGetLastError());
   }
   // residual CSR
@@ -730,8 +741,9 @@ gattn_status tile_build(Plan* p, Scratch& scr, cudaStream_t st) {
   GATTN_CUDA(cudaStreamSynchronize(st));
   p->M_res = mres;
   GATTN_CUDA(plan_alloc(p, &p->indices_r, mres));
+  GATTN_CUDA(plan_alloc(p, &p->res_eid, mres));
   k_res_fill<<<warp_grid, kThreads, 0, st>>>(p->indptr, N, p->indices, in_tile, p->indptr_r,
-                                            p->indices_r);
+                                            p->indices_r, p->res_eid);
   GATTN_CUDA(cudaGetLastError());
   // row blocks with tiles
   int32_t n_trows = 0;

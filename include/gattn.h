@@ -308,6 +308,30 @@ GATTN_API gattn_status gattn_pool_bwd(const gattn_plan* plan, int32_t F, gattn_d
                                       gattn_stream_t stream);
 
 /*
+ * Weighted SpMM with the adjacency ("Methodology", SpMM-based convolutions
+ * such as GCN: H' = A H W; the transposed adjacency is cached for the
+ * backward; a weighted block-sparse form of locally dense neighbourhoods
+ * runs on the tensor cores), on the same plan:
+ *   transpose = 0 : y[i] = sum over the edges e = (j -> i) of w[e] x[j]
+ *   transpose = 1 : y[j] = sum over the edges e = (j -> i) of w[e] x[i]
+ *                   (the backward of the first: dX = A^T dY)
+ *   w      : device fp32 [M], one weight per edge in the plan's CSR order.
+ *   x, y   : device [N, F] in `dtype`, distinct; F * sizeof(dtype) a power of
+ *            two in [32, 2048] bytes.  A node without edges gets 0.
+ * With transpose = 0, a plan built with tile_enable, bf16 and F a multiple
+ * of 64, the tiles' edges run as bf16-weight [128 x 128] x [128 x F] tensor-
+ * core products added to the CSR result of the other edges (weights rounded
+ * to bf16 there, and that CSR part rounded to bf16 before the addition);
+ * otherwise every edge goes through the CSR pass (fp32 sums, one rounding).
+ *   workspace : device, gattn_spmm_workspace_size bytes, 16-byte aligned.
+ */
+GATTN_API gattn_status gattn_spmm_workspace_size(const gattn_plan* plan, int32_t F,
+                                                 gattn_dtype dtype, size_t* bytes);
+GATTN_API gattn_status gattn_spmm(const gattn_plan* plan, int32_t F, gattn_dtype dtype,
+                                  const float* w, const void* x, void* y, int32_t transpose,
+                                  void* workspace, size_t workspace_bytes, gattn_stream_t stream);
+
+/*
  * Node relabelling for gather locality ("Methodology" and results: graph
  * reordering helps gather-dominated kernels on high-degree graphs; the
  * pages name no method).  HOST pointers, synchronous, no device work.
