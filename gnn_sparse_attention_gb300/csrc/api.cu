@@ -66,10 +66,12 @@ Workspace ws_layout(const Plan& p, int H, int D) {
   w.fwd_part = off;
   const size_t slots = size_t(p.n_chunks + p.n_inner);
   const size_t slots_res = size_t(p.n_chunks_r + p.n_inner_r);  // residual forward (tiles)
-  const size_t slots_src = size_t(p.n_src_chunks + p.n_inner_src);
+  const size_t slots_src_full = size_t(p.n_src_chunks + p.n_inner_src);
+  const size_t slots_src_res = size_t(p.n_chunks_src_r + p.n_inner_src_r);
+  const size_t slots_src = slots_src_full > slots_src_res ? slots_src_full : slots_src_res;
   off = align_up(off + (slots > slots_res ? slots : slots_res) * w.pstride * 4, 256);
   w.dq_part = off;
-  off = align_up(off + slots * HD * 4, 256);
+  off = align_up(off + (slots > slots_res ? slots : slots_res) * HD * 4, 256);
   w.delta = off;
   off = align_up(off + size_t(p.N) * H * 4, 256);
   w.dkv_part = off;
@@ -112,6 +114,14 @@ gattn_status check_tensor(const void* t, const char* name) {
     return GATTN_ERR_INVALID_ARG;
   }
   return GATTN_OK;
+}
+
+// A tiled plan runs its dense tiles on the tensor cores for bf16 I/O, the
+// dot score and D = 64 or 128; other layouts take the CSR path over every
+// edge.
+bool tile_path(const Plan& p, gattn_dtype dt, int kind, int D) {
+  return p.tile_min > 0 && p.n_tiles > 0 && dt == GATTN_BF16 && kind == GATTN_SCORE_DOT &&
+         (D == 64 || D == 128);
 }
 
 gattn_status launched(const char* what) {
@@ -390,8 +400,7 @@ gattn_status gattn_fwd(const gattn_plan* plan, int32_t H, int32_t D, gattn_dtype
                 w.total, workspace_bytes);
   char* ws = static_cast<char*>(workspace);
   // dense tiles on the tensor cores: the CSR pass covers the residual edges
-  const bool tiles = p.tile_min > 0 && p.n_tiles > 0 && dtype == GATTN_BF16 &&
-                     score->kind == GATTN_SCORE_DOT && (D == 64 || D == 128);
+  const bool tiles = tile_path(p, dtype, score->kind, D);
   f.items = tiles ? p.items_r : p.items;
   f.sorted = tiles ? p.sorted_r : p.sorted;
   f.n_items = tiles ? p.n_chunks_r + p.n_light_r : p.n_chunks + p.n_light;
@@ -504,11 +513,14 @@ gattn_status gattn_bwd_dq(const gattn_plan* plan, int32_t H, int32_t D, gattn_dt
   }
   if ((s = check_tensor(out, "out")) || (s = check_tensor(dQ, "dQ"))) return s;
   GATTN_REQUIRE(!gat || !da || aligned(da, 4), GATTN_ERR_INVALID_ARG, "da misaligned");
+  // dense tiles on the tensor cores: the CSR pass covers the residual edges
+  // (and writes Delta for every node), the tile pass adds the tiles' dQ
+  const bool tiles = tile_path(p, dtype, score->kind, D);
   b.O = out;
-  b.items = p.items;
-  b.sorted = p.sorted;
-  b.n_items = p.n_chunks + p.n_light;
-  b.n_chunks = p.n_chunks;
+  b.items = tiles ? p.items_r : p.items;
+  b.sorted = tiles ? p.sorted_r : p.sorted;
+  b.n_items = tiles ? p.n_chunks_r + p.n_light_r : p.n_chunks + p.n_light;
+  b.n_chunks = tiles ? p.n_chunks_r : p.n_chunks;
   b.N = p.N;
   {
     const int es = (int)dtype_size(dtype);
@@ -521,17 +533,39 @@ gattn_status gattn_bwd_dq(const gattn_plan* plan, int32_t H, int32_t D, gattn_dt
         (b.rows16 && !encode_rows_map(&b.ms0, lse, 4, false, p.N, H)))
       return GATTN_ERR_CUDA;
   }
-  b.idx = p.indices;
+  b.idx = tiles ? p.indices_r : p.indices;
   b.G1 = dQ;
   b.G2 = nullptr;
   b.da = gat ? da : nullptr;
   b.part = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.dq_part);
-  b.tree = Tree{p.parent, p.kids, p.n_chunks, p.cnt_dq};
+  b.tree = tiles ? Tree{p.parent_r, p.kids_r, p.n_chunks_r, p.cnt_dq_r}
+                 : Tree{p.parent, p.kids, p.n_chunks, p.cnt_dq};
   if ((s = launch_bwd_csr(dtype, rb, D * (int)dtype_size(dtype), score->kind,
-                          stage_bytes(p.M, p.n_chunks + p.n_light), b, p.num_sms,
-                          st, nullptr)) != GATTN_OK)
+                          stage_bytes(tiles ? p.M_res : p.M, b.n_items), b, p.num_sms, st,
+                          nullptr)) != GATTN_OK)
     return s;
-  return launched("backward (CSR pass)");
+  if ((s = launched("backward (CSR pass)")) != GATTN_OK || !tiles) return s;
+  TileBwdParams tp{};
+  const int64_t HD = int64_t(H) * D;
+  if (!encode_tile_map(&tp.ma0, Q, p.N, HD) || !encode_tile_map(&tp.ma1, dout, p.N, HD) ||
+      !encode_tile_map(&tp.mb0, K, p.N, HD) || !encode_tile_map(&tp.mb1, V, p.N, HD))
+    return GATTN_ERR_CUDA;
+  tp.mask = p.tile_mask;
+  tp.tile_other = p.tile_cb;
+  tp.list = nullptr;
+  tp.grp_blk = p.trow_rb;
+  tp.grp_ptr = p.trow_ptr;
+  tp.n_grp = p.n_trows;
+  tp.N = p.N;
+  tp.H = H;
+  tp.qmul = b.qmul;
+  tp.scale = b.scale;
+  tp.lse = lse;
+  tp.delta = b.delta;
+  tp.g1 = dQ;
+  tp.g2 = nullptr;
+  tp.err = p.err;
+  return launch_tile_bwd(tp, D, false, p.num_sms, st);
 }
 
 gattn_status gattn_bwd_dkdv(const gattn_plan* plan, int32_t H, int32_t D, gattn_dtype dtype,
@@ -548,10 +582,12 @@ gattn_status gattn_bwd_dkdv(const gattn_plan* plan, int32_t H, int32_t D, gattn_
   const Plan& p = plan->p;
   if (p.N == 0) return GATTN_OK;
   if ((s = check_tensor(dK, "dK")) || (s = check_tensor(dV, "dV"))) return s;
-  b.items = p.items_src;
-  b.sorted = p.sorted_src;
-  b.n_items = p.n_src_chunks + p.n_light_src;
-  b.n_chunks = p.n_src_chunks;
+  // dense tiles: the CSC pass covers the residual edges, the tile pass adds
+  const bool tiles = tile_path(p, dtype, score->kind, D);
+  b.items = tiles ? p.items_src_r : p.items_src;
+  b.sorted = tiles ? p.sorted_src_r : p.sorted_src;
+  b.n_items = tiles ? p.n_chunks_src_r + p.n_light_src_r : p.n_src_chunks + p.n_light_src;
+  b.n_chunks = tiles ? p.n_chunks_src_r : p.n_src_chunks;
   b.N = p.N;
   {
     const int es = (int)dtype_size(dtype);
@@ -564,17 +600,40 @@ gattn_status gattn_bwd_dkdv(const gattn_plan* plan, int32_t H, int32_t D, gattn_
         (b.delta16 && !encode_rows_map(&b.ms1, b.delta, 4, false, p.N, H)))
       return GATTN_ERR_CUDA;
   }
-  b.idx = p.csc_dst;
+  b.idx = tiles ? p.csc_dst_r : p.csc_dst;
   b.G1 = dK;
   b.G2 = dV;
   b.da = nullptr;
   b.part = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.dkv_part);
-  b.tree = Tree{p.parent_src, p.kids_src, p.n_src_chunks, p.cnt_dkv};
+  b.tree = tiles ? Tree{p.parent_src_r, p.kids_src_r, p.n_chunks_src_r, p.cnt_dkv_r}
+                 : Tree{p.parent_src, p.kids_src, p.n_src_chunks, p.cnt_dkv};
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if ((s = launch_bwd_csc(dtype, rb, D * (int)dtype_size(dtype), score->kind,
-                          stage_bytes(p.M, p.n_src_chunks + p.n_light_src), b, p.num_sms,
-                          reinterpret_cast<cudaStream_t>(stream), nullptr)) != GATTN_OK)
+                          stage_bytes(tiles ? p.M_res : p.M, b.n_items), b, p.num_sms, st,
+                          nullptr)) != GATTN_OK)
     return s;
-  return launched("backward (CSC pass)");
+  if ((s = launched("backward (CSC pass)")) != GATTN_OK || !tiles) return s;
+  TileBwdParams tp{};
+  const int64_t HD = int64_t(H) * D;
+  if (!encode_tile_map(&tp.ma0, K, p.N, HD) || !encode_tile_map(&tp.ma1, V, p.N, HD) ||
+      !encode_tile_map(&tp.mb0, Q, p.N, HD) || !encode_tile_map(&tp.mb1, dout, p.N, HD))
+    return GATTN_ERR_CUDA;
+  tp.mask = p.tile_mask_t;
+  tp.tile_other = p.tile_rb;
+  tp.list = p.tcol_tile;
+  tp.grp_blk = p.tcol_cb;
+  tp.grp_ptr = p.tcol_ptr;
+  tp.n_grp = p.n_tcols;
+  tp.N = p.N;
+  tp.H = H;
+  tp.qmul = b.qmul;
+  tp.scale = b.scale;
+  tp.lse = lse;
+  tp.delta = b.delta;
+  tp.g1 = dK;
+  tp.g2 = dV;
+  tp.err = p.err;
+  return launch_tile_bwd(tp, D, true, p.num_sms, st);
 }
 
 gattn_status gattn_bwd(const gattn_plan* plan, int32_t H, int32_t D, gattn_dtype dtype,

@@ -21,6 +21,33 @@ struct TileParams {
   int32_t* err;
 };
 
+// Backward of the tiles (attn_tile_bwd.cu).  The row kernel (COL = false)
+// walks the row blocks that have tiles and adds dQ; the column kernel (COL =
+// true) walks the column blocks and adds dK, dV.  "Own" rows are the
+// block the CTA works on, "other" rows the tile's block on the other side.
+struct TileBwdParams {
+  CUtensorMap ma0, ma1;        // own block:   row kernel Q, dO;  column kernel K, V
+  CUtensorMap mb0, mb1;        // other block: row kernel K, V;   column kernel Q, dO
+  const uint32_t* mask;        // row kernel: tile masks; column kernel: transposed masks
+  const int32_t* tile_other;   // [n_tiles] other block of each tile (tile_cb or tile_rb)
+  const int32_t* list;         // column kernel: tile ids by column (tcol_tile); row kernel: null
+  const int32_t* grp_blk;      // [n_grp] own blocks (trow_rb or tcol_cb)
+  const int32_t* grp_ptr;      // [n_grp + 1] their tiles
+  int64_t n_grp;
+  int N, H;
+  float qmul;                  // scale * log2(e)
+  float scale;
+  const float* lse;            // [N, H]
+  const float* delta;          // [N, H]
+  void* g1;                    // bf16: row kernel dQ, column kernel dK (residual in, sum out)
+  void* g2;                    // bf16: column kernel dV
+  int32_t* err;
+};
+
+// Launch the row (dQ) or column (dK, dV) tile backward, D = 64 or 128,
+// after the residual pass of the same side.
+gattn_status launch_tile_bwd(const TileBwdParams& p, int D, bool col, int num_sms, cudaStream_t st);
+
 // Tensor map of a [rows, width] bf16 matrix read in 64-column x 128-row
 // boxes with the 128-byte swizzle (the tensor cores' operand layout).
 bool encode_tile_map(CUtensorMap* map, const void* base, int64_t rows, int64_t width);

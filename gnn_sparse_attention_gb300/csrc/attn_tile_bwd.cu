@@ -1,0 +1,410 @@
+// attn_tile_bwd.cu -- dense-tile backward on the tensor cores (tcgen05 + TMEM).
+//
+// "On Efficient Scaling of GNNs via IO-Aware Layers Implementations", zh/ko
+// technical summaries, "Methodology", attention-based layers: the backward
+// pass recomputes the attention weights from the cached log-sum-exp, and
+// locally dense neighbourhoods packed into block tiles become dense matrix
+// products on the tensor cores.
+//
+// For the edges of a tile (row block I, column block J, bit mask), with
+// p_ij = exp(s_ij - lse_i) and ds_ij = p_ij (dO_i . v_j - Delta_i):
+//   row kernel    (one row block at a time):    dQ_I += scale * dS K_J
+//   column kernel (one column block at a time): dV_J += P^T dO_I
+//                                               dK_J += scale * dS^T Q_I
+// Both recompute their 128 x 128 block of scores and of dO . v on the
+// tensor cores -- the row kernel S = Q K^T and dP = dO V^T, the column
+// kernel the transposes S^T = K Q^T and dP^T = V dO^T, so that thread r
+// always owns TMEM lane r, row r of its own block -- form p and ds in fp32
+// from the forward's lse and the destination's Delta (written by the
+// residual CSR pass), store them as bf16 operand tiles in shared memory (the
+// 128-byte swizzled K-major layout the TMA loads use) and issue the
+// gradient products.  The residual passes (CSR for dQ, CSC for dK and dV,
+// over the edges outside the tiles) run first and write every row; the tile
+// kernels add their part in fp32 and round the sum to bf16.
+//
+// Schedule: one CTA per SM walks its blocks (grid stride), the heads, and
+// the block's tiles.  With two operand slots (D = 64) the next step's TMA
+// loads (four 128 x D operand tiles and the 2 KB mask) are in flight while
+// the current step computes.  TMEM holds S [0, 128), dP [128, 256) and the
+// gradient accumulators from column 256 (row kernel dQ; column kernel dV,
+// then dK), which sum over the tiles of a block and head.  Every mbarrier
+// wait is bounded; a wait that gives up sets the plan's error word, the
+// block drains what it issued (again bounded), frees its TMEM and returns.
+#include <cuda.h>
+
+#include "attn_pipe.cuh"
+#include "attn_tile.cuh"
+#include "tcgen05.cuh"
+
+namespace gattn {
+
+namespace {
+
+constexpr int kT = kTileRows;        // rows / columns of a tile
+constexpr int kThr = 128;            // one thread per row of the own block
+constexpr int kTB = kT * 128;        // one 128 x 64 bf16 operand tile (16 KB)
+constexpr int kMaskB = kT * 16;      // 128 rows x 4 mask words
+constexpr uint32_t kCols = 512;      // TMEM columns
+
+// Shared memory of one CTA: NS operand slots [A0 A1 B0 B1 mask], the
+// thread-written operand tiles, the other block's statistics (column
+// kernel) and the barriers.
+template <int D, int NS, bool COL>
+struct BwdSmem {
+  static constexpr int KB = D / 64;                     // 64-column pieces of a head
+  static constexpr int A0 = 0;                          // own block:   Q (row) / K (column)
+  static constexpr int A1 = KB * kTB;                   // own block:   dO (row) / V (column)
+  static constexpr int B0 = 2 * KB * kTB;               // other block: K (row) / Q (column)
+  static constexpr int B1 = 3 * KB * kTB;               // other block: V (row) / dO (column)
+  static constexpr int MASK = 4 * KB * kTB;
+  static constexpr int SLOT = MASK + kMaskB;
+  static constexpr int W0 = NS * SLOT;                  // dS (row) / P^T (column)
+  static constexpr int W1 = W0 + 2 * kTB;               // dS^T (column)
+  static constexpr int STAT = W1 + (COL ? 2 * kTB : 0); // lse * log2(e), Delta of the other block
+  static constexpr int BAR = STAT + (COL ? 2 * kT * 4 : 0);
+  static constexpr int END = BAR + 64;
+  static constexpr int BYTES = END + 1024;              // slack to align the base to 1024
+  static_assert(SLOT % 1024 == 0 && W0 % 1024 == 0, "swizzled tiles start on 1024-byte boundaries");
+  static_assert(BYTES <= 227 * 1024, "shared memory of one CTA");
+};
+
+// One step: block list entry g, head h, position q in the block's tile list.
+struct Step {
+  int g, h, q;
+};
+
+__device__ __forceinline__ Step step_begin(const TileBwdParams& p, int64_t g) {
+  return Step{int(g), 0, g < p.n_grp ? p.grp_ptr[g] : 0};
+}
+
+__device__ __forceinline__ Step step_next(const TileBwdParams& p, const Step& c) {
+  if (c.q + 1 < p.grp_ptr[c.g + 1]) return Step{c.g, c.h, c.q + 1};
+  if (c.h + 1 < p.H) return Step{c.g, c.h + 1, p.grp_ptr[c.g]};
+  return step_begin(p, int64_t(c.g) + gridDim.x);
+}
+
+// out = acc * mul + residual (8 bf16 values)
+__device__ __forceinline__ uint4 add_rounded(const float* acc, float mul, uint4 res) {
+  const uint32_t in[4] = {res.x, res.y, res.z, res.w};
+  uint32_t w[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float r0 = __uint_as_float(in[q] << 16), r1 = __uint_as_float(in[q] & 0xffff0000u);
+    w[q] = tc::bf16x2_bits(fmaf(acc[2 * q], mul, r0), fmaf(acc[2 * q + 1], mul, r1));
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+}  // namespace
+
+template <int D, int NS, bool COL>
+__global__ void __launch_bounds__(kThr, 1) tile_bwd_kernel(const __grid_constant__ TileBwdParams p) {
+  using namespace tc;
+  using SM = BwdSmem<D, NS, COL>;
+  constexpr int KB = SM::KB;
+  constexpr int RV = D / 8;                           // 16-byte pieces of a head row
+  constexpr uint32_t IDESC_S = f16_idesc(kT, kT, false);
+  constexpr uint32_t IDESC_G = f16_idesc(kT, 64, true);  // one 64-column piece of a gradient
+  constexpr uint32_t LOAD_BYTES = 4 * KB * kTB + kMaskB;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint64_t* barL = reinterpret_cast<uint64_t*>(smem + SM::BAR);  // [2] operand slots
+  uint64_t* barS = barL + 2;
+  uint64_t* barD = barL + 3;
+  uint32_t* sTmem = reinterpret_cast<uint32_t*>(barL + 4);
+  float* sL = reinterpret_cast<float*>(smem + SM::STAT);  // column kernel only
+  float* sDl = sL + kT;
+
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if (tid == 0) {
+#pragma unroll
+    for (int s = 0; s < NS; ++s) mbar_init(barL + s, 1);
+    mbar_init(barS, 1);
+    mbar_init(barD, 1);
+    mbar_init_fence();
+  }
+  if (warp == 0) {
+    asm volatile(
+        "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
+            smem_u32(sTmem)),
+        "r"(kCols)
+        : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *sTmem;
+  const uint32_t tS = tmem, tP = tmem + kT, tG = tmem + 2 * kT, tG2 = tmem + 2 * kT + D;
+  const uint32_t lane_off = uint32_t(warp * 32) << 16;  // this warp's TMEM lane quarter
+
+  // TMA loads of one step into slot s (thread 0)
+  auto issue = [&](const Step& c, int s) {
+    uint8_t* sl = smem + s * SM::SLOT;
+    const int tile = p.list ? p.list[c.q] : c.q;
+    const int own = p.grp_blk[c.g], oth = p.tile_other[tile];
+    fence_proxy_async();
+    mbar_expect_tx(barL + s, LOAD_BYTES);
+#pragma unroll
+    for (int kb = 0; kb < KB; ++kb) {
+      const int x = c.h * D + kb * 64;
+      tma_tile2d(sl + SM::A0 + kb * kTB, &p.ma0, x, own * kT, barL + s);
+      tma_tile2d(sl + SM::A1 + kb * kTB, &p.ma1, x, own * kT, barL + s);
+      tma_tile2d(sl + SM::B0 + kb * kTB, &p.mb0, x, oth * kT, barL + s);
+      tma_tile2d(sl + SM::B1 + kb * kTB, &p.mb1, x, oth * kT, barL + s);
+    }
+    bulk_g2s(sl + SM::MASK, p.mask + int64_t(tile) * kT * 4, kMaskB, barL + s);
+  };
+
+  // barrier phases: bit s of phL = parity of slot s's next completion;
+  // bit s of pendL = a load into slot s is in flight
+  uint32_t phL = 0, pendL = 0, nS = 0, nD = 0;
+  bool pendS = false, pendD = false;
+  bool bad = false;
+
+  Step cur = step_begin(p, blockIdx.x);
+  if (cur.g < p.n_grp) {
+    if (tid == 0) issue(cur, 0);
+    pendL = 1u;
+  }
+  for (int k = 0; cur.g < p.n_grp; ++k) {
+    const int s = NS == 2 ? (k & 1) : 0;
+    const Step nxt = step_next(p, cur);
+    const bool more = nxt.g < p.n_grp;
+    const bool first = cur.q == p.grp_ptr[cur.g];
+    const bool last = cur.q + 1 == p.grp_ptr[cur.g + 1];
+    const int node = p.grp_blk[cur.g] * kT + tid;  // this thread's row of the own block
+    if constexpr (NS == 2) {
+      if (more) {
+        if (tid == 0) issue(nxt, s ^ 1);  // slot s ^ 1 was released by the previous step
+        pendL |= 1u << (s ^ 1);
+      }
+    }
+    // statistics: the row kernel's own row; the column kernel's 128 other rows
+    float lse2 = 0.f, dl = 0.f;
+    if constexpr (COL) {
+      const int i = p.tile_other[p.list[cur.q]] * kT + tid;
+      float a = 0.f, b = 0.f;
+      if (i < p.N) {
+        a = p.lse[int64_t(i) * p.H + cur.h] * kLog2e;
+        b = p.delta[int64_t(i) * p.H + cur.h];
+      }
+      sL[tid] = a;
+      sDl[tid] = b;
+    } else {
+      if (node < p.N) {
+        lse2 = p.lse[int64_t(node) * p.H + cur.h] * kLog2e;
+        dl = p.delta[int64_t(node) * p.H + cur.h];
+      }
+    }
+    bool ok = mbar_wait(barL + s, (phL >> s) & 1u);
+    if (__syncthreads_or(!ok)) { bad = true; break; }
+    phL ^= 1u << s;
+    pendL &= ~(1u << s);
+
+    // ---- S and dP (row kernel: Q K^T, dO V^T; column kernel: K Q^T, V dO^T)
+    const uint8_t* sl = smem + s * SM::SLOT;
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int k2 = 0; k2 < D / 16; ++k2) {
+        const int kb = k2 / 4, ko = (k2 % 4) * 32;
+        mma_bf16(tS, sw128_desc(smem_u32(sl + SM::A0 + kb * kTB) + ko, 16, 1024),
+                 sw128_desc(smem_u32(sl + SM::B0 + kb * kTB) + ko, 16, 1024), IDESC_S, k2 > 0);
+        mma_bf16(tP, sw128_desc(smem_u32(sl + SM::A1 + kb * kTB) + ko, 16, 1024),
+                 sw128_desc(smem_u32(sl + SM::B1 + kb * kTB) + ko, 16, 1024), IDESC_S, k2 > 0);
+      }
+      mma_commit(barS);
+    }
+    pendS = true;
+    ok = mbar_wait(barS, nS & 1);
+    if (__syncthreads_or(!ok)) { bad = true; break; }
+    ++nS;
+    pendS = false;
+    tc_fence_after();
+
+    // ---- p and ds of row `tid` -> bf16 operand tiles
+    {
+      const uint32_t* sMask = reinterpret_cast<const uint32_t*>(sl + SM::MASK);
+      uint8_t* wds = smem + (COL ? SM::W1 : SM::W0);
+      uint8_t* wp = smem + SM::W0;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float sv[32], dv[32];
+        tmem_ld32(tS + lane_off + c * 32, sv);
+        tmem_ld32(tP + lane_off + c * 32, dv);
+        tmem_wait_ld();
+        const uint32_t mw = sMask[tid * 4 + c];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t wd[4], wq[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j0 = q * 8 + 2 * e, j1 = j0 + 1;
+            const float L0 = COL ? sL[c * 32 + j0] : lse2, L1 = COL ? sL[c * 32 + j1] : lse2;
+            const float D0 = COL ? sDl[c * 32 + j0] : dl, D1 = COL ? sDl[c * 32 + j1] : dl;
+            const float p0 = ((mw >> j0) & 1u) ? ex2(fmaf(sv[j0], p.qmul, -L0)) : 0.f;
+            const float p1 = ((mw >> j1) & 1u) ? ex2(fmaf(sv[j1], p.qmul, -L1)) : 0.f;
+            wd[e] = bf16x2_bits(p0 * (dv[j0] - D0), p1 * (dv[j1] - D1));
+            if (COL) wq[e] = bf16x2_bits(p0, p1);
+          }
+          // 8-column piece c8 of the row: tile c8 / 8, swizzled 16-byte chunk (c8 % 8) ^ (row % 8)
+          const int c8 = c * 4 + q;
+          const int off = (c8 / 8) * kTB + tid * 128 + (((c8 % 8) ^ (tid & 7)) * 16);
+          *reinterpret_cast<uint4*>(wds + off) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+          if (COL) *reinterpret_cast<uint4*>(wp + off) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+        }
+      }
+    }
+    fence_proxy_async();  // generic stores of the operand tiles -> visible to the tensor cores
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- gradient products (K = the 128 columns of the tile)
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int k2 = 0; k2 < kT / 16; ++k2) {
+        const uint32_t acc = (!first || k2 > 0) ? 1u : 0u;
+        const int aoff = (k2 / 4) * kTB + (k2 % 4) * 32;
+        const uint64_t a0 = sw128_desc(smem_u32(smem + SM::W0 + aoff), 16, 1024);
+#pragma unroll
+        for (int kb = 0; kb < KB; ++kb) {
+          // other-block operand, MN-major: 16 rows (K) = two 1024-byte swizzle atoms per step
+          const int boff = kb * kTB + k2 * 2048;
+          if (!COL) {
+            mma_bf16(tG + kb * 64, a0, sw128_desc(smem_u32(sl + SM::B0 + boff), 1024, 1024),
+                     IDESC_G, acc);                                     // dQ += dS K
+          } else {
+            mma_bf16(tG + kb * 64, a0, sw128_desc(smem_u32(sl + SM::B1 + boff), 1024, 1024),
+                     IDESC_G, acc);                                     // dV += P^T dO
+          }
+        }
+        if (COL) {
+          const uint64_t a1 = sw128_desc(smem_u32(smem + SM::W1 + aoff), 16, 1024);
+#pragma unroll
+          for (int kb = 0; kb < KB; ++kb)
+            mma_bf16(tG2 + kb * 64, a1,
+                     sw128_desc(smem_u32(sl + SM::B0 + kb * kTB + k2 * 2048), 1024, 1024), IDESC_G,
+                     acc);                                              // dK += dS^T Q
+        }
+      }
+      mma_commit(barD);
+    }
+    pendD = true;
+
+    // residual rows of the epilogue, fetched while the products run (the
+    // column kernel with D = 128 reads dK's after writing dV)
+    constexpr bool PRE_K = COL && D <= 64;
+    const bool live = last && node < p.N;
+    const int64_t row = (int64_t(node) * p.H + cur.h) * D;
+    uint4 r1[RV], rk[COL ? RV : 1];
+    if (live) {
+      const uint4* g = reinterpret_cast<const uint4*>(
+          static_cast<const __nv_bfloat16*>(COL ? p.g2 : p.g1) + row);
+#pragma unroll
+      for (int c = 0; c < RV; ++c) r1[c] = g[c];
+      if constexpr (PRE_K) {
+        const uint4* gk = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.g1) + row);
+#pragma unroll
+        for (int c = 0; c < RV; ++c) rk[c] = gk[c];
+      }
+    }
+    ok = mbar_wait(barD, nD & 1);
+    if (__syncthreads_or(!ok)) { bad = true; break; }
+    ++nD;
+    pendD = false;
+    tc_fence_after();
+
+    if constexpr (NS == 1) {
+      if (more) {
+        if (tid == 0) issue(nxt, 0);  // the slot is free: both products have completed
+        pendL |= 1u;
+      }
+    }
+
+    // ---- epilogue after the block's last tile of this head
+    if (last) {
+      // row kernel: dQ = scale * acc + residual; column kernel: dV = acc + residual
+      uint4* o1 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(COL ? p.g2 : p.g1) + row);
+      const float m1 = COL ? 1.f : p.scale;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        float a[32];
+        tmem_ld32(tG + lane_off + c * 32, a);
+        tmem_wait_ld();
+        if (live) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) o1[c * 4 + q] = add_rounded(a + 8 * q, m1, r1[c * 4 + q]);
+        }
+      }
+      if constexpr (COL) {  // dK = scale * acc + residual
+        uint4* o2 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.g1) + row);
+        if constexpr (!PRE_K) {
+          if (live) {
+#pragma unroll
+            for (int c = 0; c < RV; ++c) rk[c] = o2[c];
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          float a[32];
+          tmem_ld32(tG2 + lane_off + c * 32, a);
+          tmem_wait_ld();
+          if (live) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) o2[c * 4 + q] = add_rounded(a + 8 * q, p.scale, rk[c * 4 + q]);
+          }
+        }
+      }
+    }
+    cur = nxt;
+  }
+
+  if (bad && tid == 0) {
+    atomicOr(p.err, 2);
+    // drain what this block issued (bounded), then free the TMEM
+#pragma unroll
+    for (int s = 0; s < NS; ++s)
+      if ((pendL >> s) & 1u) mbar_wait(barL + s, (phL >> s) & 1u);
+    if (pendS) mbar_wait(barS, nS & 1);
+    if (pendD) mbar_wait(barD, nD & 1);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kCols)
+                 : "memory");
+}
+
+gattn_status launch_tile_bwd(const TileBwdParams& p, int D, bool col, int num_sms,
+                             cudaStream_t st) {
+  if (p.n_grp <= 0) return GATTN_OK;
+  if (D != 64 && D != 128) {
+    set_error("the dense-tile backward supports D = 64 or 128 (got %d)", D);
+    return GATTN_ERR_UNSUPPORTED;
+  }
+  const unsigned grid = (unsigned)(p.n_grp < num_sms ? p.n_grp : num_sms);
+  auto go = [&](auto kern, int bytes) -> gattn_status {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) {
+      set_error("tile backward attribute: %s", cudaGetErrorString(e));
+      return GATTN_ERR_CUDA;
+    }
+    kern<<<grid, kThr, bytes, st>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) {
+      set_error("tile backward launch: %s", cudaGetErrorString(e));
+      return GATTN_ERR_CUDA;
+    }
+    return GATTN_OK;
+  };
+  if (D == 64)
+    return col ? go(tile_bwd_kernel<64, 2, true>, BwdSmem<64, 2, true>::BYTES)
+               : go(tile_bwd_kernel<64, 2, false>, BwdSmem<64, 2, false>::BYTES);
+  return col ? go(tile_bwd_kernel<128, 1, true>, BwdSmem<128, 1, true>::BYTES)
+             : go(tile_bwd_kernel<128, 1, false>, BwdSmem<128, 1, false>::BYTES);
+}
+
+}  // namespace gattn

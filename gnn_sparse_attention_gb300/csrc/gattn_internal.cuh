@@ -63,7 +63,7 @@ struct Plan {
   // a tile, listed in (row block, column block) order with its bit mask
   // (bit j % 128 of row i % 128: 4 words a row).  Edges outside the tiles
   // (and repeated pairs inside them) form the residual CSR, which has its
-  // own forward split; the backward always runs on the full graph.
+  // own forward split.
   int32_t tile_min = 0;
   int64_t n_tiles = 0, n_trows = 0, M_res = 0;
   int32_t* tile_rb = nullptr;     // [n_tiles]
@@ -82,6 +82,23 @@ struct Plan {
   int32_t* parent_r = nullptr;
   int2* kids_r = nullptr;
   int32_t* cnt_fwd_r = nullptr;   // [n_inner_r]
+  int32_t* cnt_dq_r = nullptr;    // [n_inner_r]
+  // backward of a tiled plan: tiles by column block (transposed masks: bit
+  // i % 128 of column j % 128, 4 words a column) and the residual CSC with
+  // its own source split
+  int64_t n_tcols = 0;
+  int32_t* tcol_cb = nullptr;       // [n_tcols] column blocks that have tiles
+  int32_t* tcol_ptr = nullptr;      // [n_tcols + 1] their tiles in tcol_tile
+  int32_t* tcol_tile = nullptr;     // [n_tiles] tile ids by (column block, row block)
+  uint32_t* tile_mask_t = nullptr;  // [n_tiles][128][4]
+  int32_t* indptrT_r = nullptr;     // [N+1]
+  int32_t* csc_dst_r = nullptr;     // [M_res] destination of each residual CSC position
+  int64_t n_light_src_r = 0, n_chunks_src_r = 0, n_inner_src_r = 0;
+  int4* items_src_r = nullptr;
+  int4* sorted_src_r = nullptr;
+  int32_t* parent_src_r = nullptr;
+  int2* kids_src_r = nullptr;
+  int32_t* cnt_dkv_r = nullptr;     // [n_inner_src_r]
   // last-arriver counters (zero between calls; the merging warp resets them)
   int32_t* cnt_fwd = nullptr;  // [n_inner]
   int32_t* cnt_dq = nullptr;   // [n_inner]

@@ -531,6 +531,31 @@ __global__ void k_trow_fill(const int32_t* __restrict__ tile_rb, const int32_t* 
     }
 }
 
+// Transposed tile masks: bit i % 128 of column j % 128 (4 words a column),
+// for the backward pass that walks a tile by source column.  One block of
+// 128 threads per tile; thread j assembles column j.
+__global__ void k_mask_transpose(const uint32_t* __restrict__ mask, uint32_t* __restrict__ mask_t) {
+  __shared__ uint32_t s_m[kTileRows * 4];
+  const int64_t base = int64_t(blockIdx.x) * kTileRows * 4;
+  for (int w = threadIdx.x; w < kTileRows * 4; w += blockDim.x) s_m[w] = mask[base + w];
+  __syncthreads();
+  for (int j = threadIdx.x; j < kTileRows; j += blockDim.x) {
+    uint32_t col[4] = {0u, 0u, 0u, 0u};
+    for (int i = 0; i < kTileRows; ++i)
+      col[i / 32] |= ((s_m[i * 4 + j / 32] >> (j % 32)) & 1u) << (i % 32);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) mask_t[base + j * 4 + w] = col[w];
+  }
+}
+
+// tcol_cb[c] = column block of the c-th column group (its first sorted key)
+__global__ void k_group_keys(const int32_t* __restrict__ start, int64_t n_groups,
+                             const int32_t* __restrict__ skey, int32_t* __restrict__ blk) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t c = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; c < n_groups; c += stride)
+    blk[c] = skey[start[c]];
+}
+
 int grid_1d(int64_t n, int num_sms) {
   const int64_t want = (n + kThreads - 1) / kThreads;
   const int64_t cap = int64_t(num_sms) * 8;
@@ -568,6 +593,39 @@ gattn_status radix_sort(int32_t* keys, int32_t* vals, int64_t n, int bits, Scrat
   }
   *vout_final = vin;
   if (kout_final) *kout_final = kin;
+  return GATTN_OK;
+}
+
+// Transpose of a CSR (row pointer ptr, sources idx, M edges): the column
+// pointer ptrT [N+1] and, per CSC position, the CSR edge id (eid [M]) and
+// its destination row (dst [M]).  A stable LSD radix sort of the edge ids
+// keyed by source keeps every column in CSR edge order.
+gattn_status build_csc(const Plan* p, const int32_t* ptr, const int32_t* idx, int64_t M,
+                       Scratch& scr, cudaStream_t st, int32_t* ptrT, int32_t* eid, int32_t* dst) {
+  const int32_t N = p->N;
+  int32_t* counts = nullptr;
+  GATTN_CUDA(scr.get(&counts, N + 1));
+  GATTN_CUDA(cudaMemsetAsync(counts, 0, (N + 1) * sizeof(int32_t), st));
+  if (M) {
+    k_count_sources<<<grid_1d(M, p->num_sms), kThreads, 0, st>>>(idx, M, counts);
+    GATTN_CUDA(cudaGetLastError());
+  }
+  gattn_status r;
+  if ((r = exclusive_scan(counts, ptrT, N + 1, scr, st)) != GATTN_OK) return r;
+  if (M) {
+    int32_t *ka, *va, *sorted_eid;
+    GATTN_CUDA(scr.get(&ka, M));
+    GATTN_CUDA(scr.get(&va, M));
+    GATTN_CUDA(cudaMemcpyAsync(ka, idx, M * sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
+    k_iota<<<grid_1d(M, p->num_sms), kThreads, 0, st>>>(va, M);
+    GATTN_CUDA(cudaGetLastError());
+    int bits = 1;
+    while (bits < 31 && (int64_t(1) << bits) < N) ++bits;
+    if ((r = radix_sort(ka, va, M, bits, scr, st, &sorted_eid)) != GATTN_OK) return r;
+    GATTN_CUDA(cudaMemcpyAsync(eid, sorted_eid, M * sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
+    k_edge_rows<<<grid_1d(M, p->num_sms), kThreads, 0, st>>>(ptr, N, eid, M, dst);
+    GATTN_CUDA(cudaGetLastError());
+  }
   return GATTN_OK;
 }
 
@@ -776,6 +834,72 @@ gattn_status tile_build(Plan* p, Scratch& scr, cudaStream_t st) {
   p->n_inner_r = rs.n_inner;
   GATTN_CUDA(plan_alloc(p, &p->cnt_fwd_r, rs.n_inner));
   GATTN_CUDA(cudaMemsetAsync(p->cnt_fwd_r, 0, (rs.n_inner ? rs.n_inner : 1) * 4, st));
+  GATTN_CUDA(plan_alloc(p, &p->cnt_dq_r, rs.n_inner));
+  GATTN_CUDA(cudaMemsetAsync(p->cnt_dq_r, 0, (rs.n_inner ? rs.n_inner : 1) * 4, st));
+  // residual CSC (backward dK / dV outside the tiles) and its source split
+  {
+    int32_t* reid;
+    GATTN_CUDA(scr.get(&reid, mres));
+    GATTN_CUDA(plan_alloc(p, &p->indptrT_r, int64_t(N) + 1));
+    GATTN_CUDA(plan_alloc(p, &p->csc_dst_r, mres));
+    if ((r = build_csc(p, p->indptr_r, p->indices_r, mres, scr, st, p->indptrT_r, reid,
+                       p->csc_dst_r)) != GATTN_OK)
+      return r;
+    Side ss{};
+    if ((r = build_side(p, p->indptrT_r, scr, st, &ss)) != GATTN_OK) return r;
+    p->items_src_r = ss.items;
+    p->sorted_src_r = ss.sorted;
+    p->parent_src_r = ss.parent;
+    p->kids_src_r = ss.kids;
+    p->n_light_src_r = ss.n_light;
+    p->n_chunks_src_r = ss.n_chunks;
+    p->n_inner_src_r = ss.n_inner;
+    GATTN_CUDA(plan_alloc(p, &p->cnt_dkv_r, ss.n_inner));
+    GATTN_CUDA(cudaMemsetAsync(p->cnt_dkv_r, 0, (ss.n_inner ? ss.n_inner : 1) * 4, st));
+  }
+  // tiles by column block (stable sort of the tile ids by column block, so
+  // each column lists its tiles by row block) and the transposed masks
+  GATTN_CUDA(plan_alloc(p, &p->tcol_tile, n_tiles));
+  GATTN_CUDA(plan_alloc(p, &p->tile_mask_t, int64_t(n_tiles) * kTileRows * 4));
+  int32_t n_tcols = 0;
+  if (n_tiles > 0) {
+    int32_t *ck, *cv, *sid, *skey, *head, *pos, *start;
+    GATTN_CUDA(scr.get(&ck, n_tiles));
+    GATTN_CUDA(scr.get(&cv, n_tiles));
+    GATTN_CUDA(cudaMemcpyAsync(ck, p->tile_cb, n_tiles * sizeof(int32_t),
+                               cudaMemcpyDeviceToDevice, st));
+    k_iota<<<grid_1d(n_tiles, p->num_sms), kThreads, 0, st>>>(cv, n_tiles);
+    GATTN_CUDA(cudaGetLastError());
+    int bits = 1;
+    while (bits < 31 && (int64_t(1) << bits) < int64_t(nb)) ++bits;
+    if ((r = radix_sort(ck, cv, n_tiles, bits, scr, st, &sid, &skey)) != GATTN_OK) return r;
+    GATTN_CUDA(cudaMemcpyAsync(p->tcol_tile, sid, n_tiles * sizeof(int32_t),
+                               cudaMemcpyDeviceToDevice, st));
+    GATTN_CUDA(scr.get(&head, int64_t(n_tiles) + 1));
+    GATTN_CUDA(scr.get(&pos, int64_t(n_tiles) + 1));
+    k_run_heads<<<grid_1d(int64_t(n_tiles) + 1, p->num_sms), kThreads, 0, st>>>(skey, n_tiles,
+                                                                               head);
+    GATTN_CUDA(cudaGetLastError());
+    if ((r = exclusive_scan(head, pos, int64_t(n_tiles) + 1, scr, st)) != GATTN_OK) return r;
+    GATTN_CUDA(cudaMemcpyAsync(&n_tcols, pos + n_tiles, 4, cudaMemcpyDeviceToHost, st));
+    GATTN_CUDA(cudaStreamSynchronize(st));
+    GATTN_CUDA(plan_alloc(p, &p->tcol_ptr, int64_t(n_tcols) + 1));
+    GATTN_CUDA(plan_alloc(p, &p->tcol_cb, n_tcols));
+    start = p->tcol_ptr;
+    k_run_starts<<<grid_1d(int64_t(n_tiles) + 1, p->num_sms), kThreads, 0, st>>>(head, pos,
+                                                                                n_tiles, start);
+    GATTN_CUDA(cudaGetLastError());
+    k_group_keys<<<grid_1d(n_tcols, p->num_sms), kThreads, 0, st>>>(start, n_tcols, skey,
+                                                                    p->tcol_cb);
+    GATTN_CUDA(cudaGetLastError());
+    k_mask_transpose<<<(unsigned)n_tiles, kTileRows, 0, st>>>(p->tile_mask, p->tile_mask_t);
+    GATTN_CUDA(cudaGetLastError());
+  } else {
+    GATTN_CUDA(plan_alloc(p, &p->tcol_ptr, 1));
+    GATTN_CUDA(plan_alloc(p, &p->tcol_cb, 0));
+    GATTN_CUDA(cudaMemsetAsync(p->tcol_ptr, 0, sizeof(int32_t), st));
+  }
+  p->n_tcols = n_tcols;
   return GATTN_OK;
 }
 
@@ -813,33 +937,12 @@ gattn_status plan_build(Plan* p, const int32_t* indptr, const int32_t* indices, 
   gattn_status r = build_side(p, p->indptr, scr, st, &d);
   if (r != GATTN_OK) return r;
   // 4. transpose: out-degrees -> indptrT -> stable sort of edge ids by source
-  int32_t* counts = nullptr;
-  GATTN_CUDA(scr.get(&counts, N + 1));
-  GATTN_CUDA(cudaMemsetAsync(counts, 0, (N + 1) * sizeof(int32_t), st));
-  if (M) {
-    k_count_sources<<<grid_1d(M, p->num_sms), kThreads, 0, st>>>(p->indices, M, counts);
-    GATTN_CUDA(cudaGetLastError());
-  }
   GATTN_CUDA(plan_alloc(p, &p->indptrT, N + 1));
-  if ((r = exclusive_scan(counts, p->indptrT, N + 1, scr, st)) != GATTN_OK) return r;
   GATTN_CUDA(plan_alloc(p, &p->csc_eid, M));
   GATTN_CUDA(plan_alloc(p, &p->csc_dst, M));
-  if (M) {
-    int32_t *ka, *va, *sorted_eid;
-    GATTN_CUDA(scr.get(&ka, M));
-    GATTN_CUDA(scr.get(&va, M));
-    GATTN_CUDA(cudaMemcpyAsync(ka, p->indices, M * sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
-    k_iota<<<grid_1d(M, p->num_sms), kThreads, 0, st>>>(va, M);
-    GATTN_CUDA(cudaGetLastError());
-    int bits = 1;
-    while (bits < 31 && (int64_t(1) << bits) < N) ++bits;
-    if ((r = radix_sort(ka, va, M, bits, scr, st, &sorted_eid)) != GATTN_OK) return r;
-    GATTN_CUDA(cudaMemcpyAsync(p->csc_eid, sorted_eid, M * sizeof(int32_t),
-                               cudaMemcpyDeviceToDevice, st));
-    k_edge_rows<<<grid_1d(M, p->num_sms), kThreads, 0, st>>>(p->indptr, N, p->csc_eid, M,
-                                                             p->csc_dst);
-    GATTN_CUDA(cudaGetLastError());
-  }
+  if ((r = build_csc(p, p->indptr, p->indices, M, scr, st, p->indptrT, p->csc_eid, p->csc_dst)) !=
+      GATTN_OK)
+    return r;
   // 5. source side
   Side s{};
   if ((r = build_side(p, p->indptrT, scr, st, &s)) != GATTN_OK) return r;

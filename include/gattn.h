@@ -225,6 +225,11 @@ GATTN_API gattn_status gattn_fwd(const gattn_plan* plan, int32_t H, int32_t D, g
  *   dQ, dK, dV: device [N, H, D] in `dtype` (written, not accumulated).
  *   da        : GATv2: device fp32 [H, D] (written), or NULL to skip; DOT: ignored.
  *   workspace : as for gattn_fwd.
+ * With a plan built with tile_enable, the DOT score, bf16 and D = 64 or
+ * 128, each pass runs in two launches: the CSR (CSC) pass over the
+ * residual edges, then the tiles on the tensor cores, which recompute their
+ * score blocks and add their dQ (dK and dV) to the rows the first launch
+ * wrote; otherwise the passes cover every edge.
  */
 GATTN_API gattn_status gattn_bwd(const gattn_plan* plan, int32_t H, int32_t D, gattn_dtype dtype,
                        const void* Q, const void* K, const void* V, const gattn_score* score,

@@ -1,7 +1,8 @@
 """Dense-tile path on the GPU through the C ABI: the device-built tile split
-is bit-exact against the oracle's, and the forward that runs the tiles on the
-tensor cores (plus the residual CSR pass) matches the oracle's softmax
-attention; the backward of a tiled plan runs on the full graph."""
+is bit-exact against the oracle's; the forward and the backward that run the
+tiles on the tensor cores (plus the residual CSR / CSC passes) match the
+oracle's softmax attention and its analytic gradients, and agree with the
+CSR-only path of an untiled plan."""
 import numpy as np
 import pytest
 
@@ -35,6 +36,24 @@ def with_extras(indptr, indices, seed, dup=40, isolate=0.05):
     for i in range(N):
         if r.random() < isolate:
             rows[i] = []
+        r.shuffle(rows[i])
+    ptr = np.zeros(N + 1, np.int64)
+    ptr[1:] = np.cumsum([len(x) for x in rows])
+    return ptr.astype(np.int32), np.array([j for x in rows for j in x], np.int32)
+
+
+def dense_blocks_graph(N, pairs, p, seed, extra=2):
+    """Edges j -> i kept with probability p inside the listed (row block,
+    column block) pairs of 128 ids, plus ``extra`` uniform in-edges per node
+    (repeats allowed): several tiles per row block and per column block."""
+    r = np.random.default_rng(seed)
+    rows = [[] for _ in range(N)]
+    for rb, cb in pairs:
+        j0, j1 = cb * 128, min(cb * 128 + 128, N)
+        for i in range(rb * 128, min(rb * 128 + 128, N)):
+            rows[i].extend((np.nonzero(r.random(j1 - j0) < p)[0] + j0).tolist())
+    for i in range(N):
+        rows[i].extend(r.integers(0, N, extra).tolist())
         r.shuffle(rows[i])
     ptr = np.zeros(N + 1, np.int64)
     ptr[1:] = np.cumsum([len(x) for x in rows])
@@ -147,5 +166,57 @@ def test_sbm1m_tiles_full_size():
         ref = sampled_oracle(case, rows, srcs)
         compare({k: res[k] for k in ("out", "lse", "dQ")}, ref["rows"], TOL["bf16"], rows=rows)
         compare({k: res[k] for k in ("dK", "dV")}, ref["srcs"], TOL["bf16"], rows=srcs)
+    finally:
+        case.close()
+
+
+BLOCK_PAIRS = [(0, 0), (0, 1), (0, 2), (1, 1), (2, 1), (2, 3), (3, 0), (4, 4), (4, 1)]
+
+
+@pytest.mark.parametrize("H,D,p", [(2, 64, 0.3), (1, 128, 0.5), (4, 64, 0.08)])
+def test_tile_backward_several_tiles_per_block(H, D, p):
+    """Row blocks and column blocks with up to four tiles each (the gradient
+    accumulators sum over a block's tiles), a partial last block, repeated
+    edges and random residual edges: forward and backward against the oracle."""
+    ip, ix = dense_blocks_graph(600, BLOCK_PAIRS, p, seed=int(p * 100) + D)
+    case = GpuCase(ip, ix, H, D, "bf16", "dot", seed=7, tile=True)
+    try:
+        info = case.plan.info()
+        want = oracle.tile_plan(ip, ix, info["tile_min_edges"])
+        assert info["n_tiles"] == len(want["tile_rb"]) >= 7
+        compare(case.run(), full_oracle(case), TOL["bf16"])
+    finally:
+        case.close()
+
+
+def test_tile_and_csr_backward_agree():
+    ip, ix = with_extras(*sbm_graph(1500, seed=19), seed=19)
+    a = GpuCase(ip, ix, 2, 64, "bf16", "dot", seed=8, tile=True)
+    b = GpuCase(ip, ix, 2, 64, "bf16", "dot", seed=8)
+    try:
+        ra, rb = a.run(), b.run()
+        for k in ("dQ", "dK", "dV"):
+            assert relerr(to64(ra[k]), to64(rb[k])) < TOL["bf16"], k
+        ref = full_oracle(b)
+        compare(ra, ref, TOL["bf16"])
+        compare(rb, ref, TOL["bf16"])
+    finally:
+        a.close()
+        b.close()
+
+
+def test_tile_backward_is_deterministic():
+    ip, ix = dense_blocks_graph(520, BLOCK_PAIRS[:6], 0.4, seed=3)
+    from gnn_sparse_attention_gb300 import binding as gb
+    case = GpuCase(ip, ix, 2, 64, "bf16", "dot", seed=2, tile=True)
+    try:
+        Q, K, V, G = (case.t[k] for k in ("Q", "K", "V", "dO"))
+        out, lse = gb.gattn_fwd(case.plan, Q, K, V, case.score)
+        g1 = gb.gattn_bwd(case.plan, Q, K, V, out, G, lse, case.score)
+        g2 = gb.gattn_bwd(case.plan, Q, K, V, out, G, lse, case.score)
+        torch.cuda.synchronize()
+        gb.gattn_plan_check_errors(case.plan)
+        for x, y in zip(g1[:3], g2[:3]):
+            assert torch.equal(x, y)
     finally:
         case.close()
