@@ -551,9 +551,7 @@ gattn_status gattn_bwd_dq(const gattn_plan* plan, int32_t H, int32_t D, gattn_dt
       !encode_tile_map(&tp.mb0, K, p.N, HD) || !encode_tile_map(&tp.mb1, V, p.N, HD))
     return GATTN_ERR_CUDA;
   tp.mask = p.tile_mask;
-  tp.tile_other = p.tile_cb;
-  tp.list = nullptr;
-  tp.grp_blk = p.trow_rb;
+  tp.desc = p.tdesc_row;
   tp.grp_ptr = p.trow_ptr;
   tp.n_grp = p.n_trows;
   tp.N = p.N;
@@ -619,9 +617,7 @@ gattn_status gattn_bwd_dkdv(const gattn_plan* plan, int32_t H, int32_t D, gattn_
       !encode_tile_map(&tp.mb0, Q, p.N, HD) || !encode_tile_map(&tp.mb1, dout, p.N, HD))
     return GATTN_ERR_CUDA;
   tp.mask = p.tile_mask_t;
-  tp.tile_other = p.tile_rb;
-  tp.list = p.tcol_tile;
-  tp.grp_blk = p.tcol_cb;
+  tp.desc = p.tdesc_col;
   tp.grp_ptr = p.tcol_ptr;
   tp.n_grp = p.n_tcols;
   tp.N = p.N;

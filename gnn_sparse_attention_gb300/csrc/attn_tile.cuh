@@ -29,10 +29,9 @@ struct TileBwdParams {
   CUtensorMap ma0, ma1;        // own block:   row kernel Q, dO;  column kernel K, V
   CUtensorMap mb0, mb1;        // other block: row kernel K, V;   column kernel Q, dO
   const uint32_t* mask;        // row kernel: tile masks; column kernel: transposed masks
-  const int32_t* tile_other;   // [n_tiles] other block of each tile (tile_cb or tile_rb)
-  const int32_t* list;         // column kernel: tile ids by column (tcol_tile); row kernel: null
-  const int32_t* grp_blk;      // [n_grp] own blocks (trow_rb or tcol_cb)
-  const int32_t* grp_ptr;      // [n_grp + 1] their tiles
+  const int4* desc;            // [n_tiles] per list position: own block, other block, tile
+                               // id, flags (1 first, 2 last tile of the own block)
+  const int32_t* grp_ptr;      // [n_grp + 1] list positions of each own block's tiles
   int64_t n_grp;
   int N, H;
   float qmul;                  // scale * log2(e)

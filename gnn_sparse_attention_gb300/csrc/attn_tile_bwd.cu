@@ -13,8 +13,10 @@
 //                                               dK_J += scale * dS^T Q_I
 // Both recompute their 128 x 128 block of scores and of dO . v on the
 // tensor cores -- the row kernel S = Q K^T and dP = dO V^T, the column
-// kernel the transposes S^T = K Q^T and dP^T = V dO^T, so that thread r
-// always owns TMEM lane r, row r of its own block -- form p and ds in fp32
+// kernel the transposes S^T = K Q^T and dP^T = V dO^T, so that TMEM lane r
+// is always row r of the own block; 16 warps split each lane's 128 columns
+// into four 32-column chunks (a warp reads only its own lane quarter) --
+// form p and ds in fp32
 // from the forward's lse and the destination's Delta (written by the
 // residual CSR pass), store them as bf16 operand tiles in shared memory (the
 // 128-byte swizzled K-major layout the TMA loads use) and issue the
@@ -41,7 +43,9 @@ namespace gattn {
 namespace {
 
 constexpr int kT = kTileRows;        // rows / columns of a tile
-constexpr int kThr = 128;            // one thread per row of the own block
+constexpr int kWarps = 16;           // four warps per TMEM lane quarter
+constexpr int kThr = kWarps * 32;    // thread (row r, chunk c): row r of the own block,
+                                     // columns [32c, 32c + 32) of the 128-wide blocks
 constexpr int kTB = kT * 128;        // one 128 x 64 bf16 operand tile (16 KB)
 constexpr int kMaskB = kT * 16;      // 128 rows x 4 mask words
 constexpr uint32_t kCols = 512;      // TMEM columns
@@ -68,19 +72,24 @@ struct BwdSmem {
   static_assert(BYTES <= 227 * 1024, "shared memory of one CTA");
 };
 
-// One step: block list entry g, head h, position q in the block's tile list.
+// One step: block list entry g, head h, position q in the tile list; q0
+// is the first position of g's tiles and qn that of the CTA's next block
+// (-1 past the end), fetched when the block starts.
 struct Step {
-  int g, h, q;
+  int g, h, q, q0, qn;
 };
 
-__device__ __forceinline__ Step step_begin(const TileBwdParams& p, int64_t g) {
-  return Step{int(g), 0, g < p.n_grp ? p.grp_ptr[g] : 0};
+__device__ __forceinline__ Step step_block(const TileBwdParams& p, int64_t g, int q0) {
+  const int64_t gn = g + gridDim.x;
+  return Step{int(g), 0, q0, q0, gn < p.n_grp ? p.grp_ptr[gn] : -1};
 }
 
-__device__ __forceinline__ Step step_next(const TileBwdParams& p, const Step& c) {
-  if (c.q + 1 < p.grp_ptr[c.g + 1]) return Step{c.g, c.h, c.q + 1};
-  if (c.h + 1 < p.H) return Step{c.g, c.h + 1, p.grp_ptr[c.g]};
-  return step_begin(p, int64_t(c.g) + gridDim.x);
+// The step after c, whose descriptor is d (no loads but the next block's qn).
+__device__ __forceinline__ Step step_after(const TileBwdParams& p, const Step& c, int4 d) {
+  if (!(d.w & 2)) return Step{c.g, c.h, c.q + 1, c.q0, c.qn};
+  if (c.h + 1 < p.H) return Step{c.g, c.h + 1, c.q0, c.q0, c.qn};
+  if (c.qn < 0) return Step{-1, 0, 0, 0, -1};
+  return step_block(p, int64_t(c.g) + gridDim.x, c.qn);
 }
 
 // out = acc * mul + residual (8 bf16 values)
@@ -102,7 +111,6 @@ __global__ void __launch_bounds__(kThr, 1) tile_bwd_kernel(const __grid_constant
   using namespace tc;
   using SM = BwdSmem<D, NS, COL>;
   constexpr int KB = SM::KB;
-  constexpr int RV = D / 8;                           // 16-byte pieces of a head row
   constexpr uint32_t IDESC_S = f16_idesc(kT, kT, false);
   constexpr uint32_t IDESC_G = f16_idesc(kT, 64, true);  // one 64-column piece of a gradient
   constexpr uint32_t LOAD_BYTES = 4 * KB * kTB + kMaskB;
@@ -116,6 +124,10 @@ __global__ void __launch_bounds__(kThr, 1) tile_bwd_kernel(const __grid_constant
   float* sDl = sL + kT;
 
   const int tid = threadIdx.x, warp = tid >> 5;
+  // warp w reads TMEM lanes [32 (w % 4), + 32) (a warp may only touch its
+  // lane quarter) and owns the 32-column chunk cc = w / 4 of those rows
+  const int r = (warp & 3) * 32 + (tid & 31);
+  const int cc = warp >> 2;
   if (tid == 0) {
 #pragma unroll
     for (int s = 0; s < NS; ++s) mbar_init(barL + s, 1);
@@ -136,24 +148,22 @@ __global__ void __launch_bounds__(kThr, 1) tile_bwd_kernel(const __grid_constant
   tc_fence_after();
   const uint32_t tmem = *sTmem;
   const uint32_t tS = tmem, tP = tmem + kT, tG = tmem + 2 * kT, tG2 = tmem + 2 * kT + D;
-  const uint32_t lane_off = uint32_t(warp * 32) << 16;  // this warp's TMEM lane quarter
+  const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;  // this warp's TMEM lane quarter
 
-  // TMA loads of one step into slot s (thread 0)
-  auto issue = [&](const Step& c, int s) {
+  // TMA loads of one step (descriptor d) into slot s (thread 0)
+  auto issue = [&](const Step& c, int4 d, int s) {
     uint8_t* sl = smem + s * SM::SLOT;
-    const int tile = p.list ? p.list[c.q] : c.q;
-    const int own = p.grp_blk[c.g], oth = p.tile_other[tile];
     fence_proxy_async();
     mbar_expect_tx(barL + s, LOAD_BYTES);
 #pragma unroll
     for (int kb = 0; kb < KB; ++kb) {
       const int x = c.h * D + kb * 64;
-      tma_tile2d(sl + SM::A0 + kb * kTB, &p.ma0, x, own * kT, barL + s);
-      tma_tile2d(sl + SM::A1 + kb * kTB, &p.ma1, x, own * kT, barL + s);
-      tma_tile2d(sl + SM::B0 + kb * kTB, &p.mb0, x, oth * kT, barL + s);
-      tma_tile2d(sl + SM::B1 + kb * kTB, &p.mb1, x, oth * kT, barL + s);
+      tma_tile2d(sl + SM::A0 + kb * kTB, &p.ma0, x, d.x * kT, barL + s);
+      tma_tile2d(sl + SM::A1 + kb * kTB, &p.ma1, x, d.x * kT, barL + s);
+      tma_tile2d(sl + SM::B0 + kb * kTB, &p.mb0, x, d.y * kT, barL + s);
+      tma_tile2d(sl + SM::B1 + kb * kTB, &p.mb1, x, d.y * kT, barL + s);
     }
-    bulk_g2s(sl + SM::MASK, p.mask + int64_t(tile) * kT * 4, kMaskB, barL + s);
+    bulk_g2s(sl + SM::MASK, p.mask + int64_t(d.z) * kT * 4, kMaskB, barL + s);
   };
 
   // barrier phases: bit s of phL = parity of slot s's next completion;
@@ -162,41 +172,110 @@ __global__ void __launch_bounds__(kThr, 1) tile_bwd_kernel(const __grid_constant
   bool pendS = false, pendD = false;
   bool bad = false;
 
-  Step cur = step_begin(p, blockIdx.x);
-  if (cur.g < p.n_grp) {
-    if (tid == 0) issue(cur, 0);
-    pendL = 1u;
+  // lse * log2(e) and Delta of row r of the rows a step's scores belong to
+  // (row kernel: the own block; column kernel: the tile's row block)
+  auto stats = [&](const Step& c, int4 d, float& a, float& b) {
+    const int i = (COL ? d.y : d.x) * kT + r;
+    a = 0.f;
+    b = 0.f;
+    if (i < p.N) {
+      a = p.lse[int64_t(i) * p.H + c.h] * kLog2e;
+      b = p.delta[int64_t(i) * p.H + c.h];
+    }
+  };
+  // The epilogue's 32-column pieces: NG gradient tensors (row kernel dQ;
+  // column kernel dV, dK) of D / 32 pieces each; thread chunk cc takes
+  // pieces cc, cc + 4, ...  Piece x is tensor x / (D / 32), columns
+  // 32 (x % (D / 32)) of the head row.
+  constexpr int NG = COL ? 2 : 1;
+  constexpr int NPC = NG * D / 32;
+  constexpr int NPT = (NPC + 3) / 4;  // pieces per thread (at most)
+  auto piece_out = [&](int x) -> __nv_bfloat16* {
+    return static_cast<__nv_bfloat16*>((COL && x < D / 32) ? p.g2 : p.g1);
+  };
+  // residual rows (written by the CSR / CSC pass) of a step's epilogue,
+  // fetched into registers a step ahead
+  uint4 res[NPT][4];
+  auto fetch_res = [&](int own, int h) {
+    const int node = own * kT + r;
+    if (node < p.N) {
+      const int64_t row = (int64_t(node) * p.H + h) * D;
+#pragma unroll
+      for (int j = 0; j < NPT; ++j) {
+        const int x = cc + 4 * j;
+        if (x < NPC) {
+          const uint4* g = reinterpret_cast<const uint4*>(piece_out(x) + row + (x % (D / 32)) * 32);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) res[j][q] = g[q];
+        }
+      }
+    }
+  };
+  // gradient rows of a finished (block, head): row kernel dQ = scale * acc +
+  // residual; column kernel dV = acc + residual, dK = scale * acc + residual
+  auto epilogue = [&](int own, int h) {
+    const int node = own * kT + r;
+    const int64_t row = (int64_t(node) * p.H + h) * D;
+#pragma unroll
+    for (int j = 0; j < NPT; ++j) {
+      const int x = cc + 4 * j;
+      if (x < NPC) {  // warp-uniform: the TMEM load is a whole-warp instruction
+        const int t = x / (D / 32), col = (x % (D / 32)) * 32;
+        float a[32];
+        tmem_ld32((t ? tG2 : tG) + lane_off + col, a);
+        tmem_wait_ld();
+        if (node < p.N) {
+          uint4* o = reinterpret_cast<uint4*>(piece_out(x) + row + col);
+          const float mul = (COL && t == 0) ? 1.f : p.scale;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) o[q] = add_rounded(a + 8 * q, mul, res[j][q]);
+        }
+      }
+    }
+  };
+
+  // Step k: wait for its operands -> S, dP products -> the epilogue of the
+  // previous (block, head), which overlaps those products -> p, ds -> the
+  // gradient products.  Its own epilogue runs in step k + 1.  Descriptors
+  // are loaded two steps ahead and statistics one step ahead, so no
+  // dependent chain of small loads sits on a step's critical path.
+  Step cur{-1, 0, 0, 0, -1}, nx{-1, 0, 0, 0, -1};
+  int4 dc = make_int4(0, 0, 0, 0), dn = make_int4(0, 0, 0, 0);
+  if (blockIdx.x < p.n_grp) {
+    cur = step_block(p, blockIdx.x, p.grp_ptr[blockIdx.x]);
+    dc = p.desc[cur.q];
+    nx = step_after(p, cur, dc);
+    if (nx.g >= 0) dn = p.desc[nx.q];
   }
-  for (int k = 0; cur.g < p.n_grp; ++k) {
+  int done_own = 0, done_h = 0;  // the (block, head) whose epilogue is pending
+  bool pend_epi = false;
+  float nl = 0.f, nd = 0.f;      // statistics of `cur`, fetched a step ahead
+  if (cur.g >= 0) {
+    if (tid == 0) issue(cur, dc, 0);
+    pendL = 1u;
+    stats(cur, dc, nl, nd);
+  }
+  for (int k = 0; cur.g >= 0; ++k) {
     const int s = NS == 2 ? (k & 1) : 0;
-    const Step nxt = step_next(p, cur);
-    const bool more = nxt.g < p.n_grp;
-    const bool first = cur.q == p.grp_ptr[cur.g];
-    const bool last = cur.q + 1 == p.grp_ptr[cur.g + 1];
-    const int node = p.grp_blk[cur.g] * kT + tid;  // this thread's row of the own block
+    const bool more = nx.g >= 0;
+    const Step n2 = more ? step_after(p, nx, dn) : Step{-1, 0, 0, 0, -1};
+    const int4 d2 = n2.g >= 0 ? p.desc[n2.q] : make_int4(0, 0, 0, 0);  // used next step
+    const bool first = dc.w & 1;
+    const bool last = dc.w & 2;
     if constexpr (NS == 2) {
       if (more) {
-        if (tid == 0) issue(nxt, s ^ 1);  // slot s ^ 1 was released by the previous step
+        if (tid == 0) issue(nx, dn, s ^ 1);  // slot s ^ 1 was released by the previous step
         pendL |= 1u << (s ^ 1);
       }
     }
-    // statistics: the row kernel's own row; the column kernel's 128 other rows
-    float lse2 = 0.f, dl = 0.f;
-    if constexpr (COL) {
-      const int i = p.tile_other[p.list[cur.q]] * kT + tid;
-      float a = 0.f, b = 0.f;
-      if (i < p.N) {
-        a = p.lse[int64_t(i) * p.H + cur.h] * kLog2e;
-        b = p.delta[int64_t(i) * p.H + cur.h];
-      }
-      sL[tid] = a;
-      sDl[tid] = b;
-    } else {
-      if (node < p.N) {
-        lse2 = p.lse[int64_t(node) * p.H + cur.h] * kLog2e;
-        dl = p.delta[int64_t(node) * p.H + cur.h];
+    const float lse2 = nl, dl = nd;
+    if constexpr (COL) {  // the previous step's reads of sL / sDl ended before its mid-step barrier
+      if (cc == 0) {
+        sL[r] = lse2;
+        sDl[r] = dl;
       }
     }
+    if (more) stats(nx, dn, nl, nd);
     bool ok = mbar_wait(barL + s, (phL >> s) & 1u);
     if (__syncthreads_or(!ok)) { bad = true; break; }
     phL ^= 1u << s;
@@ -217,43 +296,60 @@ __global__ void __launch_bounds__(kThr, 1) tile_bwd_kernel(const __grid_constant
       mma_commit(barS);
     }
     pendS = true;
+    // the previous (block, head)'s epilogue reads only the gradient columns
+    if (pend_epi) {
+      epilogue(done_own, done_h);
+      pend_epi = false;
+    }
+    if (last) fetch_res(dc.x, cur.h);
     ok = mbar_wait(barS, nS & 1);
     if (__syncthreads_or(!ok)) { bad = true; break; }
     ++nS;
     pendS = false;
     tc_fence_after();
 
-    // ---- p and ds of row `tid` -> bf16 operand tiles
+    // ---- p and ds of row r, columns [32 cc, 32 cc + 32) -> bf16 operand tiles
     {
       const uint32_t* sMask = reinterpret_cast<const uint32_t*>(sl + SM::MASK);
       uint8_t* wds = smem + (COL ? SM::W1 : SM::W0);
       uint8_t* wp = smem + SM::W0;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        float sv[32], dv[32];
-        tmem_ld32(tS + lane_off + c * 32, sv);
-        tmem_ld32(tP + lane_off + c * 32, dv);
-        tmem_wait_ld();
-        const uint32_t mw = sMask[tid * 4 + c];
+      float sv[32], dv[32];
+      tmem_ld32(tS + lane_off + cc * 32, sv);
+      tmem_ld32(tP + lane_off + cc * 32, dv);
+      tmem_wait_ld();
+      const uint32_t mw = sMask[r * 4 + cc];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t wd[4], wq[4];
+      for (int q = 0; q < 4; ++q) {
+        float L[8], Dl[8];
+        if constexpr (COL) {  // statistics of the 8 destination columns
+          const float4* l4 = reinterpret_cast<const float4*>(sL + cc * 32 + q * 8);
+          const float4* d4 = reinterpret_cast<const float4*>(sDl + cc * 32 + q * 8);
+          const float4 la = l4[0], lb = l4[1], da = d4[0], db = d4[1];
+          L[0] = la.x; L[1] = la.y; L[2] = la.z; L[3] = la.w;
+          L[4] = lb.x; L[5] = lb.y; L[6] = lb.z; L[7] = lb.w;
+          Dl[0] = da.x; Dl[1] = da.y; Dl[2] = da.z; Dl[3] = da.w;
+          Dl[4] = db.x; Dl[5] = db.y; Dl[6] = db.z; Dl[7] = db.w;
+        } else {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int j0 = q * 8 + 2 * e, j1 = j0 + 1;
-            const float L0 = COL ? sL[c * 32 + j0] : lse2, L1 = COL ? sL[c * 32 + j1] : lse2;
-            const float D0 = COL ? sDl[c * 32 + j0] : dl, D1 = COL ? sDl[c * 32 + j1] : dl;
-            const float p0 = ((mw >> j0) & 1u) ? ex2(fmaf(sv[j0], p.qmul, -L0)) : 0.f;
-            const float p1 = ((mw >> j1) & 1u) ? ex2(fmaf(sv[j1], p.qmul, -L1)) : 0.f;
-            wd[e] = bf16x2_bits(p0 * (dv[j0] - D0), p1 * (dv[j1] - D1));
-            if (COL) wq[e] = bf16x2_bits(p0, p1);
+          for (int e = 0; e < 8; ++e) {
+            L[e] = lse2;
+            Dl[e] = dl;
           }
-          // 8-column piece c8 of the row: tile c8 / 8, swizzled 16-byte chunk (c8 % 8) ^ (row % 8)
-          const int c8 = c * 4 + q;
-          const int off = (c8 / 8) * kTB + tid * 128 + (((c8 % 8) ^ (tid & 7)) * 16);
-          *reinterpret_cast<uint4*>(wds + off) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-          if (COL) *reinterpret_cast<uint4*>(wp + off) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
         }
+        uint32_t wd[4], wq[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int j0 = q * 8 + 2 * e, j1 = j0 + 1;
+          const float p0 = ((mw >> j0) & 1u) ? ex2(fmaf(sv[j0], p.qmul, -L[2 * e])) : 0.f;
+          const float p1 = ((mw >> j1) & 1u) ? ex2(fmaf(sv[j1], p.qmul, -L[2 * e + 1])) : 0.f;
+          wd[e] = bf16x2_bits(p0 * (dv[j0] - Dl[2 * e]), p1 * (dv[j1] - Dl[2 * e + 1]));
+          if (COL) wq[e] = bf16x2_bits(p0, p1);
+        }
+        // 8-column piece c8 of the row: tile c8 / 8, swizzled 16-byte chunk (c8 % 8) ^ (row % 8)
+        const int c8 = cc * 4 + q;
+        const int off = (c8 / 8) * kTB + r * 128 + (((c8 % 8) ^ (r & 7)) * 16);
+        *reinterpret_cast<uint4*>(wds + off) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+        if (COL) *reinterpret_cast<uint4*>(wp + off) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
       }
     }
     fence_proxy_async();  // generic stores of the operand tiles -> visible to the tensor cores
@@ -292,24 +388,6 @@ __global__ void __launch_bounds__(kThr, 1) tile_bwd_kernel(const __grid_constant
       mma_commit(barD);
     }
     pendD = true;
-
-    // residual rows of the epilogue, fetched while the products run (the
-    // column kernel with D = 128 reads dK's after writing dV)
-    constexpr bool PRE_K = COL && D <= 64;
-    const bool live = last && node < p.N;
-    const int64_t row = (int64_t(node) * p.H + cur.h) * D;
-    uint4 r1[RV], rk[COL ? RV : 1];
-    if (live) {
-      const uint4* g = reinterpret_cast<const uint4*>(
-          static_cast<const __nv_bfloat16*>(COL ? p.g2 : p.g1) + row);
-#pragma unroll
-      for (int c = 0; c < RV; ++c) r1[c] = g[c];
-      if constexpr (PRE_K) {
-        const uint4* gk = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.g1) + row);
-#pragma unroll
-        for (int c = 0; c < RV; ++c) rk[c] = gk[c];
-      }
-    }
     ok = mbar_wait(barD, nD & 1);
     if (__syncthreads_or(!ok)) { bad = true; break; }
     ++nD;
@@ -318,48 +396,21 @@ __global__ void __launch_bounds__(kThr, 1) tile_bwd_kernel(const __grid_constant
 
     if constexpr (NS == 1) {
       if (more) {
-        if (tid == 0) issue(nxt, 0);  // the slot is free: both products have completed
+        if (tid == 0) issue(nx, dn, 0);  // the slot is free: both products have completed
         pendL |= 1u;
       }
     }
-
-    // ---- epilogue after the block's last tile of this head
     if (last) {
-      // row kernel: dQ = scale * acc + residual; column kernel: dV = acc + residual
-      uint4* o1 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(COL ? p.g2 : p.g1) + row);
-      const float m1 = COL ? 1.f : p.scale;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        float a[32];
-        tmem_ld32(tG + lane_off + c * 32, a);
-        tmem_wait_ld();
-        if (live) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) o1[c * 4 + q] = add_rounded(a + 8 * q, m1, r1[c * 4 + q]);
-        }
-      }
-      if constexpr (COL) {  // dK = scale * acc + residual
-        uint4* o2 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.g1) + row);
-        if constexpr (!PRE_K) {
-          if (live) {
-#pragma unroll
-            for (int c = 0; c < RV; ++c) rk[c] = o2[c];
-          }
-        }
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          float a[32];
-          tmem_ld32(tG2 + lane_off + c * 32, a);
-          tmem_wait_ld();
-          if (live) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) o2[c * 4 + q] = add_rounded(a + 8 * q, p.scale, rk[c * 4 + q]);
-          }
-        }
-      }
+      done_own = dc.x;
+      done_h = cur.h;
+      pend_epi = true;
     }
-    cur = nxt;
+    cur = nx;
+    dc = dn;
+    nx = n2;
+    dn = d2;
   }
+  if (!bad && pend_epi) epilogue(done_own, done_h);
 
   if (bad && tid == 0) {
     atomicOr(p.err, 2);

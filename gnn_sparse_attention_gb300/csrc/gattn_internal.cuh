@@ -91,6 +91,11 @@ struct Plan {
   int32_t* tcol_ptr = nullptr;      // [n_tcols + 1] their tiles in tcol_tile
   int32_t* tcol_tile = nullptr;     // [n_tiles] tile ids by (column block, row block)
   uint32_t* tile_mask_t = nullptr;  // [n_tiles][128][4]
+  // step descriptors of the tile backward, per position of the row-order
+  // (tile) list and of the column-order list: (own block, other block,
+  // tile id, 1 = first / 2 = last tile of its own block)
+  int4* tdesc_row = nullptr;        // [n_tiles]
+  int4* tdesc_col = nullptr;        // [n_tiles]
   int32_t* indptrT_r = nullptr;     // [N+1]
   int32_t* csc_dst_r = nullptr;     // [M_res] destination of each residual CSC position
   int64_t n_light_src_r = 0, n_chunks_src_r = 0, n_inner_src_r = 0;

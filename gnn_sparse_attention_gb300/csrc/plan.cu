@@ -548,6 +548,21 @@ __global__ void k_mask_transpose(const uint32_t* __restrict__ mask, uint32_t* __
   }
 }
 
+// Step descriptors of a tile list (order: positions -> tile ids, or null
+// for the tiles themselves): (own block, other block, tile id, flags 1 =
+// first and 2 = last of the list's run of its own block).
+__global__ void k_tile_desc(const int32_t* __restrict__ order, const int32_t* __restrict__ own,
+                            const int32_t* __restrict__ oth, int64_t n, int4* __restrict__ desc) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t q = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; q < n; q += stride) {
+    const int32_t t = order ? order[q] : int32_t(q);
+    const int32_t o = own[t];
+    const bool first = q == 0 || own[order ? order[q - 1] : int32_t(q - 1)] != o;
+    const bool last = q == n - 1 || own[order ? order[q + 1] : int32_t(q + 1)] != o;
+    desc[q] = make_int4(o, oth[t], t, (first ? 1 : 0) | (last ? 2 : 0));
+  }
+}
+
 // tcol_cb[c] = column block of the c-th column group (its first sorted key)
 __global__ void k_group_keys(const int32_t* __restrict__ start, int64_t n_groups,
                              const int32_t* __restrict__ skey, int32_t* __restrict__ blk) {
@@ -893,6 +908,16 @@ gattn_status tile_build(Plan* p, Scratch& scr, cudaStream_t st) {
                                                                     p->tcol_cb);
     GATTN_CUDA(cudaGetLastError());
     k_mask_transpose<<<(unsigned)n_tiles, kTileRows, 0, st>>>(p->tile_mask, p->tile_mask_t);
+    GATTN_CUDA(cudaGetLastError());
+  }
+  GATTN_CUDA(plan_alloc(p, &p->tdesc_row, n_tiles));
+  GATTN_CUDA(plan_alloc(p, &p->tdesc_col, n_tiles));
+  if (n_tiles > 0) {
+    k_tile_desc<<<grid_1d(n_tiles, p->num_sms), kThreads, 0, st>>>(nullptr, p->tile_rb, p->tile_cb,
+                                                                   n_tiles, p->tdesc_row);
+    GATTN_CUDA(cudaGetLastError());
+    k_tile_desc<<<grid_1d(n_tiles, p->num_sms), kThreads, 0, st>>>(p->tcol_tile, p->tile_cb,
+                                                                   p->tile_rb, n_tiles, p->tdesc_col);
     GATTN_CUDA(cudaGetLastError());
   } else {
     GATTN_CUDA(plan_alloc(p, &p->tcol_ptr, 1));
