@@ -73,7 +73,7 @@ struct CsrShape {
   using L = Lay<T, RB, SB>;
   static constexpr int LS = StatBytes<RB>::value;
   // per item slot: Q, dO, O rows and the lse row; per edge: K row, V row
-  static constexpr int OL = 3 * L::QR * RB;             // lse sets
+  static constexpr int OL = 3 * L::IR * RB;             // lse sets
   static constexpr int OK = OL + L::QR / 4 * L::SSB;    // K rows
   static constexpr int OV = OK + L::B * RB;             // V rows
   static constexpr int STAGE = OV + L::B * RB;
@@ -88,7 +88,7 @@ struct CscShape {
   using L = Lay<T, RB, SB>;
   static constexpr int LS = StatBytes<RB>::value;
   // per item slot: K, V rows; per edge: Q row, dO row, lse row, Delta row
-  static constexpr int OQE = 2 * L::QR * RB;            // Q rows of the edges
+  static constexpr int OQE = 2 * L::IR * RB;            // Q rows of the edges
   static constexpr int OGE = OQE + L::B * RB;           // dO rows
   static constexpr int OLS = OGE + L::B * RB;           // lse sets
   static constexpr int ODL = OLS + L::B / 4 * L::SSB;   // Delta sets
@@ -164,11 +164,12 @@ __global__ void __launch_bounds__(CsrShape<T, RB, SB>::THREADS) bwd_csr_kernel(c
   BundleCursor<G, SE> cur;
   cur.start(p.sorted, p.n_items, p.idx, p.N, warp, nwarps, ring.items, lane);
 
-  // stage: [QR][Q row] [QR][dO row] [QR][O row] [QR][lse row] [B][K row]
+  // stage: [IR][Q row] [IR][dO row] [IR][O row] [QR/4][lse set] [B][K row]
   // [B][V row].  TMA gathers from lane 0 (item rows only for 4-row sets that
-  // hold a starting item, pad row N elsewhere); lse rows by gather when
+  // hold a starting item, pad row N elsewhere; with fewer than 4 groups a
+  // warp copies just the starting items' rows); lse rows by gather when
   // they are whole 16-byte pieces, else by 4-byte cp.async.
-  constexpr int OQ = 0, ODO = L::QR * RB, OO = 2 * L::QR * RB;
+  constexpr int OQ = 0, ODO = L::IR * RB, OO = 2 * L::IR * RB;
   constexpr int OL = Sh::OL, OK = Sh::OK, OV = Sh::OV;
   auto issue = [&](int s) {
     const int4* dsc = ring.desc_at(s);
@@ -184,16 +185,24 @@ __global__ void __launch_bounds__(CsrShape<T, RB, SB>::THREADS) bwd_csr_kernel(c
                          qr[q4].w != p.N;
         qmask |= uint32_t(any) << q4;
       }
-      const uint32_t qset = 3 * L::SET_BYTES + (p.rows16 ? 16 * p.H : 0);
+      const uint32_t ibytes = L::IBULK ? item_rows<L>(qr[0], p.N) * 3 * RB
+                                       : __popc(qmask) * 3 * L::SET_BYTES;
       fence_proxy_async();
-      mbar_expect_tx(bar, __popc(qmask) * qset + 2 * (B / 4) * L::SET_BYTES);
+      mbar_expect_tx(bar, ibytes + (p.rows16 ? __popc(qmask) * 16 * p.H : 0) +
+                              2 * (B / 4) * L::SET_BYTES);
 #pragma unroll
       for (int q4 = 0; q4 < L::QR / 4; ++q4)
         if ((qmask >> q4) & 1) {
           const int4 r = qr[q4];
-          L::gather(st + OQ, 4 * q4, &p.mi0, r.x, r.y, r.z, r.w, bar);
-          L::gather(st + ODO, 4 * q4, &p.mi1, r.x, r.y, r.z, r.w, bar);
-          L::gather(st + OO, 4 * q4, &p.mi2, r.x, r.y, r.z, r.w, bar);
+          if constexpr (L::IBULK) {
+            fetch_item_rows<L>(st + OQ, p.Q, r, p.N, bar);
+            fetch_item_rows<L>(st + ODO, p.dO, r, p.N, bar);
+            fetch_item_rows<L>(st + OO, p.O, r, p.N, bar);
+          } else {
+            L::gather(st + OQ, 4 * q4, &p.mi0, r.x, r.y, r.z, r.w, bar);
+            L::gather(st + ODO, 4 * q4, &p.mi1, r.x, r.y, r.z, r.w, bar);
+            L::gather(st + OO, 4 * q4, &p.mi2, r.x, r.y, r.z, r.w, bar);
+          }
           if (p.rows16) tma_gather4(st + OL + q4 * L::SSB, &p.ms0, 0, r.x, r.y, r.z, r.w, bar);
         }
 #pragma unroll
@@ -245,7 +254,7 @@ __global__ void __launch_bounds__(CsrShape<T, RB, SB>::THREADS) bwd_csr_kernel(c
       for (int c = 0; c < NC; ++c) {
         float2 o[PP];
         if (first) {
-          const int x = L::off(g, (t * NC + c) * 16);
+          const int x = L::offI(g, (t * NC + c) * 16);
           PR::load(lds16(st + OQ + x), q[c]);
           PR::load(lds16(st + ODO + x), gq[c]);
           PR::load(lds16(st + OO + x), o);
@@ -494,11 +503,12 @@ __global__ void __launch_bounds__(CscShape<T, RB, SB>::THREADS) bwd_csc_kernel(c
   BundleCursor<G, SE> cur;
   cur.start(p.sorted, p.n_items, p.idx, p.N, warp, nwarps, ring.items, lane);
 
-  // stage: [QR][K row] [QR][V row] [B][Q row] [B][dO row] [B][lse row]
-  // [B][Delta row].  TMA gathers from lane 0 (pad row N in unused slots);
+  // stage: [IR][K row] [IR][V row] [B][Q row] [B][dO row] [B][lse row]
+  // [B][Delta row].  TMA gathers from lane 0 (pad row N in unused slots;
+  // with fewer than 4 groups a warp copies just the starting items' rows);
   // stat rows by gather when they are whole 16-byte pieces, else by 4-byte
   // cp.async.
-  constexpr int OKI = 0, OVI = L::QR * RB;
+  constexpr int OKI = 0, OVI = L::IR * RB;
   constexpr int OQE = Sh::OQE, OGE = Sh::OGE, OLS = Sh::OLS, ODL = Sh::ODL;
   auto issue = [&](int s) {
     const int4* dsc = ring.desc_at(s);
@@ -516,14 +526,21 @@ __global__ void __launch_bounds__(CscShape<T, RB, SB>::THREADS) bwd_csc_kernel(c
       }
       const uint32_t eset =
           2 * L::SET_BYTES + (p.rows16 ? 16 * p.H : 0) + (p.delta16 ? 16 * p.H : 0);
+      const uint32_t ibytes = L::IBULK ? item_rows<L>(qr[0], p.N) * 2 * RB
+                                       : __popc(qmask) * 2 * L::SET_BYTES;
       fence_proxy_async();
-      mbar_expect_tx(bar, __popc(qmask) * 2 * L::SET_BYTES + (B / 4) * eset);
+      mbar_expect_tx(bar, ibytes + (B / 4) * eset);
 #pragma unroll
       for (int q4 = 0; q4 < L::QR / 4; ++q4)
         if ((qmask >> q4) & 1) {
           const int4 r = qr[q4];
-          L::gather(st + OKI, 4 * q4, &p.mi0, r.x, r.y, r.z, r.w, bar);
-          L::gather(st + OVI, 4 * q4, &p.mi1, r.x, r.y, r.z, r.w, bar);
+          if constexpr (L::IBULK) {
+            fetch_item_rows<L>(st + OKI, p.K, r, p.N, bar);
+            fetch_item_rows<L>(st + OVI, p.V, r, p.N, bar);
+          } else {
+            L::gather(st + OKI, 4 * q4, &p.mi0, r.x, r.y, r.z, r.w, bar);
+            L::gather(st + OVI, 4 * q4, &p.mi1, r.x, r.y, r.z, r.w, bar);
+          }
         }
 #pragma unroll
       for (int b4 = 0; b4 < B / 4; ++b4) {
@@ -574,7 +591,7 @@ __global__ void __launch_bounds__(CscShape<T, RB, SB>::THREADS) bwd_csc_kernel(c
     if (act && (d.z & kFirst)) {
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
-        const int x = L::off(g, (t * NC + c) * 16);
+        const int x = L::offI(g, (t * NC + c) * 16);
         PR::load(lds16(st + OKI + x), k[c]);
         PR::load(lds16(st + OVI + x), vv[c]);
 #pragma unroll

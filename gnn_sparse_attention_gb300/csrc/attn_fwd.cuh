@@ -51,8 +51,8 @@ struct FwdParams {
 template <typename T, int RB, int SB>
 struct FwdShape {
   using L = Lay<T, RB, SB>;
-  // Q rows of the G items (QR slots), then B K rows and B V rows
-  static constexpr int STAGE = RB * (L::QR + 2 * L::B);
+  // Q rows of the G items (IR slots), then B K rows and B V rows
+  static constexpr int STAGE = RB * (L::IR + 2 * L::B);
   static constexpr int WARP_BYTES = align128(kStages * STAGE + L::META);
   static constexpr int WARPS = WarpsFor<WARP_BYTES>::value;
   static constexpr int THREADS = 32 * WARPS;
@@ -123,16 +123,22 @@ __global__ void __launch_bounds__(FwdShape<T, RB, SB>::THREADS) fwd_kernel(const
           qmask |= uint32_t(any) << q4;
         }
         fence_proxy_async();
-        mbar_expect_tx(bar, (__popc(qmask) + 2 * (B / 4)) * L::SET_BYTES);
+        const uint32_t ibytes = L::IBULK ? item_rows<L>(qr[0], p.N) * RB
+                                         : __popc(qmask) * L::SET_BYTES;
+        mbar_expect_tx(bar, ibytes + 2 * (B / 4) * L::SET_BYTES);
+        if constexpr (L::IBULK) {
+          fetch_item_rows<L>(st, p.Q, qr[0], p.N, bar);
+        } else {
 #pragma unroll
-        for (int q4 = 0; q4 < L::QR / 4; ++q4)
-          if ((qmask >> q4) & 1)
-            L::gather(st, 4 * q4, &p.mq, qr[q4].x, qr[q4].y, qr[q4].z, qr[q4].w, bar);
+          for (int q4 = 0; q4 < L::QR / 4; ++q4)
+            if ((qmask >> q4) & 1)
+              L::gather(st, 4 * q4, &p.mq, qr[q4].x, qr[q4].y, qr[q4].z, qr[q4].w, bar);
+        }
 #pragma unroll
         for (int b4 = 0; b4 < B / 4; ++b4) {
           const int4 r = ring.eset(s, b4);
-          L::gather(st + L::QR * RB, 4 * b4, &p.mk, r.x, r.y, r.z, r.w, bar);
-          L::gather(st + (L::QR + B) * RB, 4 * b4, &p.mv, r.x, r.y, r.z, r.w, bar);
+          L::gather(st + L::IR * RB, 4 * b4, &p.mk, r.x, r.y, r.z, r.w, bar);
+          L::gather(st + (L::IR + B) * RB, 4 * b4, &p.mv, r.x, r.y, r.z, r.w, bar);
         }
       }
     }
@@ -169,7 +175,7 @@ __global__ void __launch_bounds__(FwdShape<T, RB, SB>::THREADS) fwd_kernel(const
     if (act && (d.z & kFirst)) {
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
-        PR::load(lds16(st + L::off(g, (t * NC + c) * 16)), q[c]);
+        PR::load(lds16(st + L::offI(g, (t * NC + c) * 16)), q[c]);
         if (!GAT) {
 #pragma unroll
           for (int v = 0; v < PP; ++v) q[c][v] = f2mul(q[c][v], f2s(p.qmul));
@@ -184,7 +190,7 @@ __global__ void __launch_bounds__(FwdShape<T, RB, SB>::THREADS) fwd_kernel(const
       }
     }
 
-    const uint8_t* ks = st + L::QR * RB;
+    const uint8_t* ks = st + L::IR * RB;
     const uint8_t* vs = ks + B * RB;
     const int kmax = __reduce_max_sync(FULL, cnt);  // edges of the warp's longest item here
     float sc[SE][HL];

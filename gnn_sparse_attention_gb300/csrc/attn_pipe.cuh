@@ -48,6 +48,7 @@ constexpr int kSmemPerSm = 227 * 1024;
 // picks by the plan's mean item length).
 template <typename T, int RB, int SB>
 struct Lay {
+  static constexpr int RBYTES = RB;                 // bytes of a row
   static constexpr int VEC = 16 / (int)sizeof(T);  // elements per 16-byte chunk
   static constexpr int PT = RB <= 1024 ? 32 : RB / 32;
   static constexpr int NC = PT / 16;                // chunks per thread
@@ -61,7 +62,12 @@ struct Lay {
   static constexpr int SE2 = SE1 * G > 32 ? 32 / G : SE1;  // at most 32 edges per stage
   static constexpr int SE = SE2 * G < 4 ? 4 / G : SE2;     // whole 4-row gathers
   static constexpr int B = G * SE;                  // edges per stage
-  static constexpr int QR = (G + 3) / 4 * 4;        // item-row slots per stage
+  static constexpr int QR = (G + 3) / 4 * 4;        // item-row indices per stage (whole 4-row sets)
+  // Item rows held in a stage: whole 4-row gather sets when a warp holds 4
+  // or more groups; one row per group otherwise, fetched by plain bulk
+  // copies (no zero-filled pad rows taking shared memory).
+  static constexpr bool IBULK = G < 4;
+  static constexpr int IR = IBULK ? G : QR;
   // one gather moves 4 rows of BOXE elements; a row is NCOL such pieces
   static constexpr int HD = RB / (int)sizeof(T);
   static constexpr int BOXE = HD < kGatherBoxMax ? HD : kGatherBoxMax;
@@ -79,6 +85,11 @@ struct Lay {
   __device__ __forceinline__ static int off(int b, int x) {
     if constexpr (NCOL == 1) return b * RB + x;
     else return (b / 4) * 4 * RB + (x / BOXB) * 4 * BOXB + (b % 4) * BOXB + x % BOXB;
+  }
+  // Byte offset of row byte x of item row b (the layout the item rows land in).
+  __device__ __forceinline__ static int offI(int b, int x) {
+    if constexpr (IBULK) return b * RB + x;
+    else return off(b, x);
   }
   // Issue the gathers of rows r0..r3 into a region at row slot b0 (multiple of 4).
   __device__ __forceinline__ static void gather(uint8_t* region, int b0, const CUtensorMap* map,
@@ -177,6 +188,27 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
           smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Item rows of a warp with fewer than 4 groups (Lay::IBULK): group b's row
+// (index q[b], `pad` = none) is copied whole from `base` to region + b * RB.
+template <typename L>
+__device__ __forceinline__ int item_rows(int4 q, int pad) {
+  const int r[4] = {q.x, q.y, q.z, q.w};
+  int n = 0;
+#pragma unroll
+  for (int b = 0; b < L::G; ++b) n += r[b] != pad;
+  return n;
+}
+template <typename L>
+__device__ __forceinline__ void fetch_item_rows(uint8_t* region, const void* base, int4 q, int pad,
+                                                uint64_t* bar) {
+  const int r[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int b = 0; b < L::G; ++b)
+    if (r[b] != pad)
+      bulk_g2s(region + b * L::RBYTES, static_cast<const uint8_t*>(base) + int64_t(r[b]) * L::RBYTES,
+               L::RBYTES, bar);
 }
 
 // ---------------------------------------------------------------------------
