@@ -194,6 +194,7 @@ GRAPH_TEXT = {
     "er1k": "directed Erdos-Renyi graph (avg in-degree 8 + self-loops)",
     "lognormal233k": "lognormal in-degrees (mu 5.5, sigma 1.2)",
     "gatv2_powerlaw2m4": "power-law graph (62M Zipf(2.3) in-edges)",
+    "gatv2_powerlaw600k": "power-law graph (15.5M Zipf(2.3) in-edges)",
     "sbm1m": "stochastic block model (64-node communities, p_in 0.5, 4N inter edges)",
     "sbm256k": "stochastic block model (64-node communities, p_in 0.5, 4N inter edges)",
 }

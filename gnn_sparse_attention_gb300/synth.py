@@ -54,6 +54,10 @@ WORKLOADS = {
     "gatv2_powerlaw2m4": Workload("gatv2_powerlaw2m4", "zipf", 2_400_000, 4, 32, "bf16",
                                   "gatv2", False,
                                   {"alpha": 2.3, "cap": 2_399_999, "edges": 62_000_000}),
+    # The same GATv2 recipe on a quarter of the nodes and edges (profiling-sized case).
+    "gatv2_powerlaw600k": Workload("gatv2_powerlaw600k", "zipf", 600_000, 4, 32, "bf16",
+                                   "gatv2", False,
+                                   {"alpha": 2.3, "cap": 599_999, "edges": 15_500_000}),
     # Stochastic block model, 64-node communities ordered by community.
     "sbm1m": Workload("sbm1m", "sbm", 1 << 20, 8, 64, "bf16", "dot", False,
                       {"block": 64, "p_in": 0.5, "inter_per_node": 4}),
