@@ -25,7 +25,7 @@ GATTN_SCORE_DOT, GATTN_SCORE_GATV2 = 0, 1
 EXPORTED = ("gattn_plan_create", "gattn_plan_destroy", "gattn_plan_get_info",
             "gattn_plan_export", "gattn_workspace_size", "gattn_fwd", "gattn_bwd",
             "gattn_bwd_dq", "gattn_bwd_dkdv", "gattn_plan_check_errors", "gattn_fwd_noalloc",
-            "gattn_plan_export_tiles", "gattn_reorder", "gattn_permute_csr",
+            "gattn_plan_export_tiles", "gattn_plan_export_tile_bwd", "gattn_reorder", "gattn_permute_csr",
             "gattn_permute_rows", "gattn_pool_workspace_size", "gattn_pool_fwd",
             "gattn_pool_bwd", "gattn_spmm_workspace_size", "gattn_spmm", "gattn_last_error",
             "gattn_version")
@@ -98,6 +98,7 @@ def load_library(path: str | None = None):
         lib.gattn_fwd_noalloc.argtypes = [P, i32, i32, ctypes.c_int, P, P, P,
                                           ctypes.POINTER(_Score), P, P, P]
         lib.gattn_plan_export_tiles.argtypes = [P] * 6
+        lib.gattn_plan_export_tile_bwd.argtypes = [P, ctypes.POINTER(i64)] + [P] * 6
         lib.gattn_reorder.argtypes = [P, P, i32, i64, i32, P]
         lib.gattn_permute_csr.argtypes = [P, P, i32, i64, P, P, P]
         lib.gattn_permute_rows.argtypes = [P, P, P, i32, i64, i32, P]
@@ -261,6 +262,28 @@ def gattn_plan_export_tiles(plan: Plan) -> dict:
     order = ("tile_rb", "tile_cb", "masks", "indptr_r", "indices_r")
     ptrs = [arr[k].ctypes.data_as(ctypes.c_void_p) if arr[k].size else None for k in order]
     _check(load_library().gattn_plan_export_tiles(plan.handle, *ptrs), "gattn_plan_export_tiles")
+    return arr
+
+
+def gattn_plan_export_tile_bwd(plan: Plan) -> dict:
+    """Structures of the tile backward: tiles by column block, transposed
+    masks, and the residual CSC."""
+    info = gattn_plan_get_info(plan)
+    nt, N = info["n_tiles"], info["N"]
+    lib = load_library()
+    n = ctypes.c_int64(0)
+    _check(lib.gattn_plan_export_tile_bwd(plan.handle, ctypes.byref(n), *([None] * 6)),
+           "gattn_plan_export_tile_bwd")
+    nc = int(n.value)
+    arr = {
+        "tcol_cb": np.zeros(nc, np.int32), "tcol_ptr": np.zeros(nc + 1, np.int32),
+        "tcol_tile": np.zeros(nt, np.int32), "masks_t": np.zeros((nt, 128, 4), np.uint32),
+        "indptrT_r": np.zeros(N + 1, np.int32),
+        "csc_dst_r": np.zeros(info["M"] - info["tile_edges"], np.int32),
+    }
+    order = ("tcol_cb", "tcol_ptr", "tcol_tile", "masks_t", "indptrT_r", "csc_dst_r")
+    ptrs = [arr[k].ctypes.data_as(ctypes.c_void_p) if arr[k].size else None for k in order]
+    _check(lib.gattn_plan_export_tile_bwd(plan.handle, None, *ptrs), "gattn_plan_export_tile_bwd")
     return arr
 
 

@@ -350,6 +350,26 @@ gattn_status gattn_plan_export_tiles(const gattn_plan* plan, int32_t* tile_rb, i
   return GATTN_OK;
 }
 
+gattn_status gattn_plan_export_tile_bwd(const gattn_plan* plan, int64_t* n_tcols,
+                                        int32_t* tcol_cb, int32_t* tcol_ptr, int32_t* tcol_tile,
+                                        uint32_t* masks_t, int32_t* indptrT_r,
+                                        int32_t* csc_dst_r) {
+  GATTN_REQUIRE(plan, GATTN_ERR_INVALID_ARG, "plan is NULL");
+  const Plan& p = plan->p;
+  GATTN_REQUIRE(p.tile_min > 0, GATTN_ERR_INVALID_ARG, "the plan was built without tile_enable");
+  if (n_tcols) *n_tcols = p.n_tcols;
+  gattn_status s;
+  if ((s = copy_out(tcol_cb, p.tcol_cb, p.n_tcols)) != GATTN_OK) return s;
+  if ((s = copy_out(tcol_ptr, p.tcol_ptr, size_t(p.n_tcols) + 1)) != GATTN_OK) return s;
+  if ((s = copy_out(tcol_tile, p.tcol_tile, p.n_tiles)) != GATTN_OK) return s;
+  if ((s = copy_out(reinterpret_cast<int32_t*>(masks_t), p.tile_mask_t,
+                    size_t(p.n_tiles) * kTileRows * 4)) != GATTN_OK)
+    return s;
+  if ((s = copy_out(indptrT_r, p.indptrT_r, size_t(p.N) + 1)) != GATTN_OK) return s;
+  if ((s = copy_out(csc_dst_r, p.csc_dst_r, p.M_res)) != GATTN_OK) return s;
+  return GATTN_OK;
+}
+
 gattn_status gattn_plan_check_errors(const gattn_plan* plan) {
   GATTN_REQUIRE(plan, GATTN_ERR_INVALID_ARG, "plan is NULL");
   cudaError_t e = cudaDeviceSynchronize();
@@ -548,7 +568,8 @@ gattn_status gattn_bwd_dq(const gattn_plan* plan, int32_t H, int32_t D, gattn_dt
   TileBwdParams tp{};
   const int64_t HD = int64_t(H) * D;
   if (!encode_tile_map(&tp.ma0, Q, p.N, HD) || !encode_tile_map(&tp.ma1, dout, p.N, HD) ||
-      !encode_tile_map(&tp.mb0, K, p.N, HD) || !encode_tile_map(&tp.mb1, V, p.N, HD))
+      !encode_tile_map(&tp.mb0, K, p.N, HD) || !encode_tile_map(&tp.mb1, V, p.N, HD) ||
+      !encode_tile_map(&tp.mg1, dQ, p.N, HD))
     return GATTN_ERR_CUDA;
   tp.mask = p.tile_mask;
   tp.desc = p.tdesc_row;
@@ -614,7 +635,8 @@ gattn_status gattn_bwd_dkdv(const gattn_plan* plan, int32_t H, int32_t D, gattn_
   TileBwdParams tp{};
   const int64_t HD = int64_t(H) * D;
   if (!encode_tile_map(&tp.ma0, K, p.N, HD) || !encode_tile_map(&tp.ma1, V, p.N, HD) ||
-      !encode_tile_map(&tp.mb0, Q, p.N, HD) || !encode_tile_map(&tp.mb1, dout, p.N, HD))
+      !encode_tile_map(&tp.mb0, Q, p.N, HD) || !encode_tile_map(&tp.mb1, dout, p.N, HD) ||
+      !encode_tile_map(&tp.mg1, dK, p.N, HD) || !encode_tile_map(&tp.mg2, dV, p.N, HD))
     return GATTN_ERR_CUDA;
   tp.mask = p.tile_mask_t;
   tp.desc = p.tdesc_col;

@@ -28,6 +28,7 @@ struct TileParams {
 struct TileBwdParams {
   CUtensorMap ma0, ma1;        // own block:   row kernel Q, dO;  column kernel K, V
   CUtensorMap mb0, mb1;        // other block: row kernel K, V;   column kernel Q, dO
+  CUtensorMap mg1, mg2;        // gradients (tile maps of g1, g2)
   const uint32_t* mask;        // row kernel: tile masks; column kernel: transposed masks
   const int4* desc;            // [n_tiles] per list position: own block, other block, tile
                                // id, flags (1 first, 2 last tile of the own block)

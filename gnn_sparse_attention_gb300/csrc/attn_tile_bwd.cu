@@ -119,7 +119,8 @@ __global__ void __launch_bounds__(kThr, 1) tile_bwd_kernel(const __grid_constant
   uint64_t* barL = reinterpret_cast<uint64_t*>(smem + SM::BAR);  // [2] operand slots
   uint64_t* barS = barL + 2;
   uint64_t* barD = barL + 3;
-  uint32_t* sTmem = reinterpret_cast<uint32_t*>(barL + 4);
+  uint64_t* barR = barL + 4;  // residual tiles of the epilogue
+  uint32_t* sTmem = reinterpret_cast<uint32_t*>(barL + 5);
   float* sL = reinterpret_cast<float*>(smem + SM::STAT);  // column kernel only
   float* sDl = sL + kT;
 
@@ -133,6 +134,7 @@ __global__ void __launch_bounds__(kThr, 1) tile_bwd_kernel(const __grid_constant
     for (int s = 0; s < NS; ++s) mbar_init(barL + s, 1);
     mbar_init(barS, 1);
     mbar_init(barD, 1);
+    mbar_init(barR, 1);
     mbar_init_fence();
   }
   if (warp == 0) {
@@ -168,8 +170,8 @@ __global__ void __launch_bounds__(kThr, 1) tile_bwd_kernel(const __grid_constant
 
   // barrier phases: bit s of phL = parity of slot s's next completion;
   // bit s of pendL = a load into slot s is in flight
-  uint32_t phL = 0, pendL = 0, nS = 0, nD = 0;
-  bool pendS = false, pendD = false;
+  uint32_t phL = 0, pendL = 0, nS = 0, nD = 0, nR = 0;
+  bool pendS = false, pendD = false, pendR = false;
   bool bad = false;
 
   // lse * log2(e) and Delta of row r of the rows a step's scores belong to
@@ -185,37 +187,26 @@ __global__ void __launch_bounds__(kThr, 1) tile_bwd_kernel(const __grid_constant
   };
   // The epilogue's 32-column pieces: NG gradient tensors (row kernel dQ;
   // column kernel dV, dK) of D / 32 pieces each; thread chunk cc takes
-  // pieces cc, cc + 4, ...  Piece x is tensor x / (D / 32), columns
-  // 32 (x % (D / 32)) of the head row.
+  // pieces cc, cc + 4, ...  Piece x is tensor t = x / (D / 32), columns
+  // 32 (x % (D / 32)) of the head row.  Tensor t's residual tile (rows the
+  // CSR / CSC pass wrote) arrives by TMA in the slot's own-block operand
+  // region, free once S and dP are done (t = 0 in A0, t = 1 in A1, swizzled
+  // like every operand tile); the sums are written back in place and leave
+  // by TMA stores, so no thread touches global memory in the epilogue.
   constexpr int NG = COL ? 2 : 1;
   constexpr int NPC = NG * D / 32;
   constexpr int NPT = (NPC + 3) / 4;  // pieces per thread (at most)
-  auto piece_out = [&](int x) -> __nv_bfloat16* {
-    return static_cast<__nv_bfloat16*>((COL && x < D / 32) ? p.g2 : p.g1);
-  };
-  // residual rows (written by the CSR / CSC pass) of a step's epilogue,
-  // fetched into registers a step ahead
-  uint4 res[NPT][4];
-  auto fetch_res = [&](int own, int h) {
-    const int node = own * kT + r;
-    if (node < p.N) {
-      const int64_t row = (int64_t(node) * p.H + h) * D;
+  auto gmap = [&](int t) -> const CUtensorMap* { return (COL && t == 0) ? &p.mg2 : &p.mg1; };
+  auto load_res = [&](uint8_t* sl, int own, int h) {  // thread 0
+    fence_proxy_async();
+    mbar_expect_tx(barR, NG * KB * kTB);
 #pragma unroll
-      for (int j = 0; j < NPT; ++j) {
-        const int x = cc + 4 * j;
-        if (x < NPC) {
-          const uint4* g = reinterpret_cast<const uint4*>(piece_out(x) + row + (x % (D / 32)) * 32);
+    for (int t = 0; t < NG; ++t)
 #pragma unroll
-          for (int q = 0; q < 4; ++q) res[j][q] = g[q];
-        }
-      }
-    }
+      for (int kb = 0; kb < KB; ++kb)
+        tma_tile2d(sl + (t ? SM::A1 : SM::A0) + kb * kTB, gmap(t), h * D + kb * 64, own * kT, barR);
   };
-  // gradient rows of a finished (block, head): row kernel dQ = scale * acc +
-  // residual; column kernel dV = acc + residual, dK = scale * acc + residual
-  auto epilogue = [&](int own, int h) {
-    const int node = own * kT + r;
-    const int64_t row = (int64_t(node) * p.H + h) * D;
+  auto epilogue = [&](uint8_t* sl) {
 #pragma unroll
     for (int j = 0; j < NPT; ++j) {
       const int x = cc + 4 * j;
@@ -224,21 +215,30 @@ __global__ void __launch_bounds__(kThr, 1) tile_bwd_kernel(const __grid_constant
         float a[32];
         tmem_ld32((t ? tG2 : tG) + lane_off + col, a);
         tmem_wait_ld();
-        if (node < p.N) {
-          uint4* o = reinterpret_cast<uint4*>(piece_out(x) + row + col);
-          const float mul = (COL && t == 0) ? 1.f : p.scale;
+        uint8_t* row = sl + (t ? SM::A1 : SM::A0) + (col / 64) * kTB + r * 128;
+        const float mul = (COL && t == 0) ? 1.f : p.scale;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) o[q] = add_rounded(a + 8 * q, mul, res[j][q]);
+        for (int q = 0; q < 4; ++q) {
+          uint4* ptr = reinterpret_cast<uint4*>(row + ((((col % 64) / 8 + q) ^ (r & 7)) * 16));
+          *ptr = add_rounded(a + 8 * q, mul, *ptr);
         }
       }
     }
   };
+  auto store_res = [&](const uint8_t* sl, int own, int h) {  // thread 0
+#pragma unroll
+    for (int t = 0; t < NG; ++t)
+#pragma unroll
+      for (int kb = 0; kb < KB; ++kb)
+        tma_store2d(gmap(t), h * D + kb * 64, own * kT, sl + (t ? SM::A1 : SM::A0) + kb * kTB);
+    bulk_commit();
+  };
 
-  // Step k: wait for its operands -> S, dP products -> the epilogue of the
-  // previous (block, head), which overlaps those products -> p, ds -> the
-  // gradient products.  Its own epilogue runs in step k + 1.  Descriptors
-  // are loaded two steps ahead and statistics one step ahead, so no
-  // dependent chain of small loads sits on a step's critical path.
+  // Step k: wait for its operands -> S, dP products (then the residual
+  // tiles' loads when the step ends a (block, head)) -> p, ds -> the
+  // gradient products -> the epilogue.  Descriptors are loaded two steps
+  // ahead and statistics one step ahead, so no dependent chain of small
+  // loads sits on a step's critical path.
   Step cur{-1, 0, 0, 0, -1}, nx{-1, 0, 0, 0, -1};
   int4 dc = make_int4(0, 0, 0, 0), dn = make_int4(0, 0, 0, 0);
   if (blockIdx.x < p.n_grp) {
@@ -247,8 +247,6 @@ __global__ void __launch_bounds__(kThr, 1) tile_bwd_kernel(const __grid_constant
     nx = step_after(p, cur, dc);
     if (nx.g >= 0) dn = p.desc[nx.q];
   }
-  int done_own = 0, done_h = 0;  // the (block, head) whose epilogue is pending
-  bool pend_epi = false;
   float nl = 0.f, nd = 0.f;      // statistics of `cur`, fetched a step ahead
   if (cur.g >= 0) {
     if (tid == 0) issue(cur, dc, 0);
@@ -264,7 +262,12 @@ __global__ void __launch_bounds__(kThr, 1) tile_bwd_kernel(const __grid_constant
     const bool last = dc.w & 2;
     if constexpr (NS == 2) {
       if (more) {
-        if (tid == 0) issue(nx, dn, s ^ 1);  // slot s ^ 1 was released by the previous step
+        // slot s ^ 1 was released by the previous step once its epilogue's
+        // stores have read their tiles
+        if (tid == 0) {
+          bulk_wait_read();
+          issue(nx, dn, s ^ 1);
+        }
         pendL |= 1u << (s ^ 1);
       }
     }
@@ -282,7 +285,7 @@ __global__ void __launch_bounds__(kThr, 1) tile_bwd_kernel(const __grid_constant
     pendL &= ~(1u << s);
 
     // ---- S and dP (row kernel: Q K^T, dO V^T; column kernel: K Q^T, V dO^T)
-    const uint8_t* sl = smem + s * SM::SLOT;
+    uint8_t* sl = smem + s * SM::SLOT;
     if (tid == 0) {
       tc_fence_after();
 #pragma unroll
@@ -296,17 +299,15 @@ __global__ void __launch_bounds__(kThr, 1) tile_bwd_kernel(const __grid_constant
       mma_commit(barS);
     }
     pendS = true;
-    // the previous (block, head)'s epilogue reads only the gradient columns
-    if (pend_epi) {
-      epilogue(done_own, done_h);
-      pend_epi = false;
-    }
-    if (last) fetch_res(dc.x, cur.h);
     ok = mbar_wait(barS, nS & 1);
     if (__syncthreads_or(!ok)) { bad = true; break; }
     ++nS;
     pendS = false;
     tc_fence_after();
+    if (last) {  // the own-block operands are consumed: their region takes the residual tiles
+      if (tid == 0) load_res(sl, dc.x, cur.h);
+      pendR = true;
+    }
 
     // ---- p and ds of row r, columns [32 cc, 32 cc + 32) -> bf16 operand tiles
     {
@@ -394,23 +395,31 @@ __global__ void __launch_bounds__(kThr, 1) tile_bwd_kernel(const __grid_constant
     pendD = false;
     tc_fence_after();
 
+    if (last) {  // ---- epilogue: residual + this (block, head)'s sums, out by TMA
+      ok = mbar_wait(barR, nR & 1);
+      if (__syncthreads_or(!ok)) { bad = true; break; }
+      ++nR;
+      pendR = false;
+      epilogue(sl);
+      fence_proxy_async();  // generic stores of the sums -> visible to the TMA stores
+      tc_fence_before();
+      __syncthreads();
+      if (tid == 0) store_res(sl, dc.x, cur.h);
+    }
     if constexpr (NS == 1) {
       if (more) {
-        if (tid == 0) issue(nx, dn, 0);  // the slot is free: both products have completed
+        if (tid == 0) {  // the slot is free once the products are done and the stores have read it
+          bulk_wait_read();
+          issue(nx, dn, 0);
+        }
         pendL |= 1u;
       }
-    }
-    if (last) {
-      done_own = dc.x;
-      done_h = cur.h;
-      pend_epi = true;
     }
     cur = nx;
     dc = dn;
     nx = n2;
     dn = d2;
   }
-  if (!bad && pend_epi) epilogue(done_own, done_h);
 
   if (bad && tid == 0) {
     atomicOr(p.err, 2);
@@ -420,7 +429,9 @@ __global__ void __launch_bounds__(kThr, 1) tile_bwd_kernel(const __grid_constant
       if ((pendL >> s) & 1u) mbar_wait(barL + s, (phL >> s) & 1u);
     if (pendS) mbar_wait(barS, nS & 1);
     if (pendD) mbar_wait(barD, nD & 1);
+    if (pendR) mbar_wait(barR, nR & 1);
   }
+  if (tid == 0) bulk_wait();  // the epilogues' stores have completed
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

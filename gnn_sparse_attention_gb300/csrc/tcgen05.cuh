@@ -19,6 +19,26 @@ __device__ __forceinline__ void tma_tile2d(void* dst, const CUtensorMap* map, in
       : "memory");
 }
 
+// 2-D TMA tile store (shared -> global, bulk group of the issuing thread);
+// rows past the tensor's end are not written.
+__device__ __forceinline__ void tma_store2d(const CUtensorMap* map, int x, int y, const void* src) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];\n" ::"l"(map),
+      "r"(x), "r"(y), "r"(smem_u32(src))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+}
+// Wait until this thread's bulk stores have read their shared memory.
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
+}
+// Wait until this thread's bulk stores have completed.
+__device__ __forceinline__ void bulk_wait() {
+  asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
+}
+
 // Shared-memory matrix descriptor: 128-byte swizzle, start address, leading
 // and stride byte offsets (16-byte units), descriptor version 1.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {

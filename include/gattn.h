@@ -177,6 +177,28 @@ GATTN_API gattn_status gattn_plan_export_tiles(const gattn_plan* plan, int32_t* 
                                                int32_t* indptr_r, int32_t* indices_r);
 
 /*
+ * Copy the structures the tile backward walks to HOST buffers (each
+ * nullable; synchronous; "Methodology", attention-based layers: the
+ * backward recomputes the weights tile by tile, and the transposed adjacency
+ * is cached for the source-side gradients).
+ *   n_tcols (out)        : column blocks that have tiles
+ *   tcol_cb[n_tcols]     : those column blocks, ascending
+ *   tcol_ptr[n_tcols+1], tcol_tile[n_tiles] : tile ids of each column block,
+ *                          ascending (so ascending row block)
+ *   masks_t[n_tiles * 512] : the masks transposed: per tile 128 columns of 4
+ *                          words; bit b of word w of column c is the mask bit
+ *                          of row 32 w + b, column c
+ *   indptrT_r[N+1], csc_dst_r[M - tile_edges] : the transpose of the
+ *                          residual CSR, each column in residual CSR order
+ * Call once with only n_tcols to size tcol_cb and tcol_ptr.  Returns
+ * GATTN_ERR_INVALID_ARG for a plan built without tile_enable.
+ */
+GATTN_API gattn_status gattn_plan_export_tile_bwd(const gattn_plan* plan, int64_t* n_tcols,
+                                                  int32_t* tcol_cb, int32_t* tcol_ptr,
+                                                  int32_t* tcol_tile, uint32_t* masks_t,
+                                                  int32_t* indptrT_r, int32_t* csc_dst_r);
+
+/*
  * Synchronise the device and report whether any kernel run with this plan
  * since the last check gave up a bounded wait for its asynchronous copies
  * (every wait in the kernels has an iteration limit; on expiry the kernel

@@ -220,3 +220,39 @@ def test_tile_backward_is_deterministic():
             assert torch.equal(x, y)
     finally:
         case.close()
+
+
+def _transposed_masks(masks):
+    """masks [n, 128 rows, 4 words] -> [n, 128 columns, 4 words] (numpy bit transpose)."""
+    bits = np.unpackbits(masks.view(np.uint8).reshape(len(masks), 128, 16), axis=2,
+                         bitorder="little").reshape(len(masks), 128, 128)   # [t, row, column]
+    return np.packbits(bits.transpose(0, 2, 1).reshape(len(masks), 128, 128), axis=2,
+                       bitorder="little").reshape(len(masks), 128, 16).view(np.uint32)
+
+
+@pytest.mark.parametrize("kind", ["sbm", "blocks", "blocks_sparse"])
+def test_tile_backward_plan_matches_oracle(kind):
+    """The residual CSC is the oracle plan's CSC of the oracle's residual CSR,
+    the column grouping is a stable sort of the oracle's tiles by column
+    block, and the transposed masks are the oracle's masks transposed."""
+    from gnn_sparse_attention_gb300 import binding as gb
+    if kind == "sbm":
+        ip, ix = with_extras(*sbm_graph(1200, seed=21), seed=21)
+    else:
+        ip, ix = dense_blocks_graph(600, BLOCK_PAIRS, 0.3 if kind == "blocks" else 0.08, seed=5)
+    case = GpuCase(ip, ix, 1, 64, "bf16", "dot", tile=True)
+    try:
+        got = gb.gattn_plan_export_tile_bwd(case.plan)
+        info = case.plan.info()
+        tp = oracle.tile_plan(ip, ix, info["tile_min_edges"])
+        res = oracle.plan(tp["indptr_r"], tp["indices_r"], 32, 32)
+        np.testing.assert_array_equal(got["indptrT_r"], res["indptrT"])
+        np.testing.assert_array_equal(got["csc_dst_r"], res["csc_dst"])
+        order = np.argsort(tp["tile_cb"], kind="stable").astype(np.int32)
+        cbs, starts = np.unique(tp["tile_cb"][order], return_index=True)
+        np.testing.assert_array_equal(got["tcol_tile"], order)
+        np.testing.assert_array_equal(got["tcol_cb"], cbs)
+        np.testing.assert_array_equal(got["tcol_ptr"], np.append(starts, len(order)))
+        np.testing.assert_array_equal(got["masks_t"], _transposed_masks(tp["masks"]))
+    finally:
+        case.close()
