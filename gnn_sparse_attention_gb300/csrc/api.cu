@@ -458,20 +458,18 @@ gattn_status gattn_fwd(const gattn_plan* plan, int32_t H, int32_t D, gattn_dtype
   TileParams tp{};
   const int64_t HD = int64_t(H) * D;
   if (!encode_tile_map(&tp.mq, Q, p.N, HD) || !encode_tile_map(&tp.mk, K, p.N, HD) ||
-      !encode_tile_map(&tp.mv, V, p.N, HD))
+      !encode_tile_map(&tp.mv, V, p.N, HD) || !encode_tile_map(&tp.mo, out, p.N, HD))
     return GATTN_ERR_CUDA;
   tp.mask = p.tile_mask;
-  tp.tile_cb = p.tile_cb;
-  tp.trow_rb = p.trow_rb;
-  tp.trow_ptr = p.trow_ptr;
-  tp.n_trows = p.n_trows;
+  tp.desc = p.tdesc_row;
+  tp.grp_ptr = p.trow_ptr;
+  tp.n_grp = p.n_trows;
   tp.N = p.N;
   tp.H = H;
   tp.qmul = f.qmul;
-  tp.out = out;
   tp.lse = lse;
   tp.err = p.err;
-  return launch_tile_fwd(tp, D, st);
+  return launch_tile_fwd(tp, D, p.num_sms, st);
 }
 
 static gattn_status bwd_common(const gattn_plan* plan, int32_t H, int32_t D, gattn_dtype dtype,

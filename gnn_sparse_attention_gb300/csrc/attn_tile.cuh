@@ -7,16 +7,18 @@
 
 namespace gattn {
 
+// Forward of the tiles (attn_tile.cu): one CTA per SM walks the row blocks
+// that have tiles, the heads, and each row block's tiles.
 struct TileParams {
   CUtensorMap mq, mk, mv;      // Q, K, V as [N, H*D] bf16 with 64 x 128 boxes, 128-byte swizzle
+  CUtensorMap mo;              // out, the same way (residual result in, merged result out)
   const uint32_t* mask;        // [n_tiles][128][4] tile bit masks
-  const int32_t* tile_cb;      // [n_tiles] column block of each tile
-  const int32_t* trow_rb;      // [n_trows] row block of each CTA
-  const int32_t* trow_ptr;     // [n_trows + 1] tiles of each row block
-  int64_t n_trows;
+  const int4* desc;            // [n_tiles] per tile: row block, column block, tile id,
+                               // flags (1 first, 2 last tile of its row block)
+  const int32_t* grp_ptr;      // [n_grp + 1] tiles of each row block that has tiles
+  int64_t n_grp;
   int N, H;
   float qmul;                  // scale * log2(e)
-  void* out;                   // bf16 [N, H, D]: residual result in, merged result out
   float* lse;                  // [N, H]: residual lse in, merged lse out
   int32_t* err;
 };
@@ -48,11 +50,35 @@ struct TileBwdParams {
 // after the residual pass of the same side.
 gattn_status launch_tile_bwd(const TileBwdParams& p, int D, bool col, int num_sms, cudaStream_t st);
 
+// A step of the tile kernels: block list entry g, head h, position q in the
+// tile list; q0 is the first position of g's tiles and qn that of the
+// CTA's next block (-1 past the end), fetched when the block starts.  The
+// CTAs take the blocks in grid stride, and for each block every head in
+// turn, and for each head the block's tiles.
+struct TileStep {
+  int g, h, q, q0, qn;
+};
+
+template <class P>
+__device__ __forceinline__ TileStep tile_step_block(const P& p, int64_t g, int q0) {
+  const int64_t gn = g + gridDim.x;
+  return TileStep{int(g), 0, q0, q0, gn < p.n_grp ? p.grp_ptr[gn] : -1};
+}
+
+// The step after c, whose descriptor is d (no loads but the next block's qn).
+template <class P>
+__device__ __forceinline__ TileStep tile_step_after(const P& p, const TileStep& c, int4 d) {
+  if (!(d.w & 2)) return TileStep{c.g, c.h, c.q + 1, c.q0, c.qn};
+  if (c.h + 1 < p.H) return TileStep{c.g, c.h + 1, c.q0, c.q0, c.qn};
+  if (c.qn < 0) return TileStep{-1, 0, 0, 0, -1};
+  return tile_step_block(p, int64_t(c.g) + gridDim.x, c.qn);
+}
+
 // Tensor map of a [rows, width] bf16 matrix read in 64-column x 128-row
 // boxes with the 128-byte swizzle (the tensor cores' operand layout).
 bool encode_tile_map(CUtensorMap* map, const void* base, int64_t rows, int64_t width);
 
 // Launch the dense-tile forward (D = 64 or 128) after the residual pass.
-gattn_status launch_tile_fwd(const TileParams& p, int D, cudaStream_t st);
+gattn_status launch_tile_fwd(const TileParams& p, int D, int num_sms, cudaStream_t st);
 
 }  // namespace gattn

@@ -72,26 +72,6 @@ struct BwdSmem {
   static_assert(BYTES <= 227 * 1024, "shared memory of one CTA");
 };
 
-// One step: block list entry g, head h, position q in the tile list; q0
-// is the first position of g's tiles and qn that of the CTA's next block
-// (-1 past the end), fetched when the block starts.
-struct Step {
-  int g, h, q, q0, qn;
-};
-
-__device__ __forceinline__ Step step_block(const TileBwdParams& p, int64_t g, int q0) {
-  const int64_t gn = g + gridDim.x;
-  return Step{int(g), 0, q0, q0, gn < p.n_grp ? p.grp_ptr[gn] : -1};
-}
-
-// The step after c, whose descriptor is d (no loads but the next block's qn).
-__device__ __forceinline__ Step step_after(const TileBwdParams& p, const Step& c, int4 d) {
-  if (!(d.w & 2)) return Step{c.g, c.h, c.q + 1, c.q0, c.qn};
-  if (c.h + 1 < p.H) return Step{c.g, c.h + 1, c.q0, c.q0, c.qn};
-  if (c.qn < 0) return Step{-1, 0, 0, 0, -1};
-  return step_block(p, int64_t(c.g) + gridDim.x, c.qn);
-}
-
 // out = acc * mul + residual (8 bf16 values)
 __device__ __forceinline__ uint4 add_rounded(const float* acc, float mul, uint4 res) {
   const uint32_t in[4] = {res.x, res.y, res.z, res.w};
@@ -153,7 +133,7 @@ __global__ void __launch_bounds__(kThr, 1) tile_bwd_kernel(const __grid_constant
   const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;  // this warp's TMEM lane quarter
 
   // TMA loads of one step (descriptor d) into slot s (thread 0)
-  auto issue = [&](const Step& c, int4 d, int s) {
+  auto issue = [&](const TileStep& c, int4 d, int s) {
     uint8_t* sl = smem + s * SM::SLOT;
     fence_proxy_async();
     mbar_expect_tx(barL + s, LOAD_BYTES);
@@ -176,7 +156,7 @@ __global__ void __launch_bounds__(kThr, 1) tile_bwd_kernel(const __grid_constant
 
   // lse * log2(e) and Delta of row r of the rows a step's scores belong to
   // (row kernel: the own block; column kernel: the tile's row block)
-  auto stats = [&](const Step& c, int4 d, float& a, float& b) {
+  auto stats = [&](const TileStep& c, int4 d, float& a, float& b) {
     const int i = (COL ? d.y : d.x) * kT + r;
     a = 0.f;
     b = 0.f;
@@ -239,12 +219,12 @@ __global__ void __launch_bounds__(kThr, 1) tile_bwd_kernel(const __grid_constant
   // gradient products -> the epilogue.  Descriptors are loaded two steps
   // ahead and statistics one step ahead, so no dependent chain of small
   // loads sits on a step's critical path.
-  Step cur{-1, 0, 0, 0, -1}, nx{-1, 0, 0, 0, -1};
+  TileStep cur{-1, 0, 0, 0, -1}, nx{-1, 0, 0, 0, -1};
   int4 dc = make_int4(0, 0, 0, 0), dn = make_int4(0, 0, 0, 0);
   if (blockIdx.x < p.n_grp) {
-    cur = step_block(p, blockIdx.x, p.grp_ptr[blockIdx.x]);
+    cur = tile_step_block(p, blockIdx.x, p.grp_ptr[blockIdx.x]);
     dc = p.desc[cur.q];
-    nx = step_after(p, cur, dc);
+    nx = tile_step_after(p, cur, dc);
     if (nx.g >= 0) dn = p.desc[nx.q];
   }
   float nl = 0.f, nd = 0.f;      // statistics of `cur`, fetched a step ahead
@@ -256,7 +236,7 @@ __global__ void __launch_bounds__(kThr, 1) tile_bwd_kernel(const __grid_constant
   for (int k = 0; cur.g >= 0; ++k) {
     const int s = NS == 2 ? (k & 1) : 0;
     const bool more = nx.g >= 0;
-    const Step n2 = more ? step_after(p, nx, dn) : Step{-1, 0, 0, 0, -1};
+    const TileStep n2 = more ? tile_step_after(p, nx, dn) : TileStep{-1, 0, 0, 0, -1};
     const int4 d2 = n2.g >= 0 ? p.desc[n2.q] : make_int4(0, 0, 0, 0);  // used next step
     const bool first = dc.w & 1;
     const bool last = dc.w & 2;
