@@ -73,7 +73,7 @@ Workspace ws_layout(const Plan& p, int H, int D) {
   w.dq_part = off;
   off = align_up(off + (slots > slots_res ? slots : slots_res) * HD * 4, 256);
   w.delta = off;
-  off = align_up(off + size_t(p.N) * H * 4, 256);
+  off = align_up(off + size_t(p.N) * 2 * H * 4, 256);  // (lse log2(e), Delta) per node
   w.dkv_part = off;
   off = align_up(off + slots_src * 2 * HD * 4, 256);
   w.da_part = off;
@@ -501,7 +501,7 @@ static gattn_status bwd_common(const gattn_plan* plan, int32_t H, int32_t D, gat
   b->H = H;
   b->D = D;
   b->rows16 = (H % 4 == 0) && aligned(lse, 16);
-  b->delta16 = (H % 4 == 0);
+  b->delta16 = (H % 2 == 0);
   b->da_part = reinterpret_cast<float*>(ws + w->da_part);
   b->da_cnt = plan->p.cnt_da;
   b->err = plan->p.err;
@@ -613,8 +613,7 @@ gattn_status gattn_bwd_dkdv(const gattn_plan* plan, int32_t H, int32_t D, gattn_
     if (!encode_rows_map(&b.mi0, K, es, bf, p.N, HD) || !encode_rows_map(&b.mi1, V, es, bf, p.N, HD) ||
         !encode_rows_map(&b.me0, Q, es, bf, p.N, HD) ||
         !encode_rows_map(&b.me1, dout, es, bf, p.N, HD) ||
-        (b.rows16 && !encode_rows_map(&b.ms0, lse, 4, false, p.N, H)) ||
-        (b.delta16 && !encode_rows_map(&b.ms1, b.delta, 4, false, p.N, H)))
+        (b.delta16 && !encode_rows_map(&b.ms0, b.delta, 4, false, p.N, 2 * H)))
       return GATTN_ERR_CUDA;
   }
   b.idx = tiles ? p.csc_dst_r : p.csc_dst;

@@ -29,9 +29,9 @@ namespace gattn {
 struct BwdParams {
   // row-gather maps (tma.cuh).  Pass 1: mi0..mi2 = Q, dO, O (item rows),
   // me0, me1 = K, V (edge rows), ms0 = lse (item stat rows).  Pass 2: mi0,
-  // mi1 = K, V (item rows), me0, me1 = Q, dO (edge rows), ms0, ms1 = lse,
-  // Delta (edge stat rows).
-  CUtensorMap mi0, mi1, mi2, me0, me1, ms0, ms1;
+  // mi1 = K, V (item rows), me0, me1 = Q, dO (edge rows), ms0 = the
+  // (lse log2(e), Delta) rows (edge stat rows).
+  CUtensorMap mi0, mi1, mi2, me0, me1, ms0;
   const int4* items;   // plan items (w = heavy id of a chunk)
   const int4* sorted;  // items by decreasing length
   int64_t n_items;
@@ -44,7 +44,7 @@ struct BwdParams {
   const void* O;
   const void* dO;
   const float* lse;
-  float* delta;        // [N, H] workspace
+  float* delta;        // [N, 2H] workspace: lse * log2(e) of the H heads, then Delta
   void* G1;            // pass 1: dQ;  pass 2: dK
   void* G2;            // pass 2: dV
   float* da;           // GATv2 [H*D] or null
@@ -54,7 +54,7 @@ struct BwdParams {
   float slope;
   int H, D;
   int rows16;          // lse rows are gathered by TMA (H % 4 == 0, lse 16-B aligned)
-  int delta16;         // Delta rows are gathered by TMA (H % 4 == 0)
+  int delta16;         // (lse, Delta) rows are gathered by TMA (H even: whole 16-byte pieces)
   float* part;         // partials per tree slot: pass 1 [slots][HD], pass 2 [slots][2*HD]
   Tree tree;           // merge trees of the heavy items of this pass
   float* da_part;      // [gridDim.x][HD]
@@ -90,9 +90,8 @@ struct CscShape {
   // per item slot: K, V rows; per edge: Q row, dO row, lse row, Delta row
   static constexpr int OQE = 2 * L::IR * RB;            // Q rows of the edges
   static constexpr int OGE = OQE + L::B * RB;           // dO rows
-  static constexpr int OLS = OGE + L::B * RB;           // lse sets
-  static constexpr int ODL = OLS + L::B / 4 * L::SSB;   // Delta sets
-  static constexpr int STAGE = ODL + L::B / 4 * L::SSB;
+  static constexpr int OLS = OGE + L::B * RB;           // (lse, Delta) sets: 4 rows of 2H floats
+  static constexpr int STAGE = OLS + L::B / 4 * 2 * L::SSB;
   static constexpr int WARP_BYTES = align128(kStages * STAGE + L::META);
   static constexpr int WARPS = WarpsFor<WARP_BYTES>::value;
   static constexpr int THREADS = 32 * WARPS;
@@ -275,9 +274,14 @@ __global__ void __launch_bounds__(CsrShape<T, RB, SB>::THREADS) bwd_csr_kernel(c
           const int c0 = j * LH::CPL;
           dlt[j] = dsum[j];
           lse2[j] = ls[head[c0]] * kLog2e;
-          // every chunk of a heavy node computes the same Delta: duplicate
-          // writes store identical values
-          if (hw[c0]) p.delta[int64_t(d.x) * p.H + head[c0]] = dlt[j];
+          // the CSC pass reads (lse log2(e), Delta) of a destination as one
+          // row; every chunk of a heavy node computes the same values:
+          // duplicate writes store identical values
+          if (hw[c0]) {
+            float* srow = p.delta + int64_t(d.x) * 2 * p.H;
+            srow[head[c0]] = lse2[j];
+            srow[p.H + head[c0]] = dlt[j];
+          }
         }
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
@@ -497,6 +501,7 @@ __global__ void __launch_bounds__(CscShape<T, RB, SB>::THREADS) bwd_csc_kernel(c
       for (int v = 0; v < PP; ++v)
         av[c][v] = make_float2(__ldg(p.a + elem[c] + 2 * v), __ldg(p.a + elem[c] + 2 * v + 1));
   }
+  const float gc1 = 0.5f * (1.f + p.slope), gc2 = 0.5f * (1.f - p.slope);  // LReLU = c1 z + c2 |z|
 
   const int64_t warp = (int64_t(blockIdx.x) * Sh::THREADS + threadIdx.x) >> 5;
   const int64_t nwarps = (int64_t(gridDim.x) * Sh::THREADS) >> 5;
@@ -509,7 +514,8 @@ __global__ void __launch_bounds__(CscShape<T, RB, SB>::THREADS) bwd_csc_kernel(c
   // stat rows by gather when they are whole 16-byte pieces, else by 4-byte
   // cp.async.
   constexpr int OKI = 0, OVI = L::IR * RB;
-  constexpr int OQE = Sh::OQE, OGE = Sh::OGE, OLS = Sh::OLS, ODL = Sh::ODL;
+  constexpr int OQE = Sh::OQE, OGE = Sh::OGE, OLS = Sh::OLS;
+  constexpr int SS2 = 2 * L::SSB;  // bytes of a set of 4 (lse, Delta) rows
   auto issue = [&](int s) {
     const int4* dsc = ring.desc_at(s);
     if (lane == 0 && dsc[0].x != -3) {
@@ -524,8 +530,7 @@ __global__ void __launch_bounds__(CscShape<T, RB, SB>::THREADS) bwd_csc_kernel(c
                          qr[q4].w != p.N;
         qmask |= uint32_t(any) << q4;
       }
-      const uint32_t eset =
-          2 * L::SET_BYTES + (p.rows16 ? 16 * p.H : 0) + (p.delta16 ? 16 * p.H : 0);
+      const uint32_t eset = 2 * L::SET_BYTES + (p.delta16 ? 32 * p.H : 0);
       const uint32_t ibytes = L::IBULK ? item_rows<L>(qr[0], p.N) * 2 * RB
                                        : __popc(qmask) * 2 * L::SET_BYTES;
       fence_proxy_async();
@@ -547,18 +552,16 @@ __global__ void __launch_bounds__(CscShape<T, RB, SB>::THREADS) bwd_csc_kernel(c
         const int4 r = ring.eset(s, b4);
         L::gather(st + OQE, 4 * b4, &p.me0, r.x, r.y, r.z, r.w, bar);
         L::gather(st + OGE, 4 * b4, &p.me1, r.x, r.y, r.z, r.w, bar);
-        if (p.rows16) tma_gather4(st + OLS + b4 * L::SSB, &p.ms0, 0, r.x, r.y, r.z, r.w, bar);
-        if (p.delta16) tma_gather4(st + ODL + b4 * L::SSB, &p.ms1, 0, r.x, r.y, r.z, r.w, bar);
+        if (p.delta16) tma_gather4(st + OLS + b4 * SS2, &p.ms0, 0, r.x, r.y, r.z, r.w, bar);
       }
     }
-    if (!p.rows16 || !p.delta16) {  // stat rows of the edges by 4-byte copies
+    if (!p.delta16) {  // stat rows of the edges by 4-byte copies
       const int4 dg = lane < G ? dsc[lane] : make_int4(-1, 0, 0, 0);
       const bool live = dsc[0].x != -3;
       const int ge = (lane / SE) & 31;
       const int cn = __shfl_sync(FULL, dg.x >= 0 ? (dg.z & kCntMask) : 0, ge);
       const int jv = (live && lane < B && lane % SE < cn) ? ring.ix_at(s)[lane] : -1;
-      if (!p.rows16) copy_stat_rows<L::SSB>(ring.stage_at(s) + OLS, p.lse, jv, B, p.H, lane);
-      if (!p.delta16) copy_stat_rows<L::SSB>(ring.stage_at(s) + ODL, p.delta, jv, B, p.H, lane);
+      copy_stat_rows<SS2>(ring.stage_at(s) + OLS, p.delta, jv, B, 2 * p.H, lane);
     }
     __syncwarp();
     cp_async_commit();
@@ -573,7 +576,10 @@ __global__ void __launch_bounds__(CscShape<T, RB, SB>::THREADS) bwd_csc_kernel(c
     issue(s);
   }
 
+  // dk: the dot score's dK sum; GATv2: sum of ds over z > 0 per element,
+  // with s1 the per-head sum of ds (combined at the item's end)
   float2 k[NC][PP], vv[NC][PP], dk[NC][PP], dv[NC][PP];
+  float s1[GAT ? HL : 1];
   for (int i = 0;; ++i) {
     ring.generate(cur, i + 2 * S - 1, lane);
     __syncwarp();
@@ -600,6 +606,10 @@ __global__ void __launch_bounds__(CscShape<T, RB, SB>::THREADS) bwd_csc_kernel(c
           dk[c][v] = dv[c][v] = f2s(0.f);
         }
       }
+      if (GAT) {
+#pragma unroll
+        for (int j = 0; j < HL; ++j) s1[j] = 0.f;
+      }
     }
 
     const uint8_t* qs = st + OQE;
@@ -623,10 +633,9 @@ __global__ void __launch_bounds__(CscShape<T, RB, SB>::THREADS) bwd_csc_kernel(c
           p2 = f2fma(gf[c][v], vv[c][v], p2);
           if (!GAT) {
             s2 = f2fma(qf[c][v], k[c][v], s2);
-          } else {
-            const float2 z = make_float2(qf[c][v].x + k[c][v].x, qf[c][v].y + k[c][v].y);
-            const float2 lr = make_float2(z.x > 0.f ? z.x : p.slope * z.x,
-                                          z.y > 0.f ? z.y : p.slope * z.y);
+          } else {  // qf becomes z = xl_i + xr_j
+            qf[c][v] = f2add(qf[c][v], k[c][v]);
+            const float2 lr = f2fma(f2s(gc1), qf[c][v], f2mul(f2s(gc2), f2abs(qf[c][v])));
             s2 = f2fma(av[c][v], lr, s2);
           }
         }
@@ -636,14 +645,14 @@ __global__ void __launch_bounds__(CscShape<T, RB, SB>::THREADS) bwd_csc_kernel(c
       head_sums<NC, CPH>(scp, sc);
       head_sums<NC, CPH>(dpp, dp);
       if (act && valid) {
-        const int b = g * SE + e, so = (b / 4) * L::SSB + (b % 4) * 4 * p.H;
+        const int b = g * SE + e, so = (b / 4) * SS2 + (b % 4) * 8 * p.H;
         float pr[HL], ds[HL];
 #pragma unroll
         for (int j = 0; j < HL; ++j) {
           const int hh = head[j * LH::CPL];
-          const float ls = reinterpret_cast<const float*>(st + OLS + so)[hh];
-          const float dl = reinterpret_cast<const float*>(st + ODL + so)[hh];
-          pr[j] = ex2((GAT ? sc[j] * kLog2e : sc[j]) - ls * kLog2e);
+          const float ls2 = reinterpret_cast<const float*>(st + OLS + so)[hh];
+          const float dl = reinterpret_cast<const float*>(st + OLS + so)[p.H + hh];
+          pr[j] = ex2((GAT ? sc[j] * kLog2e : sc[j]) - ls2);
           ds[j] = pr[j] * (dp[j] - dl);
         }
 #pragma unroll
@@ -657,16 +666,27 @@ __global__ void __launch_bounds__(CscShape<T, RB, SB>::THREADS) bwd_csc_kernel(c
           } else {
 #pragma unroll
             for (int v = 0; v < PP; ++v) {
-              const float2 z = make_float2(qf[c][v].x + k[c][v].x, qf[c][v].y + k[c][v].y);
-              const float2 sg = make_float2(z.x > 0.f ? 1.f : p.slope, z.y > 0.f ? 1.f : p.slope);
-              dk[c][v] = f2fma(f2mul(f2s(dsc_), av[c][v]), sg, dk[c][v]);
+              const float2 z = qf[c][v];
+              dk[c][v] = f2add(dk[c][v], make_float2(z.x > 0.f ? dsc_ : 0.f, z.y > 0.f ? dsc_ : 0.f));
             }
           }
+        }
+        if (GAT) {
+#pragma unroll
+          for (int j = 0; j < HL; ++j) s1[j] += ds[j];
         }
       }
     }
 
     const bool fin = act && (d.z & kLast);
+    if (GAT && fin) {  // dXr = a (s sum ds + (1 - s) sum_{z > 0} ds)
+#pragma unroll
+      for (int c = 0; c < NC; ++c)
+#pragma unroll
+        for (int v = 0; v < PP; ++v)
+          dk[c][v] = f2mul(av[c][v], f2fma(f2s(1.f - p.slope), dk[c][v],
+                                           f2s(p.slope * s1[LH::of(c)])));
+    }
     const bool heavy = fin && d.y < p.n_chunks;
     bool write = fin && !heavy;
     if (heavy) {

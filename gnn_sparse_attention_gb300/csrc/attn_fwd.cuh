@@ -89,13 +89,18 @@ __global__ void __launch_bounds__(FwdShape<T, RB, SB>::THREADS) fwd_kernel(const
     head[c] = elem[c] / D;
     hw[c] = ((t * NC + c) % CPH) == 0;
   }
-  float2 av[GAT ? NC : 1][PP];
+  // GATv2: a . LReLU(z) = (a c1) . z + (a c2) . |z| (attn_pipe.cuh)
+  float2 ac1[GAT ? NC : 1][PP], ac2[GAT ? NC : 1][PP];
   if (GAT) {
+    const float c1 = 0.5f * (1.f + p.slope), c2 = 0.5f * (1.f - p.slope);
 #pragma unroll
     for (int c = 0; c < NC; ++c)
 #pragma unroll
-      for (int v = 0; v < PP; ++v)
-        av[c][v] = make_float2(__ldg(p.a + elem[c] + 2 * v), __ldg(p.a + elem[c] + 2 * v + 1));
+      for (int v = 0; v < PP; ++v) {
+        const float2 a2 = make_float2(__ldg(p.a + elem[c] + 2 * v), __ldg(p.a + elem[c] + 2 * v + 1));
+        ac1[c][v] = f2mul(a2, f2s(c1));
+        ac2[c][v] = f2mul(a2, f2s(c2));
+      }
   }
 
   const int64_t warp = (int64_t(blockIdx.x) * Sh::THREADS + threadIdx.x) >> 5;
@@ -210,10 +215,8 @@ __global__ void __launch_bounds__(FwdShape<T, RB, SB>::THREADS) fwd_kernel(const
         } else {
 #pragma unroll
           for (int v = 0; v < PP; ++v) {
-            const float2 z = make_float2(q[c][v].x + kf[v].x, q[c][v].y + kf[v].y);
-            const float2 lr = make_float2(z.x > 0.f ? z.x : p.slope * z.x,
-                                          z.y > 0.f ? z.y : p.slope * z.y);
-            a2 = f2fma(av[c][v], lr, a2);
+            const float2 z = f2add(q[c][v], kf[v]);
+            a2 = f2fma(ac1[c][v], z, f2fma(ac2[c][v], f2abs(z), a2));
           }
         }
         part[c] = a2.x + a2.y;

@@ -251,6 +251,15 @@ struct Pairs<float> {
 __device__ __forceinline__ float2 f2fma(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 __device__ __forceinline__ float2 f2mul(float2 a, float2 b) { return __fmul2_rn(a, b); }
 __device__ __forceinline__ float2 f2s(float s) { return make_float2(s, s); }
+__device__ __forceinline__ float2 f2add(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 f2abs(float2 a) { return make_float2(fabsf(a.x), fabsf(a.y)); }
+
+// GATv2 LeakyReLU with slope s written as c1 z + c2 |z|, c1 = (1 + s) / 2,
+// c2 = (1 - s) / 2 (exact at z = 0, no branch).  Its derivative, s + (1 - s)
+// [z > 0], makes a gradient sum_j ds_j a LReLU'(z_j) equal to
+// a (s sum_j ds_j + (1 - s) sum_{j: z_j > 0} ds_j): a kernel can accumulate
+// the per-head sum of ds and the per-element sum over z > 0, and combine
+// them once per work item.
 
 // The heads a lane's NC chunks belong to: NC / CPH of them when a head is
 // narrower than the lane's slice, else one (the lane holds part of a head).

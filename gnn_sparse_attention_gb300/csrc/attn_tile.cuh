@@ -40,7 +40,7 @@ struct TileBwdParams {
   float qmul;                  // scale * log2(e)
   float scale;
   const float* lse;            // [N, H]
-  const float* delta;          // [N, H]
+  const float* delta;          // [N, 2H]: lse * log2(e) of the H heads, then Delta
   void* g1;                    // bf16: row kernel dQ, column kernel dK (residual in, sum out)
   void* g2;                    // bf16: column kernel dV
   int32_t* err;

@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(kThr, 1) tile_bwd_kernel(const __grid_constant
     b = 0.f;
     if (i < p.N) {
       a = p.lse[int64_t(i) * p.H + c.h] * kLog2e;
-      b = p.delta[int64_t(i) * p.H + c.h];
+      b = p.delta[int64_t(i) * 2 * p.H + p.H + c.h];
     }
   };
   // The epilogue's 32-column pieces: NG gradient tensors (row kernel dQ;
