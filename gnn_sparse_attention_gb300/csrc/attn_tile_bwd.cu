@@ -14,24 +14,28 @@
 // Both recompute their 128 x 128 block of scores and of dO . v on the
 // tensor cores -- the row kernel S = Q K^T and dP = dO V^T, the column
 // kernel the transposes S^T = K Q^T and dP^T = V dO^T, so that TMEM lane r
-// is always row r of the own block; 16 warps split each lane's 128 columns
-// into four 32-column chunks (a warp reads only its own lane quarter) --
-// form p and ds in fp32
-// from the forward's lse and the destination's Delta (written by the
-// residual CSR pass), store them as bf16 operand tiles in shared memory (the
-// 128-byte swizzled K-major layout the TMA loads use) and issue the
-// gradient products.  The residual passes (CSR for dQ, CSC for dK and dV,
-// over the edges outside the tiles) run first and write every row; the tile
-// kernels add their part in fp32 and round the sum to bf16.
+// is always row r of the own block.  16 warps split each lane's 128 columns
+// into four 32-column chunks (a warp reads only its own lane quarter); a
+// thread forms p and ds in fp32 from the forward's lse and the
+// destination's Delta (written by the residual CSR pass) and stores them as
+// bf16 operand tiles in shared memory (the 128-byte swizzled K-major layout
+// the TMA loads use); one thread issues the gradient products.  The
+// residual passes (CSR for dQ, CSC for dK and dV, over the edges outside
+// the tiles) run first and write every row; after a block's last tile of a
+// head, the tile kernels add their part in fp32 to those rows -- brought in
+// as TMA tiles into the step's own-block operand region, which the score
+// products no longer need -- and store the bf16 sums back with TMA.
 //
 // Schedule: one CTA per SM walks its blocks (grid stride), the heads, and
-// the block's tiles.  With two operand slots (D = 64) the next step's TMA
-// loads (four 128 x D operand tiles and the 2 KB mask) are in flight while
-// the current step computes.  TMEM holds S [0, 128), dP [128, 256) and the
-// gradient accumulators from column 256 (row kernel dQ; column kernel dV,
-// then dK), which sum over the tiles of a block and head.  Every mbarrier
-// wait is bounded; a wait that gives up sets the plan's error word, the
-// block drains what it issued (again bounded), frees its TMEM and returns.
+// the block's tiles, steered by the plan's per-tile step descriptors
+// (loaded two steps ahead).  With two operand slots (D = 64) the next
+// step's TMA loads (four 128 x D operand tiles and the 2 KB mask) are in
+// flight while the current step computes.  TMEM holds S [0, 128), dP
+// [128, 256) and the gradient accumulators from column 256 (row kernel dQ;
+// column kernel dV, then dK), which sum over the tiles of a block and head.
+// Every mbarrier wait is bounded; a wait that gives up sets the plan's error
+// word, the block drains what it issued (again bounded), frees its TMEM and
+// returns.
 #include <cuda.h>
 
 #include "attn_pipe.cuh"
