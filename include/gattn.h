@@ -210,7 +210,7 @@ GATTN_API gattn_status gattn_plan_check_errors(const gattn_plan* plan);
 /*
  * Bytes of caller-owned device workspace that gattn_fwd / gattn_bwd need
  * for this plan and head layout (heavy-chunk partials, the backward's
- * per-node Delta, GATv2 da partials).  Host call, no device work.
+ * per-node (lse, Delta) rows, GATv2 da partials).  Host call, no device work.
  */
 GATTN_API gattn_status gattn_workspace_size(const gattn_plan* plan, int32_t H, int32_t D,
                                   gattn_dtype dtype, size_t* bytes);
