@@ -213,6 +213,7 @@ GATTN_FOR_SPMM_ROWS(GATTN_DECLARE_SPMM, bf16)
 struct WsbParams {
   CUtensorMap mw;              // weight tiles as [n_tiles * 128, 128] bf16, 64 x 128 boxes
   CUtensorMap mx;              // x as [N, F] bf16, 64 x 128 boxes
+  CUtensorMap my;              // y the same way (residual result in, sum out)
   const int32_t* tile_cb;
   const int32_t* trow_rb;
   const int32_t* trow_ptr;

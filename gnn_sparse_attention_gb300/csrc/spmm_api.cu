@@ -193,7 +193,7 @@ gattn_status gattn_spmm(const gattn_plan* plan, int32_t F, gattn_dtype dtype, co
   WsbParams t{};
   __nv_bfloat16* tiles = reinterpret_cast<__nv_bfloat16*>(base + ws.tiles);
   if (!encode_tile_map(&t.mw, tiles, P.n_tiles * kTileRows, kTileRows) ||
-      !encode_tile_map(&t.mx, x, P.N, F))
+      !encode_tile_map(&t.mx, x, P.N, F) || !encode_tile_map(&t.my, y, P.N, F))
     return GATTN_ERR_CUDA;
   t.tile_cb = P.tile_cb;
   t.trow_rb = P.trow_rb;

@@ -11,7 +11,10 @@
 // x the B operand (MN-major, features contiguous), both loaded by TMA with
 // the 128-byte swizzle; the fp32 product accumulates in TMEM over the row
 // block's tiles, 64 feature columns per MMA, up to 256 columns per pass.
-// Thread r of the 128-thread CTA owns row r (TMEM lane r) in the epilogue.
+// Thread r of the 128-thread CTA owns row r (TMEM lane r) in the epilogue:
+// after a pass's last tile the residual y tile comes in by TMA over the
+// source-row buffer (free once the products are done), each thread adds its
+// row, and the sums leave by a TMA store.
 // Every wait is bounded; a failed wait is recorded in the plan's error word
 // and the CTA drains (bounded), frees its TMEM and returns.
 #include "spmm.cuh"
@@ -44,14 +47,15 @@ __global__ void __launch_bounds__(128) wsb_tile_kernel(const __grid_constant__ W
   uint8_t* sX = smem + SM::X;
   uint64_t* barLoad = reinterpret_cast<uint64_t*>(smem + SM::BAR);
   uint64_t* barMma = barLoad + 1;
-  uint32_t* sTmem = reinterpret_cast<uint32_t*>(barLoad + 2);
+  uint64_t* barY = barLoad + 2;
+  uint32_t* sTmem = reinterpret_cast<uint32_t*>(barLoad + 3);
   const int tid = threadIdx.x, warp = tid >> 5;
   const int rb = p.trow_rb[blockIdx.x];
   const int t0 = p.trow_ptr[blockIdx.x], t1 = p.trow_ptr[blockIdx.x + 1];
-  const int node = rb * kRows + tid;
   if (tid == 0) {
     mbar_init(barLoad, 1);
     mbar_init(barMma, 1);
+    mbar_init(barY, 1);
     mbar_init_fence();
   }
   if (warp == 0) {
@@ -66,12 +70,13 @@ __global__ void __launch_bounds__(128) wsb_tile_kernel(const __grid_constant__ W
   tc_fence_after();
   const uint32_t tD = *sTmem;
   const uint32_t lane_off = uint32_t(warp * 32) << 16;
-  uint32_t nLoad = 0, nMma = 0;
-  bool pendLoad = false, pendMma = false, bad = false;
+  uint32_t nLoad = 0, nMma = 0, nY = 0;
+  bool pendLoad = false, pendMma = false, pendY = false, bad = false;
 
   for (int f0 = 0; f0 < p.F && !bad; f0 += FC) {
     for (int t = t0; t < t1 && !bad; ++t) {
       if (tid == 0) {
+        bulk_wait_read();  // the previous pass's y store has read the source-row buffer
         fence_proxy_async();
         mbar_expect_tx(barLoad, 2 * kBox + (FC / 64) * kBox);
         const int cb = p.tile_cb[t];
@@ -107,29 +112,50 @@ __global__ void __launch_bounds__(128) wsb_tile_kernel(const __grid_constant__ W
       tc_fence_after();
     }
     if (bad) break;
-    // epilogue: y[node][f0 .. f0 + FC) += D[row]
+    // epilogue: y[rows][f0 .. f0 + FC) += D, the y tile through the
+    // source-row buffer (64-column boxes, 128-byte swizzle)
+    if (tid == 0) {
+      fence_proxy_async();
+      mbar_expect_tx(barY, (FC / 64) * kBox);
+#pragma unroll
+      for (int n = 0; n < FC / 64; ++n) tma_tile2d(sX + n * kBox, &p.my, f0 + n * 64, rb * kRows, barY);
+    }
+    pendY = true;
+    {
+      const bool ok = mbar_wait(barY, nY & 1);
+      if (__syncthreads_or(!ok)) { bad = true; break; }
+    }
+    ++nY;
+    pendY = false;
 #pragma unroll
     for (int c = 0; c < FC / 32; ++c) {
       float d[32];
       tmem_ld32(tD + lane_off + c * 32, d);
       tmem_wait_ld();
-      if (node < p.N) {
-        uint4* yr = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.y) +
-                                             int64_t(node) * p.F + f0 + c * 32);
+      uint8_t* row = sX + (c / 2) * kBox + tid * 128;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint4 u = yr[q];
-          const uint32_t in[4] = {u.x, u.y, u.z, u.w};
-          uint32_t w[4];
+      for (int q = 0; q < 4; ++q) {
+        uint4* ptr = reinterpret_cast<uint4*>(row + ((((c % 2) * 4 + q) ^ (tid & 7)) * 16));
+        const uint4 u = *ptr;
+        const uint32_t in[4] = {u.x, u.y, u.z, u.w};
+        uint32_t w[4];
 #pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const float lo = __uint_as_float(in[h] << 16) + d[q * 8 + 2 * h];
-            const float hi = __uint_as_float(in[h] & 0xffff0000u) + d[q * 8 + 2 * h + 1];
-            w[h] = bf16x2_bits(lo, hi);
-          }
-          yr[q] = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int h = 0; h < 4; ++h) {
+          const float lo = __uint_as_float(in[h] << 16) + d[q * 8 + 2 * h];
+          const float hi = __uint_as_float(in[h] & 0xffff0000u) + d[q * 8 + 2 * h + 1];
+          w[h] = bf16x2_bits(lo, hi);
         }
+        *ptr = make_uint4(w[0], w[1], w[2], w[3]);
       }
+    }
+    fence_proxy_async();  // generic stores of the sums -> visible to the TMA store
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {
+#pragma unroll
+      for (int n = 0; n < FC / 64; ++n) tma_store2d(&p.my, f0 + n * 64, rb * kRows, sX + n * kBox);
+      bulk_commit();
     }
     tc_fence_before();
     __syncthreads();  // D is read out before the next column pass overwrites it
@@ -140,7 +166,9 @@ __global__ void __launch_bounds__(128) wsb_tile_kernel(const __grid_constant__ W
     atomicOr(p.err, 4);
     if (pendLoad) mbar_wait(barLoad, nLoad & 1);
     if (pendMma) mbar_wait(barMma, nMma & 1);
+    if (pendY) mbar_wait(barY, nY & 1);
   }
+  if (tid == 0) bulk_wait();  // the y stores have completed
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
