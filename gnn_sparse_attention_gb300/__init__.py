@@ -7,8 +7,11 @@ not touch the GPU.  The public Python names mirror the C entry points.
 from __future__ import annotations
 
 __all__ = ["Score", "Plan", "GattnError", "gattn_plan_create", "gattn_plan_get_info",
-           "gattn_plan_export", "gattn_workspace_size", "gattn_fwd", "gattn_bwd", "gattn_bwd_dq", "gattn_bwd_dkdv", "gattn_plan_check_errors", "gattn_fwd_noalloc",
-           "gattn_version", "load_library"]
+           "gattn_plan_export", "gattn_plan_export_tiles", "gattn_plan_export_tile_bwd",
+           "gattn_workspace_size", "gattn_fwd", "gattn_bwd", "gattn_bwd_dq", "gattn_bwd_dkdv",
+           "gattn_plan_check_errors", "gattn_fwd_noalloc", "gattn_reorder", "gattn_permute_csr",
+           "gattn_permute_rows", "gattn_pool_workspace_size", "gattn_pool_fwd", "gattn_pool_bwd",
+           "gattn_spmm_workspace_size", "gattn_spmm", "gattn_version", "load_library"]
 
 
 def __getattr__(name):
