@@ -68,7 +68,13 @@ def library_path() -> str:
 
 
 def load_library(path: str | None = None):
-    """Load the CUDA library (no compute call is made)."""
+    """Load the CUDA library (no compute call is made).
+
+    Without ``path`` the in-tree build is loaded once and cached for every
+    call of this module.  With ``path`` that library is loaded and returned
+    but not cached: the module's own calls keep using the default library
+    unless the caller assigns the result to ``binding._lib``.
+    """
     global _lib
     with _lock:
         if _lib is not None and path is None:
