@@ -18,6 +18,7 @@ MUTANTS = {
     "softmax_jacobian_sign": ("p[e * H + h] * (ds[e * H + h] - delta)",
                               "p[e * H + h] * (ds[e * H + h] + delta)"),
     "leaky_grad_no_slope": ("z > 0.0 ? 1.0 : slope;", "z > 0.0 ? 1.0 : 0.0;"),
+    "leaky_grad_one_at_kink": ("z > 0.0 ? 1.0 : slope;", "z >= 0.0 ? 1.0 : slope;"),
     "gather_destination_value": ("const double* v = V + (int64_t)col[e] * HD;",
                                  "const double* v = V + node_of(row_ids, r) * HD;"),
     "lse_without_log": ("lse[r * H + h] = m + log(z);", "lse[r * H + h] = m + z;"),
@@ -63,6 +64,7 @@ def _battery():
         ("dense_gatv2", lambda: pins.test_dense_bruteforce(oracle.GATV2, 1, 24, 2, 4)),
         ("fd_dot", lambda: pins.test_finite_differences(oracle.DOT)),
         ("fd_gatv2", lambda: pins.test_finite_differences(oracle.GATV2)),
+        ("kink", lambda: pins.test_leaky_derivative_at_zero_takes_the_slope(0.2)),
         ("plan", lambda: pins.test_plan_recount(10, 200, 6.0, 8, 4)),
         ("plan_T", lambda: pins.test_plan_recount(11, 500, 20.0, 32, 16)),
         ("tile_split", lambda: tile_pins.test_tile_split_recount(0, 300, [(0, 0), (1, 2)], 0.3,

@@ -227,6 +227,38 @@ def test_finite_differences(kind):
     assert checked > 3 * N * H * D * 0.9
 
 
+@pytest.mark.parametrize("slope", [0.0, 0.2, 0.5])
+def test_leaky_derivative_at_zero_takes_the_slope(slope):
+    """The pages fix no derivative of LeakyReLU at its kink; the reading is
+    LReLU'(0) = slope.  With x_r = -x_l every self-loop has z = 0 exactly.
+    Moving x_l[i] down puts that edge on the linear side of slope s, so a
+    left finite difference must equal the analytic gradient there, and a
+    right one (which sees slope 1) must not."""
+    N, H, D = 6, 2, 3
+    indptr, indices = _graph(31, N, 3.0, self_loops=True)
+    Q, K, V, G = _feats(31, N, H, D)
+    K = -Q
+    a = np.random.default_rng(31).standard_normal((H, D))
+    dQ = oracle.backward(indptr, indices, Q, K, V, G, kind=oracle.GATV2, a=a, slope=slope)[0]
+
+    def loss(Qx):
+        out, _ = oracle.forward(indptr, indices, Qx, K, V, kind=oracle.GATV2, a=a, slope=slope)
+        return float((out * G).sum())
+
+    h = 1e-7
+    L0 = loss(Q)
+    far = 0.0
+    for idx in np.ndindex(Q.shape):
+        Qx = Q.copy()
+        Qx[idx] -= h
+        left = (L0 - loss(Qx)) / h
+        Qx[idx] += 2 * h
+        right = (loss(Qx) - L0) / h
+        assert abs(left - dQ[idx]) <= 1e-5 * max(1.0, abs(dQ[idx])), (idx, left, dQ[idx])
+        far = max(far, abs(right - dQ[idx]))
+    assert far > 1e-3  # the right side sees slope 1: the kink convention is observable
+
+
 # ----------------------------------------------------------------------------
 # plan
 # ----------------------------------------------------------------------------
