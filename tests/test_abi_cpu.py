@@ -55,6 +55,9 @@ def test_host_argument_checks(lib):
     assert lib.gattn_plan_get_info(None, None) == 1
     assert lib.gattn_plan_destroy(None) == 0
     assert lib.gattn_plan_export(None, *([None] * 11)) == 1
+    assert lib.gattn_plan_export_tiles(None, *([None] * 5)) == 1
+    assert lib.gattn_plan_export_tile_bwd(None, *([None] * 7)) == 1
+    assert b"plan is NULL" in lib.gattn_last_error()
     n = ctypes.c_size_t()
     assert lib.gattn_workspace_size(None, 2, 16, 0, ctypes.byref(n)) == 1
 
