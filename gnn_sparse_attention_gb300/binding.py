@@ -27,8 +27,8 @@ EXPORTED = ("gattn_plan_create", "gattn_plan_destroy", "gattn_plan_get_info",
             "gattn_bwd_dq", "gattn_bwd_dkdv", "gattn_plan_check_errors", "gattn_fwd_noalloc",
             "gattn_plan_export_tiles", "gattn_plan_export_tile_bwd", "gattn_reorder", "gattn_permute_csr",
             "gattn_permute_rows", "gattn_pool_workspace_size", "gattn_pool_fwd",
-            "gattn_pool_bwd", "gattn_spmm_workspace_size", "gattn_spmm", "gattn_last_error",
-            "gattn_version")
+            "gattn_pool_bwd", "gattn_spmm_workspace_size", "gattn_spmm",
+            "gattn_plan_set_wait_test", "gattn_last_error", "gattn_version")
 
 
 class GattnError(RuntimeError):
@@ -113,7 +113,8 @@ def load_library(path: str | None = None):
         lib.gattn_pool_bwd.argtypes = [P, i32, ctypes.c_int, P, P, P, P, sz, P]
         lib.gattn_spmm_workspace_size.argtypes = [P, i32, ctypes.c_int, ctypes.POINTER(sz)]
         lib.gattn_spmm.argtypes = [P, i32, ctypes.c_int, P, P, P, i32, P, sz, P]
-        for name in EXPORTED[:20]:
+        lib.gattn_plan_set_wait_test.argtypes = [P, i32]
+        for name in EXPORTED[:22]:
             getattr(lib, name).restype = st
         lib.gattn_last_error.restype = ctypes.c_char_p
         lib.gattn_last_error.argtypes = []
@@ -493,10 +494,20 @@ def gattn_plan_check_errors(plan: Plan) -> None:
     _check(load_library().gattn_plan_check_errors(plan.handle), "gattn_plan_check_errors")
 
 
+def gattn_plan_set_wait_test(plan: Plan, fail_first_wait: bool) -> None:
+    """Test hook of the bounded-wait failure path: while set, every warp of the
+    attention passes run with ``plan`` gives up its first wait at once (and
+    still waits for the copies it issued), so the next
+    gattn_plan_check_errors raises GATTN_ERR_TIMEOUT."""
+    _check(load_library().gattn_plan_set_wait_test(plan.handle, int(bool(fail_first_wait))),
+           "gattn_plan_set_wait_test")
+
+
 def gattn_fwd_noalloc(plan: Plan, Q, K, V, score: Score, out, lse, stream=None):
     """Forward pass that allocates nothing: ``out`` and ``lse`` must be given,
     and the heavy-chunk scratch comes from the library's fixed 32 MiB array
-    (for callers that cannot allocate device memory at call time)."""
+    (for callers that cannot allocate device memory where they run the layer,
+    e.g. under an allocator or memory pool they do not own)."""
     H, D = _shape(Q)
     sc = score._struct()
     _check(load_library().gattn_fwd_noalloc(plan.handle, H, D, _dtype_code(Q.dtype), _ptr(Q),

@@ -372,18 +372,41 @@ gattn_status gattn_plan_export_tile_bwd(const gattn_plan* plan, int64_t* n_tcols
 
 gattn_status gattn_plan_check_errors(const gattn_plan* plan) {
   GATTN_REQUIRE(plan, GATTN_ERR_INVALID_ARG, "plan is NULL");
+  const Plan& p = plan->p;
   cudaError_t e = cudaDeviceSynchronize();
   int32_t flag = 0;
-  if (e == cudaSuccess) e = cudaMemcpy(&flag, plan->p.err, 4, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemcpy(&flag, p.err, 4, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) {
     set_error("checking the plan's error flag failed: %s", cudaGetErrorString(e));
     return GATTN_ERR_CUDA;
   }
   if (flag) {
-    cudaMemset(plan->p.err, 0, 4);
+    // A warp that gave up left its items unfinished, so an arrival counter
+    // of a merge tree may hold a count of chunks that never completed: clear
+    // every counter (the device is idle) so that the next call starts clean.
+    struct {
+      int32_t* c;
+      int64_t n;
+    } cnt[] = {{p.cnt_fwd, p.n_inner},       {p.cnt_dq, p.n_inner},
+               {p.cnt_dkv, p.n_inner_src},   {p.cnt_da, 1},
+               {p.cnt_fwd_r, p.n_inner_r},   {p.cnt_dq_r, p.n_inner_r},
+               {p.cnt_dkv_r, p.n_inner_src_r}, {p.err, 1}};
+    for (const auto& x : cnt)
+      if (x.c && e == cudaSuccess) e = cudaMemset(x.c, 0, size_t(x.n > 0 ? x.n : 1) * 4);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+      set_error("clearing the plan's counters failed: %s", cudaGetErrorString(e));
+      return GATTN_ERR_CUDA;
+    }
     set_error("a kernel gave up waiting for its asynchronous copies");
     return GATTN_ERR_TIMEOUT;
   }
+  return GATTN_OK;
+}
+
+gattn_status gattn_plan_set_wait_test(gattn_plan* plan, int32_t fail_first_wait) {
+  GATTN_REQUIRE(plan, GATTN_ERR_INVALID_ARG, "plan is NULL");
+  plan->p.fail_first_wait = fail_first_wait != 0;
   return GATTN_OK;
 }
 
@@ -448,6 +471,7 @@ gattn_status gattn_fwd(const gattn_plan* plan, int32_t H, int32_t D, gattn_dtype
   f.tree = tiles ? Tree{p.parent_r, p.kids_r, p.n_chunks_r, p.cnt_fwd_r}
                  : Tree{p.parent, p.kids, p.n_chunks, p.cnt_fwd};
   f.err = p.err;
+  f.fail_first_wait = p.fail_first_wait;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int sb = tiles ? stage_bytes(p.M_res, p.n_chunks_r + p.n_light_r)
                        : stage_bytes(p.M, p.n_chunks + p.n_light);
@@ -501,10 +525,10 @@ static gattn_status bwd_common(const gattn_plan* plan, int32_t H, int32_t D, gat
   b->H = H;
   b->D = D;
   b->rows16 = (H % 4 == 0) && aligned(lse, 16);
-  b->delta16 = (H % 2 == 0);
   b->da_part = reinterpret_cast<float*>(ws + w->da_part);
   b->da_cnt = plan->p.cnt_da;
   b->err = plan->p.err;
+  b->fail_first_wait = plan->p.fail_first_wait;
   return GATTN_OK;
 }
 
@@ -612,8 +636,7 @@ gattn_status gattn_bwd_dkdv(const gattn_plan* plan, int32_t H, int32_t D, gattn_
     const int64_t HD = int64_t(H) * D;
     if (!encode_rows_map(&b.mi0, K, es, bf, p.N, HD) || !encode_rows_map(&b.mi1, V, es, bf, p.N, HD) ||
         !encode_rows_map(&b.me0, Q, es, bf, p.N, HD) ||
-        !encode_rows_map(&b.me1, dout, es, bf, p.N, HD) ||
-        (b.delta16 && !encode_rows_map(&b.ms0, b.delta, 4, false, p.N, 2 * H)))
+        !encode_rows_map(&b.me1, dout, es, bf, p.N, HD))
       return GATTN_ERR_CUDA;
   }
   b.idx = tiles ? p.csc_dst_r : p.csc_dst;

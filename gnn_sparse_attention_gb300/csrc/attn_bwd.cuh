@@ -29,8 +29,8 @@ namespace gattn {
 struct BwdParams {
   // row-gather maps (tma.cuh).  Pass 1: mi0..mi2 = Q, dO, O (item rows),
   // me0, me1 = K, V (edge rows), ms0 = lse (item stat rows).  Pass 2: mi0,
-  // mi1 = K, V (item rows), me0, me1 = Q, dO (edge rows), ms0 = the
-  // (lse log2(e), Delta) rows (edge stat rows).
+  // mi1 = K, V (item rows), me0, me1 = Q, dO (edge rows); the edges'
+  // (lse log2(e), Delta) rows are copied by the lanes.
   CUtensorMap mi0, mi1, mi2, me0, me1, ms0;
   const int4* items;   // plan items (w = heavy id of a chunk)
   const int4* sorted;  // items by decreasing length
@@ -54,12 +54,12 @@ struct BwdParams {
   float slope;
   int H, D;
   int rows16;          // lse rows are gathered by TMA (H % 4 == 0, lse 16-B aligned)
-  int delta16;         // (lse, Delta) rows are gathered by TMA (H even: whole 16-byte pieces)
   float* part;         // partials per tree slot: pass 1 [slots][HD], pass 2 [slots][2*HD]
   Tree tree;           // merge trees of the heavy items of this pass
   float* da_part;      // [gridDim.x][HD]
   int32_t* da_cnt;
   int32_t* err;        // set when a wait gives up
+  int fail_first_wait; // nonzero: every warp's first wait expires at once (failure-path test)
 };
 
 // Largest per-node fp32 row (lse or Delta): H <= RB/16 floats, padded to 16 B.
@@ -72,8 +72,15 @@ template <typename T, int RB, int SB>
 struct CsrShape {
   using L = Lay<T, RB, SB>;
   static constexpr int LS = StatBytes<RB>::value;
-  // per item slot: Q, dO, O rows and the lse row; per edge: K row, V row
-  static constexpr int OL = 3 * L::IR * RB;             // lse sets
+  // Item rows inline (attn_pipe.cuh, BundleCursor) wherever whole 4-row sets
+  // remain and at least one edge is left after the two item positions: a
+  // starting item's Q and dO rows take its group's K and V slots of the last
+  // edge position, its O row the K slot of the one before.  Otherwise the Q,
+  // dO and O rows have a region of their own (IR slots each).
+  static constexpr int RES = (L::G >= 4 && L::SE > 2) ? 2 : 0;
+  static constexpr int IRS = RES ? 0 : L::IR;
+  // [IRS Q, dO, O rows] [lse sets] [B K rows] [B V rows]
+  static constexpr int OL = 3 * IRS * RB;               // lse sets
   static constexpr int OK = OL + L::QR / 4 * L::SSB;    // K rows
   static constexpr int OV = OK + L::B * RB;             // V rows
   static constexpr int STAGE = OV + L::B * RB;
@@ -83,15 +90,21 @@ struct CsrShape {
   static constexpr int SMEM = WARPS * WARP_BYTES;
 };
 
-template <typename T, int RB, int SB>
+template <typename T, int RB, int SB, int DB>
 struct CscShape {
   using L = Lay<T, RB, SB>;
-  static constexpr int LS = StatBytes<RB>::value;
-  // per item slot: K, V rows; per edge: Q row, dO row, lse row, Delta row
-  static constexpr int OQE = 2 * L::IR * RB;            // Q rows of the edges
+  static constexpr int H = RB / DB;                     // heads
+  // Item rows inline where whole 4-row sets and an edge remain: a starting
+  // item's K and V rows take its group's Q and dO slots of the last edge
+  // position.  Otherwise K and V rows have a region of their own.
+  static constexpr int RES = (L::G >= 4 && L::SE > 1) ? 1 : 0;
+  static constexpr int IRS = RES ? 0 : L::IR;
+  // [IRS K, V rows] [B Q rows] [B dO rows] [B (lse log2 e, Delta) rows]
+  static constexpr int SROW = 8 * H;                    // bytes of one (lse, Delta) row
+  static constexpr int OQE = 2 * IRS * RB;              // Q rows of the edges
   static constexpr int OGE = OQE + L::B * RB;           // dO rows
-  static constexpr int OLS = OGE + L::B * RB;           // (lse, Delta) sets: 4 rows of 2H floats
-  static constexpr int STAGE = OLS + L::B / 4 * 2 * L::SSB;
+  static constexpr int OLS = OGE + L::B * RB;           // (lse, Delta) rows
+  static constexpr int STAGE = align128(OLS + L::B * SROW);
   static constexpr int WARP_BYTES = align128(kStages * STAGE + L::META);
   static constexpr int WARPS = WarpsFor<WARP_BYTES>::value;
   static constexpr int THREADS = 32 * WARPS;
@@ -160,16 +173,21 @@ __global__ void __launch_bounds__(CsrShape<T, RB, SB>::THREADS) bwd_csr_kernel(c
 
   const int64_t warp = (int64_t(blockIdx.x) * Sh::THREADS + threadIdx.x) >> 5;
   const int64_t nwarps = (int64_t(gridDim.x) * Sh::THREADS) >> 5;
-  BundleCursor<G, SE> cur;
+  using Cur = BundleCursor<G, SE, Sh::RES>;
+  Cur cur;
   cur.start(p.sorted, p.n_items, p.idx, p.N, warp, nwarps, ring.items, lane);
 
-  // stage: [IR][Q row] [IR][dO row] [IR][O row] [QR/4][lse set] [B][K row]
+  // stage: [IRS][Q row] [IRS][dO row] [IRS][O row] [QR/4][lse set] [B][K row]
   // [B][V row].  TMA gathers from lane 0 (item rows only for 4-row sets that
   // hold a starting item, pad row N elsewhere; with fewer than 4 groups a
-  // warp copies just the starting items' rows); lse rows by gather when
-  // they are whole 16-byte pieces, else by 4-byte cp.async.
-  constexpr int OQ = 0, ODO = L::IR * RB, OO = 2 * L::IR * RB;
+  // warp copies just the starting items' rows; inline item rows go to the
+  // K / V slots of the last two edge positions of a stage that starts a
+  // bundle); lse rows by gather when they are whole 16-byte pieces, else by
+  // 4-byte cp.async.
+  constexpr int OQ = 0, ODO = Sh::IRS * RB, OO = 2 * Sh::IRS * RB;
   constexpr int OL = Sh::OL, OK = Sh::OK, OV = Sh::OV;
+  // inline: slots of a starting item's Q / dO rows (last edge position) and O row
+  constexpr int K1 = (SE - 1) * G / 4, K2 = (SE - 2) * G / 4;
   auto issue = [&](int s) {
     const int4* dsc = ring.desc_at(s);
     if (lane == 0 && dsc[0].x != -3) {
@@ -186,14 +204,20 @@ __global__ void __launch_bounds__(CsrShape<T, RB, SB>::THREADS) bwd_csr_kernel(c
       }
       const uint32_t ibytes = L::IBULK ? item_rows<L>(qr[0], p.N) * 3 * RB
                                        : __popc(qmask) * 3 * L::SET_BYTES;
+      // inline: a stage that starts a bundle gathers edge rows only below K2
+      const int ne = (Sh::RES > 0 && qmask) ? K2 : B / 4;
       fence_proxy_async();
       mbar_expect_tx(bar, ibytes + (p.rows16 ? __popc(qmask) * 16 * p.H : 0) +
-                              2 * (B / 4) * L::SET_BYTES);
+                              2 * ne * L::SET_BYTES);
 #pragma unroll
       for (int q4 = 0; q4 < L::QR / 4; ++q4)
         if ((qmask >> q4) & 1) {
           const int4 r = qr[q4];
-          if constexpr (L::IBULK) {
+          if constexpr (Sh::RES > 0) {
+            L::gather(st + OK, 4 * (K1 + q4), &p.mi0, r.x, r.y, r.z, r.w, bar);
+            L::gather(st + OV, 4 * (K1 + q4), &p.mi1, r.x, r.y, r.z, r.w, bar);
+            L::gather(st + OK, 4 * (K2 + q4), &p.mi2, r.x, r.y, r.z, r.w, bar);
+          } else if constexpr (L::IBULK) {
             fetch_item_rows<L>(st + OQ, p.Q, r, p.N, bar);
             fetch_item_rows<L>(st + ODO, p.dO, r, p.N, bar);
             fetch_item_rows<L>(st + OO, p.O, r, p.N, bar);
@@ -206,9 +230,11 @@ __global__ void __launch_bounds__(CsrShape<T, RB, SB>::THREADS) bwd_csr_kernel(c
         }
 #pragma unroll
       for (int b4 = 0; b4 < B / 4; ++b4) {
-        const int4 r = ring.eset(s, b4);
-        L::gather(st + OK, 4 * b4, &p.me0, r.x, r.y, r.z, r.w, bar);
-        L::gather(st + OV, 4 * b4, &p.me1, r.x, r.y, r.z, r.w, bar);
+        if (b4 < ne) {
+          const int4 r = ring.eset(s, b4);
+          L::gather(st + OK, 4 * b4, &p.me0, r.x, r.y, r.z, r.w, bar);
+          L::gather(st + OV, 4 * b4, &p.me1, r.x, r.y, r.z, r.w, bar);
+        }
       }
     }
     if (!p.rows16) {  // lse rows of starting items by 4-byte copies
@@ -239,7 +265,7 @@ __global__ void __launch_bounds__(CsrShape<T, RB, SB>::THREADS) bwd_csr_kernel(c
     __syncwarp();
     const int4* dsc = ring.desc_at(i);
     if (dsc[0].x == -3) break;
-    if (!__all_sync(FULL, ring.wait_rows(i, p.err, lane))) break;
+    if (!__all_sync(FULL, ring.wait_rows(i, p.err, lane, ring.limit_at(i, p.fail_first_wait)))) break;
     const int4 d = dsc[g];
     const bool act = d.x >= 0;
     const int cnt = act ? (d.z & kCntMask) : 0;
@@ -253,10 +279,18 @@ __global__ void __launch_bounds__(CsrShape<T, RB, SB>::THREADS) bwd_csr_kernel(c
       for (int c = 0; c < NC; ++c) {
         float2 o[PP];
         if (first) {
-          const int x = L::offI(g, (t * NC + c) * 16);
-          PR::load(lds16(st + OQ + x), q[c]);
-          PR::load(lds16(st + ODO + x), gq[c]);
-          PR::load(lds16(st + OO + x), o);
+          const int x = (t * NC + c) * 16;
+          if constexpr (Sh::RES > 0) {
+            const int xa = L::off(Cur::slot(g, SE - 1), x), xb = L::off(Cur::slot(g, SE - 2), x);
+            PR::load(lds16(st + OK + xa), q[c]);
+            PR::load(lds16(st + OV + xa), gq[c]);
+            PR::load(lds16(st + OK + xb), o);
+          } else {
+            const int xi = L::offI(g, x);
+            PR::load(lds16(st + OQ + xi), q[c]);
+            PR::load(lds16(st + ODO + xi), gq[c]);
+            PR::load(lds16(st + OO + xi), o);
+          }
         } else {
 #pragma unroll
           for (int v = 0; v < PP; ++v) o[v] = f2s(0.f);
@@ -306,7 +340,7 @@ __global__ void __launch_bounds__(CsrShape<T, RB, SB>::THREADS) bwd_csr_kernel(c
       float2 kf[NC][PP];
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
-        const int off = L::off(g * SE + k, (t * NC + c) * 16);
+        const int off = L::off(Cur::slot(g, k), (t * NC + c) * 16);
         float2 vf[PP];
         PR::load(valid ? lds16(ks + off) : make_uint4(0, 0, 0, 0), kf[c]);
         PR::load(valid ? lds16(vs + off) : make_uint4(0, 0, 0, 0), vf);
@@ -468,9 +502,9 @@ __global__ void __launch_bounds__(CsrShape<T, RB, SB>::THREADS) bwd_csr_kernel(c
 // pass 2: CSC
 // ---------------------------------------------------------------------------
 template <typename T, int RB, int DB, int KIND, int SB>
-__global__ void __launch_bounds__(CscShape<T, RB, SB>::THREADS) bwd_csc_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(CscShape<T, RB, SB, DB>::THREADS) bwd_csc_kernel(const __grid_constant__ BwdParams p) {
   using L = Lay<T, RB, SB>;
-  using Sh = CscShape<T, RB, SB>;
+  using Sh = CscShape<T, RB, SB, DB>;
   using PR = Pairs<T>;
   constexpr int NC = L::NC, TPR = L::TPR, G = L::G, SE = L::SE, B = L::B;
   constexpr int PP = PR::P, S = kStages;
@@ -505,20 +539,27 @@ __global__ void __launch_bounds__(CscShape<T, RB, SB>::THREADS) bwd_csc_kernel(c
 
   const int64_t warp = (int64_t(blockIdx.x) * Sh::THREADS + threadIdx.x) >> 5;
   const int64_t nwarps = (int64_t(gridDim.x) * Sh::THREADS) >> 5;
-  BundleCursor<G, SE> cur;
+  using Cur = BundleCursor<G, SE, Sh::RES>;
+  Cur cur;
   cur.start(p.sorted, p.n_items, p.idx, p.N, warp, nwarps, ring.items, lane);
 
-  // stage: [IR][K row] [IR][V row] [B][Q row] [B][dO row] [B][lse row]
-  // [B][Delta row].  TMA gathers from lane 0 (pad row N in unused slots;
-  // with fewer than 4 groups a warp copies just the starting items' rows);
-  // stat rows by gather when they are whole 16-byte pieces, else by 4-byte
-  // cp.async.
-  constexpr int OKI = 0, OVI = L::IR * RB;
+  // stage: [IRS][K row] [IRS][V row] [B][Q row] [B][dO row] [B][(lse log2 e,
+  // Delta) row].  TMA gathers from lane 0 (pad row N in unused slots; with
+  // fewer than 4 groups a warp copies just the starting items' rows; inline
+  // item rows go to the Q / dO slots of the last edge position of a stage
+  // that starts a bundle).  The 8H-byte statistic rows of the edges are
+  // copied by the lanes with cp.async (16-byte pieces; 8 bytes when H = 1):
+  // many small independent copies are cheaper there than row gathers.
+  constexpr int OKI = 0, OVI = Sh::IRS * RB;
   constexpr int OQE = Sh::OQE, OGE = Sh::OGE, OLS = Sh::OLS;
-  constexpr int SS2 = 2 * L::SSB;  // bytes of a set of 4 (lse, Delta) rows
+  constexpr int SROW = Sh::SROW;
+  constexpr int PB = SROW < 16 ? SROW : 16;   // bytes of one statistic piece
+  constexpr int PPR = SROW / PB;             // pieces per row
+  constexpr int K1 = (SE - 1) * G / 4;       // inline: first set of the last edge position
   auto issue = [&](int s) {
     const int4* dsc = ring.desc_at(s);
-    if (lane == 0 && dsc[0].x != -3) {
+    const bool live = dsc[0].x != -3;
+    if (lane == 0 && live) {
       uint8_t* st = ring.stage_at(s);
       uint64_t* bar = ring.bar_at(s);
       int4 qr[L::QR / 4];
@@ -530,16 +571,19 @@ __global__ void __launch_bounds__(CscShape<T, RB, SB>::THREADS) bwd_csc_kernel(c
                          qr[q4].w != p.N;
         qmask |= uint32_t(any) << q4;
       }
-      const uint32_t eset = 2 * L::SET_BYTES + (p.delta16 ? 32 * p.H : 0);
       const uint32_t ibytes = L::IBULK ? item_rows<L>(qr[0], p.N) * 2 * RB
                                        : __popc(qmask) * 2 * L::SET_BYTES;
+      const int ne = (Sh::RES > 0 && qmask) ? K1 : B / 4;  // sets of edge rows
       fence_proxy_async();
-      mbar_expect_tx(bar, ibytes + (B / 4) * eset);
+      mbar_expect_tx(bar, ibytes + 2 * ne * L::SET_BYTES);
 #pragma unroll
       for (int q4 = 0; q4 < L::QR / 4; ++q4)
         if ((qmask >> q4) & 1) {
           const int4 r = qr[q4];
-          if constexpr (L::IBULK) {
+          if constexpr (Sh::RES > 0) {
+            L::gather(st + OQE, 4 * (K1 + q4), &p.mi0, r.x, r.y, r.z, r.w, bar);
+            L::gather(st + OGE, 4 * (K1 + q4), &p.mi1, r.x, r.y, r.z, r.w, bar);
+          } else if constexpr (L::IBULK) {
             fetch_item_rows<L>(st + OKI, p.K, r, p.N, bar);
             fetch_item_rows<L>(st + OVI, p.V, r, p.N, bar);
           } else {
@@ -549,19 +593,25 @@ __global__ void __launch_bounds__(CscShape<T, RB, SB>::THREADS) bwd_csc_kernel(c
         }
 #pragma unroll
       for (int b4 = 0; b4 < B / 4; ++b4) {
-        const int4 r = ring.eset(s, b4);
-        L::gather(st + OQE, 4 * b4, &p.me0, r.x, r.y, r.z, r.w, bar);
-        L::gather(st + OGE, 4 * b4, &p.me1, r.x, r.y, r.z, r.w, bar);
-        if (p.delta16) tma_gather4(st + OLS + b4 * SS2, &p.ms0, 0, r.x, r.y, r.z, r.w, bar);
+        if (b4 < ne) {
+          const int4 r = ring.eset(s, b4);
+          L::gather(st + OQE, 4 * b4, &p.me0, r.x, r.y, r.z, r.w, bar);
+          L::gather(st + OGE, 4 * b4, &p.me1, r.x, r.y, r.z, r.w, bar);
+        }
       }
     }
-    if (!p.delta16) {  // stat rows of the edges by 4-byte copies
-      const int4 dg = lane < G ? dsc[lane] : make_int4(-1, 0, 0, 0);
-      const bool live = dsc[0].x != -3;
-      const int ge = (lane / SE) & 31;
-      const int cn = __shfl_sync(FULL, dg.x >= 0 ? (dg.z & kCntMask) : 0, ge);
-      const int jv = (live && lane < B && lane % SE < cn) ? ring.ix_at(s)[lane] : -1;
-      copy_stat_rows<SS2>(ring.stage_at(s) + OLS, p.delta, jv, B, 2 * p.H, lane);
+    if (live) {  // statistic rows of the stage's edges (pad slots skipped)
+      uint8_t* sd = ring.stage_at(s) + OLS;
+      const int* ixs = ring.ix_at(s);
+      for (int x = lane; x < B * PPR; x += 32) {
+        const int b = x / PPR, pc = x % PPR;
+        const int j = ixs[b];
+        if (j != p.N) {
+          const float* src = p.delta + int64_t(j) * 2 * Sh::H + pc * (PB / 4);
+          if constexpr (PB == 16) cp_async16(sd + b * SROW + pc * PB, src);
+          else cp_async8(sd + b * SROW + pc * PB, src);
+        }
+      }
     }
     __syncwarp();
     cp_async_commit();
@@ -588,7 +638,7 @@ __global__ void __launch_bounds__(CscShape<T, RB, SB>::THREADS) bwd_csc_kernel(c
     __syncwarp();
     const int4* dsc = ring.desc_at(i);
     if (dsc[0].x == -3) break;
-    if (!__all_sync(FULL, ring.wait_rows(i, p.err, lane))) break;
+    if (!__all_sync(FULL, ring.wait_rows(i, p.err, lane, ring.limit_at(i, p.fail_first_wait)))) break;
     const int4 d = dsc[g];
     const bool act = d.x >= 0;
     const int cnt = act ? (d.z & kCntMask) : 0;
@@ -597,9 +647,15 @@ __global__ void __launch_bounds__(CscShape<T, RB, SB>::THREADS) bwd_csc_kernel(c
     if (act && (d.z & kFirst)) {
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
-        const int x = L::offI(g, (t * NC + c) * 16);
-        PR::load(lds16(st + OKI + x), k[c]);
-        PR::load(lds16(st + OVI + x), vv[c]);
+        const int x = (t * NC + c) * 16;
+        if constexpr (Sh::RES > 0) {
+          const int xa = L::off(Cur::slot(g, SE - 1), x);
+          PR::load(lds16(st + OQE + xa), k[c]);
+          PR::load(lds16(st + OGE + xa), vv[c]);
+        } else {
+          PR::load(lds16(st + OKI + L::offI(g, x)), k[c]);
+          PR::load(lds16(st + OVI + L::offI(g, x)), vv[c]);
+        }
 #pragma unroll
         for (int v = 0; v < PP; ++v) {
           if (!GAT) k[c][v] = f2mul(k[c][v], f2s(p.qmul));
@@ -624,7 +680,7 @@ __global__ void __launch_bounds__(CscShape<T, RB, SB>::THREADS) bwd_csc_kernel(c
       float2 qf[NC][PP], gf[NC][PP];
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
-        const int off = L::off(g * SE + e, (t * NC + c) * 16);
+        const int off = L::off(Cur::slot(g, e), (t * NC + c) * 16);
         PR::load(valid ? lds16(qs + off) : make_uint4(0, 0, 0, 0), qf[c]);
         PR::load(valid ? lds16(gs + off) : make_uint4(0, 0, 0, 0), gf[c]);
         float2 s2 = f2s(0.f), p2 = f2s(0.f);
@@ -645,13 +701,13 @@ __global__ void __launch_bounds__(CscShape<T, RB, SB>::THREADS) bwd_csc_kernel(c
       head_sums<NC, CPH>(scp, sc);
       head_sums<NC, CPH>(dpp, dp);
       if (act && valid) {
-        const int b = g * SE + e, so = (b / 4) * SS2 + (b % 4) * 8 * p.H;
+        const float* srow = reinterpret_cast<const float*>(st + OLS + Cur::slot(g, e) * SROW);
         float pr[HL], ds[HL];
 #pragma unroll
         for (int j = 0; j < HL; ++j) {
           const int hh = head[j * LH::CPL];
-          const float ls2 = reinterpret_cast<const float*>(st + OLS + so)[hh];
-          const float dl = reinterpret_cast<const float*>(st + OLS + so)[p.H + hh];
+          const float ls2 = srow[hh];
+          const float dl = srow[Sh::H + hh];
           pr[j] = ex2((GAT ? sc[j] * kLog2e : sc[j]) - ls2);
           ds[j] = pr[j] * (dp[j] - dl);
         }

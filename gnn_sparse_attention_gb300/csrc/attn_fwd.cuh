@@ -46,13 +46,20 @@ struct FwdParams {
   int pstride;
   Tree tree;           // merge trees of the heavy destinations
   int32_t* err;        // set when a wait gives up
+  int fail_first_wait; // nonzero: every warp's first wait expires at once (failure-path test)
 };
 
 template <typename T, int RB, int SB>
 struct FwdShape {
   using L = Lay<T, RB, SB>;
-  // Q rows of the G items (IR slots), then B K rows and B V rows
-  static constexpr int STAGE = RB * (L::IR + 2 * L::B);
+  // Item rows inline (attn_pipe.cuh, BundleCursor) wherever whole 4-row sets
+  // and at least one edge remain: a starting item's Q row takes the K-row
+  // slot of its group's last edge position.  Otherwise Q rows have a region
+  // of their own (IR slots).
+  static constexpr int RES = (L::G >= 4 && L::SE > 1) ? 1 : 0;
+  static constexpr int IRS = RES ? 0 : L::IR;
+  // [IRS Q rows] then B K rows and B V rows
+  static constexpr int STAGE = RB * (IRS + 2 * L::B);
   static constexpr int WARP_BYTES = align128(kStages * STAGE + L::META);
   static constexpr int WARPS = WarpsFor<WARP_BYTES>::value;
   static constexpr int THREADS = 32 * WARPS;
@@ -105,13 +112,17 @@ __global__ void __launch_bounds__(FwdShape<T, RB, SB>::THREADS) fwd_kernel(const
 
   const int64_t warp = (int64_t(blockIdx.x) * Sh::THREADS + threadIdx.x) >> 5;
   const int64_t nwarps = (int64_t(gridDim.x) * Sh::THREADS) >> 5;
-  BundleCursor<G, SE> cur;
+  using Cur = BundleCursor<G, SE, Sh::RES>;
+  Cur cur;
   cur.start(p.sorted, p.n_items, p.indices, p.N, warp, nwarps, ring.items, lane);
 
   // rows of stage s into its ring slot by TMA gathers issued from lane 0:
   // Q rows of the items that start here (only the 4-row sets that hold one),
   // then the K rows and the V rows of the stage's edges; unused slots gather
-  // the zero-filled pad row N.  Bytes are counted on the slot's barrier.
+  // the zero-filled pad row N.  With inline item rows, a stage that starts a
+  // bundle gathers the Q rows into the K slots of the last edge position and
+  // skips that position's V slots.  Bytes are counted on the slot's barrier.
+  constexpr int OKR = Sh::IRS * RB, OVR = (Sh::IRS + B) * RB;  // K, V row regions
   auto issue = [&](int s) {
     if (lane == 0) {
       const int4* dsc = ring.desc_at(s);
@@ -128,22 +139,39 @@ __global__ void __launch_bounds__(FwdShape<T, RB, SB>::THREADS) fwd_kernel(const
           qmask |= uint32_t(any) << q4;
         }
         fence_proxy_async();
-        const uint32_t ibytes = L::IBULK ? item_rows<L>(qr[0], p.N) * RB
-                                         : __popc(qmask) * L::SET_BYTES;
-        mbar_expect_tx(bar, ibytes + 2 * (B / 4) * L::SET_BYTES);
-        if constexpr (L::IBULK) {
-          fetch_item_rows<L>(st, p.Q, qr[0], p.N, bar);
+        if constexpr (Sh::RES > 0) {
+          constexpr int KS = (SE - 1) * G / 4;  // first 4-row set of the last edge position
+          const int ne = qmask ? KS : B / 4;    // sets of edge rows in this stage
+          mbar_expect_tx(bar, (2 * ne + __popc(qmask)) * L::SET_BYTES);
+#pragma unroll
+          for (int b4 = 0; b4 < B / 4; ++b4) {
+            if (b4 < ne) {
+              const int4 r = ring.eset(s, b4);
+              L::gather(st + OKR, 4 * b4, &p.mk, r.x, r.y, r.z, r.w, bar);
+              L::gather(st + OVR, 4 * b4, &p.mv, r.x, r.y, r.z, r.w, bar);
+            } else if ((qmask >> (b4 - KS)) & 1) {
+              const int4 r = qr[b4 - KS];
+              L::gather(st + OKR, 4 * b4, &p.mq, r.x, r.y, r.z, r.w, bar);
+            }
+          }
         } else {
+          const uint32_t ibytes = L::IBULK ? item_rows<L>(qr[0], p.N) * RB
+                                           : __popc(qmask) * L::SET_BYTES;
+          mbar_expect_tx(bar, ibytes + 2 * (B / 4) * L::SET_BYTES);
+          if constexpr (L::IBULK) {
+            fetch_item_rows<L>(st, p.Q, qr[0], p.N, bar);
+          } else {
 #pragma unroll
-          for (int q4 = 0; q4 < L::QR / 4; ++q4)
-            if ((qmask >> q4) & 1)
-              L::gather(st, 4 * q4, &p.mq, qr[q4].x, qr[q4].y, qr[q4].z, qr[q4].w, bar);
-        }
+            for (int q4 = 0; q4 < L::QR / 4; ++q4)
+              if ((qmask >> q4) & 1)
+                L::gather(st, 4 * q4, &p.mq, qr[q4].x, qr[q4].y, qr[q4].z, qr[q4].w, bar);
+          }
 #pragma unroll
-        for (int b4 = 0; b4 < B / 4; ++b4) {
-          const int4 r = ring.eset(s, b4);
-          L::gather(st + L::IR * RB, 4 * b4, &p.mk, r.x, r.y, r.z, r.w, bar);
-          L::gather(st + (L::IR + B) * RB, 4 * b4, &p.mv, r.x, r.y, r.z, r.w, bar);
+          for (int b4 = 0; b4 < B / 4; ++b4) {
+            const int4 r = ring.eset(s, b4);
+            L::gather(st + OKR, 4 * b4, &p.mk, r.x, r.y, r.z, r.w, bar);
+            L::gather(st + OVR, 4 * b4, &p.mv, r.x, r.y, r.z, r.w, bar);
+          }
         }
       }
     }
@@ -171,7 +199,7 @@ __global__ void __launch_bounds__(FwdShape<T, RB, SB>::THREADS) fwd_kernel(const
     __syncwarp();
     const int4* dsc = ring.desc_at(i);
     if (dsc[0].x == -3) break;
-    if (!__all_sync(FULL, ring.wait_rows(i, p.err, lane))) break;
+    if (!__all_sync(FULL, ring.wait_rows(i, p.err, lane, ring.limit_at(i, p.fail_first_wait)))) break;
     const int4 d = dsc[g];
     const bool act = d.x >= 0;
     const int cnt = act ? (d.z & kCntMask) : 0;
@@ -180,7 +208,9 @@ __global__ void __launch_bounds__(FwdShape<T, RB, SB>::THREADS) fwd_kernel(const
     if (act && (d.z & kFirst)) {
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
-        PR::load(lds16(st + L::offI(g, (t * NC + c) * 16)), q[c]);
+        const int x = (t * NC + c) * 16;
+        PR::load(lds16(Sh::RES ? st + OKR + L::off(Cur::slot(g, SE - 1), x) : st + L::offI(g, x)),
+                 q[c]);
         if (!GAT) {
 #pragma unroll
           for (int v = 0; v < PP; ++v) q[c][v] = f2mul(q[c][v], f2s(p.qmul));
@@ -195,8 +225,8 @@ __global__ void __launch_bounds__(FwdShape<T, RB, SB>::THREADS) fwd_kernel(const
       }
     }
 
-    const uint8_t* ks = st + L::IR * RB;
-    const uint8_t* vs = ks + B * RB;
+    const uint8_t* ks = st + OKR;
+    const uint8_t* vs = st + OVR;
     const int kmax = __reduce_max_sync(FULL, cnt);  // edges of the warp's longest item here
     float sc[SE][HL];
 #pragma unroll
@@ -205,7 +235,7 @@ __global__ void __launch_bounds__(FwdShape<T, RB, SB>::THREADS) fwd_kernel(const
       float part[NC];
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
-        const uint4 kr = k < cnt ? lds16(ks + L::off(g * SE + k, (t * NC + c) * 16)) : make_uint4(0, 0, 0, 0);
+        const uint4 kr = k < cnt ? lds16(ks + L::off(Cur::slot(g, k), (t * NC + c) * 16)) : make_uint4(0, 0, 0, 0);
         float2 kf[PP];
         PR::load(kr, kf);
         float2 a2 = f2s(0.f);
@@ -257,7 +287,7 @@ __global__ void __launch_bounds__(FwdShape<T, RB, SB>::THREADS) fwd_kernel(const
 #pragma unroll
           for (int c = 0; c < NC; ++c) {
             float2 vf[PP];
-            PR::load(lds16(vs + L::off(g * SE + k, (t * NC + c) * 16)), vf);
+            PR::load(lds16(vs + L::off(Cur::slot(g, k), (t * NC + c) * 16)), vf);
 #pragma unroll
             for (int v = 0; v < PP; ++v) acc[c][v] = f2fma(f2s(pk[LH::of(c)]), vf[v], acc[c][v]);
           }

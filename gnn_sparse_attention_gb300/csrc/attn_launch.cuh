@@ -67,7 +67,7 @@ struct Case {
     if constexpr (!ok) {
       return GATTN_ERR_UNSUPPORTED;
     } else {
-      using Sh = CscShape<T, RB, SB>;
+      using Sh = CscShape<T, RB, SB, DB>;
       static int cache[2] = {0, 0};
       auto k = kind == GATTN_SCORE_DOT ? bwd_csc_kernel<T, RB, DB, GATTN_SCORE_DOT, SB>
                                        : bwd_csc_kernel<T, RB, DB, GATTN_SCORE_GATV2, SB>;

@@ -127,6 +127,10 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dst)), "l"(src)
                : "memory");
 }
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(smem_u32(dst)), "l"(src)
                : "memory");
@@ -172,9 +176,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait for the completion of the barrier phase with this parity.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  for (uint32_t it = 0; it < kWaitLimit; ++it)
+// Bounded wait for the completion of the barrier phase with this parity
+// (at most `limit` polls).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          uint32_t limit = kWaitLimit) {
+  for (uint32_t it = 0; it < limit; ++it)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
@@ -302,10 +308,23 @@ __device__ __forceinline__ void head_sums(const float* x, float* y) {
 // warp ends up with nearly the same number of edges, deterministically and
 // without atomics.  A warp's next 32/G bundles (one item per lane) are loaded
 // into registers one such block ahead of use.
-template <int G, int SE>
+//
+// Edge slots.  With RES = 0, edge k of group g sits in slot g * SE + k and
+// the item rows of starting items have a region of their own.  With RES > 0
+// ("inline" item rows), edge k of group g sits in slot k * G + g, so that
+// edge k of every group forms whole 4-row gather sets (G >= 4), and the
+// stage in which a bundle starts carries only SE - RES edges per group: its
+// last RES edge positions hold the starting items' rows instead (the kernel
+// gathers them there from the item tensors).  No stage then reserves shared
+// memory for item rows that only the first stage of an item needs.
+template <int G, int SE, int RES = 0>
 struct BundleCursor {
   static constexpr int B = G * SE;
   static constexpr int R = kUnit / G;  // bundles per block
+  static_assert(RES == 0 || (G >= 4 && SE > RES), "inline item rows need whole sets and an edge");
+  __device__ __forceinline__ static constexpr int slot(int g, int k) {
+    return RES > 0 ? k * G + g : g * SE + k;
+  }
   const int4* sorted;     // items by decreasing length: (node, e0, e1, item index)
   const int32_t* idx;     // CSR sources (or CSC destinations)
   int pad;                // row index of unused gather slots (zero-filled)
@@ -354,7 +373,7 @@ struct BundleCursor {
 
   // Generate the next stage into ring slot (desc[G], ix[B], qix[QR]): lane
   // g < G writes group g's descriptor {node (-1 idle, -3 end), item,
-  // count|flags, first edge}; lanes b < B copy the stage's source indices
+  // count|flags, first edge}; lane b < B copies the source index of slot b
   // (pad in unused slots); qix[g] is the node of an item that starts here,
   // else pad.  The issuing lane then reads whole 4-row sets from ix / qix.
   template <int QR>
@@ -365,25 +384,27 @@ struct BundleCursor {
       if (lane < G) desc[lane] = make_int4(-3, 0, 0, 0);
       return;
     }
+    const int step = off == 0 ? SE - RES : SE;  // edges per item in this stage
     if (lane < G) {
       const int4 it = s_items[bi + lane];
       const int len = it.z - it.y;
       if (it.x >= 0 && (off < len || (off == 0 && len == 0))) {
-        const int cnt = min(SE, len - off);
-        const int fl = (off == 0 ? kFirst : 0) | (off + SE >= len ? kLast : 0);
+        const int cnt = min(step, len - off);
+        const int fl = (off == 0 ? kFirst : 0) | (off + step >= len ? kLast : 0);
         d = make_int4(it.x, it.w, cnt | fl, it.y + off);
       }
       desc[lane] = d;
     }
     if (lane < QR) qix[lane] = (d.x >= 0 && (d.z & kFirst)) ? d.x : pad;
-    const int g = (lane / SE) & 31, k = lane % SE;
+    const int g = RES > 0 ? lane % G : (lane / SE) & 31;
+    const int k = RES > 0 ? lane / G : lane % SE;
     const int es = __shfl_sync(FULL, d.w, g);
     const int cn = __shfl_sync(FULL, d.x >= 0 ? (d.z & kCntMask) : 0, g);
     if (lane < B) {
       if (k < cn) cp_async4(ix + lane, idx + es + k);
       else ix[lane] = pad;
     }
-    off += SE;
+    off += step;
     if (off >= maxlen) {
       bi += G;
       off = 0;
@@ -468,15 +489,24 @@ struct Ring {
     __syncwarp();
   }
   __device__ __forceinline__ uint64_t* bar_at(int t) { return bar + (t % kStages); }
-  // Wait for stage t's rows.  On a failed (timed-out) wait, record it in
-  // *err and wait, again bounded, for the rows of the stages issued after t
-  // so that no copy into this warp's ring is still in flight; returns false.
-  __device__ __forceinline__ bool wait_rows(int t, int32_t* err, int lane) {
-    if (mbar_wait(bar_at(t), (t / kStages) & 1)) return true;
+  // Wait for stage t's rows, polling at most `limit` times.  On a failed
+  // (timed-out) wait, record it in *err and wait again, bounded by the normal
+  // limit, for the rows of every stage issued from t on (stage t itself
+  // included), so that no copy into this warp's ring is still in flight when
+  // the warp leaves; returns false.
+  __device__ __forceinline__ bool wait_rows(int t, int32_t* err, int lane,
+                                            uint32_t limit = kWaitLimit) {
+    if (mbar_wait(bar_at(t), (t / kStages) & 1, limit)) return true;
     if (lane == 0) atomicOr(err, 1);
-    for (int u = t + 1; u < t + kStages; ++u) mbar_wait(bar_at(u), (u / kStages) & 1);
+    for (int u = t; u < t + kStages; ++u)
+      if (desc_at(u)[0].x != -3) mbar_wait(bar_at(u), (u / kStages) & 1);
     cp_async_wait<0>();
     return false;
+  }
+  // Poll limit of stage t's wait: a launch with `fail_first` set gives its
+  // warps' first wait no polls at all (the failure path run on purpose).
+  __device__ __forceinline__ static uint32_t limit_at(int t, int fail_first) {
+    return (t == 0 && fail_first) ? 0u : kWaitLimit;
   }
   __device__ __forceinline__ int4* desc_at(int t) { return desc + (t % kRing) * L::G; }
   __device__ __forceinline__ int* ix_at(int t) {

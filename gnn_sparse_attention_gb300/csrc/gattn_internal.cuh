@@ -110,6 +110,7 @@ struct Plan {
   int32_t* cnt_dkv = nullptr;  // [n_inner_src]
   int32_t* cnt_da = nullptr;   // [1]
   int32_t* err = nullptr;      // [1] nonzero once a kernel's bounded wait gave up
+  int32_t fail_first_wait = 0; // gattn_plan_set_wait_test: attention passes fail their first wait
   std::vector<void*> allocs;   // every device buffer above, freed by destroy
 };
 

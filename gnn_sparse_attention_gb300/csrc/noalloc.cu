@@ -3,11 +3,11 @@
 // gattn_fwd needs device scratch for the partial results of heavy-node
 // chunks, and the caller normally provides it (gattn_workspace_size +
 // its own allocation).  Some callers cannot allocate device memory at the
-// point where they run the layer: code that runs while a CUDA graph is being
-// captured, code that lives under an external memory pool or allocator that
-// it does not own, or plugin hosts that hand it only the tensors.  For them
-// this entry point takes its scratch from one fixed array compiled into the
-// library, so the call itself allocates nothing.
+// point where they run the layer: code that lives under an external memory
+// pool or allocator that it does not own, or a plugin host that hands it
+// only the input and output tensors.  For them this entry point takes its
+// scratch from one fixed array compiled into the library, so the call itself
+// allocates nothing.
 //
 // The array holds kNoAllocScratchBytes.  It exists on every device that loads
 // the library for as long as the process lives, it is shared by every call,
@@ -30,12 +30,41 @@ constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) unsigned char g_fwd_scratch[kNoAllocScratchBytes];
 
+// The array's device address, cached per CUDA context: a device reset (or a
+// context other than the one the address was looked up in) can place the
+// module's globals at another address.
+struct CtxAddr {
+  void* ctx;
+  void* addr;
+};
 std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
+CtxAddr g_scratch[kMaxDevices] = {};
 
-// The device address of the scratch array on the current device.  The name
+using CtxGetCurrentFn = int (*)(void**);  // cuCtxGetCurrent(CUcontext*)
+
+// The driver's current context (nullptr when there is none or the query is
+// unavailable), reached through the runtime's entry-point lookup so that the
+// library needs no link-time dependency on the driver library.
+void* current_context() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(f);
+  });
+  void* ctx = nullptr;
+  if (!fn || fn(&ctx) != 0) return nullptr;
+  return ctx;
+}
+
+// The device address of the scratch array in the current context.  The name
 // g_fwd_scratch in host code is only a stand-in, so the address is looked up
-// once per device (with that device current) and cached.
+// with cudaGetSymbolAddress (with the device current) the first time a
+// context calls, and cached for that context.
 gattn_status scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -44,20 +73,24 @@ gattn_status scratch_address(void** out) {
     return GATTN_ERR_CUDA;
   }
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_ptr[dev]) {
+  void* ctx = current_context();
+  CtxAddr& c = g_scratch[dev];
+  if (!c.addr || !ctx || c.ctx != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_fwd_scratch);
     if (e != cudaSuccess || p == nullptr) {
       set_error("gattn_fwd_noalloc: cudaGetSymbolAddress failed (%s)", cudaGetErrorString(e));
       return GATTN_ERR_CUDA;
     }
-    g_scratch_ptr[dev] = p;
+    // the lookup makes the device's primary context current if none was
+    c.ctx = ctx ? ctx : current_context();
+    c.addr = p;
   }
-  *out = g_scratch_ptr[dev];
+  *out = c.addr;
   return GATTN_OK;
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 bool pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 
 }  // namespace
@@ -90,8 +123,8 @@ extern "C" gattn_status gattn_fwd_noalloc(const gattn_plan* plan, int32_t H, int
     const float scale = score->scale != 0.f ? score->scale : 1.f / sqrtf(float(D));
     f.qmul = scale * kLog2e;
   } else if (score->kind == GATTN_SCORE_GATV2) {
-    if (!score->a) {
-      set_error("gattn_fwd_noalloc: GATv2 score needs a[H*D]");
+    if (!score->a || !aligned(score->a, 4)) {
+      set_error("gattn_fwd_noalloc: GATv2 score needs a device pointer a[H*D] (4-byte aligned)");
       return GATTN_ERR_INVALID_ARG;
     }
     f.qmul = 1.f;
@@ -101,9 +134,13 @@ extern "C" gattn_status gattn_fwd_noalloc(const gattn_plan* plan, int32_t H, int
     return GATTN_ERR_INVALID_ARG;
   }
   if (p.N == 0) return GATTN_OK;
-  if (!Q || !K || !V || !out || !lse || !aligned16(Q) || !aligned16(K) || !aligned16(V) ||
-      !aligned16(out)) {
+  if (!Q || !K || !V || !out || !aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) ||
+      !aligned(out, 16)) {
     set_error("gattn_fwd_noalloc: tensors must be non-null, 16-byte aligned device pointers");
+    return GATTN_ERR_INVALID_ARG;
+  }
+  if (!lse || !aligned(lse, 4)) {
+    set_error("gattn_fwd_noalloc: lse must be a non-null, 4-byte aligned device pointer");
     return GATTN_ERR_INVALID_ARG;
   }
   // scratch: one partial (acc[HD], m[H], l[H], padded to 4 floats) per tree slot
@@ -142,6 +179,7 @@ extern "C" gattn_status gattn_fwd_noalloc(const gattn_plan* plan, int32_t H, int
   f.pstride = pstride;
   f.tree = Tree{p.parent, p.kids, p.n_chunks, p.cnt_fwd};
   f.err = p.err;
+  f.fail_first_wait = p.fail_first_wait;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if ((s = launch_fwd(dtype, int(rb), int(db), score->kind, stage_bytes(p.M, f.n_items), f,
                       p.num_sms, st, nullptr)) !=

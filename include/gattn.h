@@ -202,10 +202,26 @@ GATTN_API gattn_status gattn_plan_export_tile_bwd(const gattn_plan* plan, int64_
  * Synchronise the device and report whether any kernel run with this plan
  * since the last check gave up a bounded wait for its asynchronous copies
  * (every wait in the kernels has an iteration limit; on expiry the kernel
- * records the failure and returns instead of hanging; its outputs are then
- * undefined).  Returns GATTN_OK or GATTN_ERR_TIMEOUT and clears the record.
+ * records the failure, waits -- again bounded -- for the copies it had
+ * already issued, and returns instead of hanging; its outputs are then
+ * undefined).  Returns GATTN_OK or GATTN_ERR_TIMEOUT.  On GATTN_ERR_TIMEOUT
+ * it also clears the record and the plan's merge-tree arrival counters (a
+ * warp that gave up may have left a count behind), so the plan can be used
+ * again.  Synchronous.
  */
 GATTN_API gattn_status gattn_plan_check_errors(const gattn_plan* plan);
+
+/*
+ * Test hook for the failure path above (not part of the method).  With
+ * fail_first_wait nonzero, every warp of the attention passes run with this
+ * plan (gattn_fwd's CSR pass, gattn_bwd_dq, gattn_bwd_dkdv, and the same
+ * passes inside gattn_bwd and gattn_fwd_noalloc) treats its first wait for
+ * gathered rows as expired without polling: it records the failure, waits
+ * with the normal limit for every copy it had issued, and returns, so the
+ * next gattn_plan_check_errors returns GATTN_ERR_TIMEOUT.  Zero restores
+ * normal operation.  Host call; affects launches made after it.
+ */
+GATTN_API gattn_status gattn_plan_set_wait_test(gattn_plan* plan, int32_t fail_first_wait);
 
 /*
  * Bytes of caller-owned device workspace that gattn_fwd / gattn_bwd need
@@ -216,6 +232,14 @@ GATTN_API gattn_status gattn_workspace_size(const gattn_plan* plan, int32_t H, i
                                   gattn_dtype dtype, size_t* bytes);
 
 /*
+ * Workspace ownership.  In the call signatures of the method's contract
+ * the plan owns its scratch (heavy-chunk partials, the per-node Delta); here
+ * the caller passes it to gattn_fwd and gattn_bwd as `workspace`, sized by
+ * gattn_workspace_size.  The scratch depends on the head layout (H, D) of
+ * each call, which the plan does not know, and caller-owned memory lets one
+ * framework allocator (e.g. PyTorch's caching allocator) hold every buffer.
+ * Either way the forward and backward calls allocate nothing.
+ *
  * Forward ("Methodology", attention-based layers, forward pass): one
  * streaming pass over each destination's in-neighbours with an online
  * softmax; heavy destinations are split over edge chunks whose partial
@@ -280,17 +304,27 @@ GATTN_API gattn_status gattn_bwd_dkdv(const gattn_plan* plan, int32_t H, int32_t
 
 /*
  * gattn_fwd without a workspace argument, for callers that cannot allocate
- * device memory where they run the layer (inside CUDA graph capture, under
- * a memory pool they do not own, in plugin hosts that only pass tensors).
- * The paper has no counterpart to this call.  Same arguments and results as
- * gattn_fwd; the heavy-chunk scratch comes from one fixed 32 MiB array
- * compiled into the library, so the call allocates nothing.
+ * device memory where they run the layer: code under a memory pool or
+ * allocator it does not own, or a plugin host that hands over only the
+ * input and output tensors.  The paper has no counterpart to this call.
+ * Same arguments as gattn_fwd minus the workspace; the heavy-chunk scratch
+ * comes from one fixed 32 MiB array compiled into the library, so the call
+ * allocates nothing.
+ *   - It always runs the CSR pass over every edge.  On a plan built without
+ *     tile_enable its results equal gattn_fwd's bit for bit; on a tiled plan
+ *     (where gattn_fwd may run the dense tiles on the tensor cores) they
+ *     agree with gattn_fwd within the rounding tolerance, not exactly.
  *   - A plan and head layout whose scratch would exceed 32 MiB are rejected
- *     with GATTN_ERR_INVALID_ARG (use gattn_fwd with a workspace instead).
- *   - The first call on a device looks up the array's device address (a
- *     cudaGetSymbolAddress); make that first call before any stream capture.
- *   - All calls share the array: calls whose kernels may overlap on the GPU
- *     (different streams or host threads) race and must be ordered.
+ *     with GATTN_ERR_INVALID_ARG (use gattn_fwd with a workspace instead),
+ *     as are a null or misaligned tensor, lse or (GATv2) a pointer.
+ *   - The first call in a CUDA context (per device, and again after the
+ *     context is replaced, e.g. by cudaDeviceReset) looks up the array's
+ *     device address with cudaGetSymbolAddress and caches it; make that
+ *     first call before any stream capture begins.
+ *   - All calls share the array, which keeps whatever the last call left in
+ *     it (nothing in it needs to start at zero): calls whose kernels may
+ *     overlap on the GPU (different streams or host threads) race and must
+ *     be ordered.
  *   - The array lives on every device that loads the library until exit.
  */
 GATTN_API gattn_status gattn_fwd_noalloc(const gattn_plan* plan, int32_t H, int32_t D,

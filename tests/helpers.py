@@ -151,8 +151,30 @@ def compact_subgraph(indptr, indices, rows):
     return row_ptr, col_c, row_ids, nodes
 
 
-def sampled_oracle(case: GpuCase, dst_rows, src_nodes):
-    """Oracle values of out/lse/dQ on ``dst_rows`` and dK/dV on ``src_nodes``."""
+def _sources_oracle(case: GpuCase, src_nodes, rows_of_edge=None):
+    """Oracle dK/dV of ``src_nodes``: the backward over every destination row
+    that holds one of their out-edges (all of those rows, complete)."""
+    if rows_of_edge is None:
+        closure = oracle.sources_closure(case.indptr, case.indices, src_nodes)
+    else:  # the same rows, with the edge -> row map computed once by the caller
+        mark = np.zeros(len(case.indptr) - 1, bool)
+        mark[np.asarray(src_nodes)] = True
+        closure = np.unique(rows_of_edge[mark[case.indices]])
+    rp, col, rid, nodes = compact_subgraph(case.indptr, case.indices, closure)
+    Q, K, V = (case.host64(k, nodes) for k in ("Q", "K", "V"))
+    G = case.host64("dO", closure)
+    _, dK, dV, _ = oracle.backward(rp, col, Q, K, V, G, kind=case.okind, a=case.a64, rows=rid)
+    pos = np.searchsorted(nodes, np.asarray(src_nodes))
+    return dK[pos], dV[pos]
+
+
+def sampled_oracle(case: GpuCase, dst_rows, src_nodes, group=0, threads=1):
+    """Oracle values of out/lse/dQ on ``dst_rows`` and dK/dV on ``src_nodes``.
+
+    With ``group`` > 0 the sources are split into groups of that many, each
+    group's closure is evaluated on its own, and ``threads`` groups run at
+    once (the oracle is C called through ctypes, which releases the
+    interpreter lock)."""
     res = {}
     rp, col, rid, nodes = compact_subgraph(case.indptr, case.indices, dst_rows)
     Q, K, V = (case.host64(k, nodes) for k in ("Q", "K", "V"))
@@ -160,11 +182,32 @@ def sampled_oracle(case: GpuCase, dst_rows, src_nodes):
     out, lse = oracle.forward(rp, col, Q, K, V, kind=case.okind, a=case.a64, rows=rid)
     dQ, _, _, _ = oracle.backward(rp, col, Q, K, V, G, kind=case.okind, a=case.a64, rows=rid)
     res["rows"] = {"out": out, "lse": lse, "dQ": dQ}
-    closure = oracle.sources_closure(case.indptr, case.indices, src_nodes)
-    rp, col, rid, nodes = compact_subgraph(case.indptr, case.indices, closure)
-    Q, K, V = (case.host64(k, nodes) for k in ("Q", "K", "V"))
-    G = case.host64("dO", closure)
-    _, dK, dV, _ = oracle.backward(rp, col, Q, K, V, G, kind=case.okind, a=case.a64, rows=rid)
-    pos = np.searchsorted(nodes, np.asarray(src_nodes))
-    res["srcs"] = {"dK": dK[pos], "dV": dV[pos]}
+    src_nodes = np.asarray(src_nodes)
+    if group <= 0:
+        dK, dV = _sources_oracle(case, src_nodes)
+    else:
+        from concurrent.futures import ThreadPoolExecutor
+        parts = [src_nodes[k:k + group] for k in range(0, len(src_nodes), group)]
+        roe = np.repeat(np.arange(len(case.indptr) - 1), np.diff(np.asarray(case.indptr)))
+        with ThreadPoolExecutor(max_workers=max(1, threads)) as ex:
+            got = list(ex.map(lambda g: _sources_oracle(case, g, roe), parts))
+        dK = np.concatenate([x[0] for x in got])
+        dV = np.concatenate([x[1] for x in got])
+    res["srcs"] = {"dK": dK, "dV": dV}
     return res
+
+
+def cheap_sources(indptr, indices, seed, n=200, candidates=2000, top=3):
+    """Sources for a sampled dK/dV check of a large graph: ``n`` of ``candidates``
+    random sources (with out-edges) whose oracle closure -- the total in-degree
+    of their out-neighbours -- is smallest, plus the ``top`` sources of largest
+    out-degree.  Sorted, distinct."""
+    r = np.random.default_rng(seed)
+    N = len(indptr) - 1
+    deg = np.diff(np.asarray(indptr, np.int64))
+    outdeg = np.bincount(indices, minlength=N)
+    cost = np.bincount(indices, weights=np.repeat(deg, deg).astype(np.float64), minlength=N)
+    has_out = np.nonzero(outdeg > 0)[0]
+    cand = r.choice(has_out, min(candidates, len(has_out)), replace=False)
+    pick = cand[np.argsort(cost[cand], kind="stable")[:n]]
+    return np.unique(np.concatenate([np.argsort(-outdeg, kind="stable")[:top], pick]))

@@ -60,6 +60,9 @@ def test_host_argument_checks(lib):
     assert b"plan is NULL" in lib.gattn_last_error()
     n = ctypes.c_size_t()
     assert lib.gattn_workspace_size(None, 2, 16, 0, ctypes.byref(n)) == 1
+    assert lib.gattn_plan_set_wait_test(None, 1) == 1
+    assert lib.gattn_plan_check_errors(None) == 1
+    assert lib.gattn_fwd_noalloc(None, 2, 16, 0, None, None, None, None, None, None, None) == 1
 
 
 def test_missing_library_fails_loudly(tmp_path):

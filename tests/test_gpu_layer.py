@@ -84,7 +84,8 @@ def test_module_matches_fp64_composition(kind):
             xr = _round_bf16(x64 @ P["lin_r.weight"].T).reshape(N, H, D)
             o, _ = oracle.forward(ip, ix, xl, xr, xr, kind=oracle.GATV2, a=P["att"])
             ref = o.reshape(N, H * D)
-        assert relerr(y.detach().double().cpu().numpy(), ref) < 3 * TOL["bf16"]
+        # the module returns bf16: round the composition's result the same way
+        assert relerr(y.detach().double().cpu().numpy(), _round_bf16(ref)) <= TOL["bf16"]
         assert x.grad is not None and torch.isfinite(x.grad).all()
         for n, p in mod.named_parameters():
             assert p.grad is not None and torch.isfinite(p.grad).all(), n
@@ -126,3 +127,4 @@ def test_training_memory_holds_no_edge_tensor():
         assert extra < 40 * node_tensor, (extra, node_tensor)
     finally:
         plan.close()
+

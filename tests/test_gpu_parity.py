@@ -6,6 +6,8 @@ workloads are compared in the launch configuration the benchmark uses
 on sampled destinations (out, lse, dQ; the largest-degree hubs included)
 and sampled sources (dK, dV; the largest out-degrees included).
 """
+import os
+
 import numpy as np
 import pytest
 
@@ -168,7 +170,18 @@ def test_large_workload_sampled(name):
     try:
         got = case.run()
         rows, srcs, zero_src = _sample(case.indptr, case.indices, 1)
-        ref = hp.sampled_oracle(case, rows, srcs)
+        if name != "sbm1m":
+            # at least 200 sources for dK/dV: those with the cheapest oracle
+            # closure among 2000 random ones, the largest out-degrees, and
+            # (where the plan has both kinds) light and heavy sources alike
+            srcs = np.union1d(srcs, hp.cheap_sources(case.indptr, case.indices, 2))
+            T = case.plan.info()["heavy_threshold"]
+            outdeg = np.bincount(case.indices, minlength=len(case.indptr) - 1)
+            heavy = outdeg[srcs] > T
+            assert len(srcs) >= 200
+            assert heavy.any() or not (outdeg > T).any()
+            assert (~heavy).any() or not ((outdeg > 0) & (outdeg <= T)).any()
+        ref = hp.sampled_oracle(case, rows, srcs, group=8, threads=min(8, os.cpu_count() or 1))
         tol = hp.TOL[case.dtype]
         e1 = hp.compare({k: got[k] for k in ("out", "lse", "dQ")}, ref["rows"], tol, rows=rows)
         e2 = hp.compare({k: got[k] for k in ("dK", "dV")}, ref["srcs"], tol, rows=srcs)
