@@ -128,3 +128,87 @@ def test_training_memory_holds_no_edge_tensor():
     finally:
         plan.close()
 
+
+class _MaterialisingGATv2(torch.nn.Module):
+    """GATv2 written edge by edge in plain torch ops, the way a message-passing
+    library computes it: per-edge pre-activations [M, H, D], per-edge scores
+    and weights [M, H], per-edge messages [M, H, D], segment softmax and sum
+    over the destination.  Shares the fused module's parameters."""
+
+    def __init__(self, fused: "layer.GATv2Conv", src: torch.Tensor, dst: torch.Tensor, N: int):
+        super().__init__()
+        self.f, self.src, self.dst, self.N = fused, src, dst, N
+
+    def forward(self, x):
+        f, N = self.f, self.N
+        H, D = f.heads, f.head_dim
+        xl = f.lin_l(x).view(N, H, D)
+        xr = f.lin_r(x).view(N, H, D)
+        z = xl[self.dst] + xr[self.src]                                  # [M, H, D]
+        e = (torch.nn.functional.leaky_relu(z, f.slope).float() * f.att).sum(-1)   # [M, H]
+        idx = self.dst[:, None].expand(-1, H)
+        emax = torch.full((N, H), float("-inf"), device=x.device).scatter_reduce(
+            0, idx, e, "amax", include_self=True)
+        p = torch.exp(e - emax[self.dst])
+        den = torch.zeros(N, H, device=x.device).index_add_(0, self.dst, p)
+        alpha = p / den[self.dst]
+        msg = xr[self.src].float() * alpha[..., None]                   # [M, H, D]
+        out = torch.zeros(N, H, D, device=x.device).index_add_(0, self.dst, msg)
+        return out.to(x.dtype).reshape(N, H * D)
+
+
+def test_peak_memory_against_edge_materialising_gatv2():
+    """One GATv2 training step (forward + backward) through GATv2Conv and
+    through an edge-materialising composition of the same layer on a graph
+    of ~6.7 M edges: the fused layer's peak extra device memory is a small
+    fraction of the composition's (the pages report up to 76x, median 6x,
+    against DGL on an A100)."""
+    N, H, D, IN = 20_000, 4, 32, 128
+    r = np.random.default_rng(0)
+    deg = np.clip(r.lognormal(5.5, 0.8, N).astype(np.int64), 1, N - 1)
+    ip = np.zeros(N + 1, np.int64)
+    np.cumsum(deg, out=ip[1:])
+    ix = r.integers(0, N, int(ip[-1])).astype(np.int32)
+    ip = ip.astype(np.int32)
+    M = int(ip[-1])
+    dev = torch.device("cuda")
+    torch.manual_seed(1)
+    mod = layer.GATv2Conv(IN, H, D, device=dev)
+    x = torch.randn(N, IN, device=dev, dtype=torch.bfloat16)
+    src = torch.from_numpy(ix).to(dev, torch.long)
+    dst = torch.repeat_interleave(torch.arange(N, device=dev), torch.from_numpy(np.diff(ip)).to(dev))
+    ref = _MaterialisingGATv2(mod, src, dst, N)
+    plan = _plan(ip, ix)
+
+    def step(fn):
+        xx = x.clone().requires_grad_()
+        y = fn(xx)
+        y.float().sum().backward()
+        torch.cuda.synchronize()
+        return y.detach()
+
+    def peak(fn):
+        step(fn)                                     # warm-up (library, workspace, caches)
+        for p in mod.parameters():
+            p.grad = None
+        torch.cuda.synchronize()
+        base = torch.cuda.memory_allocated()
+        torch.cuda.reset_peak_memory_stats()
+        y = step(fn)
+        extra = torch.cuda.max_memory_allocated() - base
+        for p in mod.parameters():
+            p.grad = None
+        return extra, y
+
+    try:
+        fused, y_f = peak(lambda xx: mod(xx, plan))
+        mat, y_m = peak(ref)
+        ratio = mat / fused
+        print(f"M={M} peak extra memory: fused {fused / 2**20:.1f} MiB, materialising "
+              f"{mat / 2**20:.1f} MiB, ratio {ratio:.1f}x")
+        assert M > 5_000_000
+        # the same layer: outputs agree (bf16 messages summed in different orders)
+        assert relerr(y_f.double().cpu().numpy(), y_m.double().cpu().numpy()) < 3e-2
+        assert ratio > 10, (fused, mat)
+    finally:
+        plan.close()
