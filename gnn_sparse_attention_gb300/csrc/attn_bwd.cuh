@@ -72,12 +72,12 @@ template <typename T, int RB, int SB>
 struct CsrShape {
   using L = Lay<T, RB, SB>;
   static constexpr int LS = StatBytes<RB>::value;
-  // Item rows inline (attn_pipe.cuh, BundleCursor) wherever whole 4-row sets
-  // remain and at least one edge is left after the two item positions: a
-  // starting item's Q and dO rows take its group's K and V slots of the last
-  // edge position, its O row the K slot of the one before.  Otherwise the Q,
-  // dO and O rows have a region of their own (IR slots each).
-  static constexpr int RES = (L::G >= 4 && L::SE > 2) ? 2 : 0;
+  // Item rows inline (attn_pipe.cuh, BundleCursor) where a stage holds whole
+  // 4-row sets and at least 4 edges per item: a starting item's Q and dO
+  // rows take its group's K and V slots of the last edge position, its O row
+  // the K slot of the one before.  Otherwise the Q, dO and O rows have a
+  // region of their own (IR slots each).
+  static constexpr int RES = (L::G >= 4 && L::SE >= 4) ? 2 : 0;
   static constexpr int IRS = RES ? 0 : L::IR;
   // [IRS Q, dO, O rows] [lse sets] [B K rows] [B V rows]
   static constexpr int OL = 3 * IRS * RB;               // lse sets
@@ -86,6 +86,7 @@ struct CsrShape {
   static constexpr int STAGE = OV + L::B * RB;
   static constexpr int WARP_BYTES = align128(kStages * STAGE + L::META);
   static constexpr int WARPS = WarpsFor<WARP_BYTES>::value;
+  static constexpr int MINB = WarpsFor<WARP_BYTES>::minb;
   static constexpr int THREADS = 32 * WARPS;
   static constexpr int SMEM = WARPS * WARP_BYTES;
 };
@@ -94,10 +95,11 @@ template <typename T, int RB, int SB, int DB>
 struct CscShape {
   using L = Lay<T, RB, SB>;
   static constexpr int H = RB / DB;                     // heads
-  // Item rows inline where whole 4-row sets and an edge remain: a starting
-  // item's K and V rows take its group's Q and dO slots of the last edge
-  // position.  Otherwise K and V rows have a region of their own.
-  static constexpr int RES = (L::G >= 4 && L::SE > 1) ? 1 : 0;
+  // Item rows inline where a stage holds whole 4-row sets and at least 4
+  // edges per item: a starting item's K and V rows take its group's Q and dO
+  // slots of the last edge position.  Otherwise K and V rows have a region
+  // of their own.
+  static constexpr int RES = (L::G >= 4 && L::SE >= 4) ? 1 : 0;
   static constexpr int IRS = RES ? 0 : L::IR;
   // [IRS K, V rows] [B Q rows] [B dO rows] [B (lse log2 e, Delta) rows]
   static constexpr int SROW = 8 * H;                    // bytes of one (lse, Delta) row
@@ -107,6 +109,7 @@ struct CscShape {
   static constexpr int STAGE = align128(OLS + L::B * SROW);
   static constexpr int WARP_BYTES = align128(kStages * STAGE + L::META);
   static constexpr int WARPS = WarpsFor<WARP_BYTES>::value;
+  static constexpr int MINB = WarpsFor<WARP_BYTES>::minb;
   static constexpr int THREADS = 32 * WARPS;
   static constexpr int SMEM = WARPS * WARP_BYTES;
 };
@@ -133,7 +136,7 @@ __device__ __forceinline__ void copy_stat_rows(uint8_t* dst, const float* src, i
 // pass 1: CSR
 // ---------------------------------------------------------------------------
 template <typename T, int RB, int DB, int KIND, int SB>
-__global__ void __launch_bounds__(CsrShape<T, RB, SB>::THREADS) bwd_csr_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(CsrShape<T, RB, SB>::THREADS, min_blocks<CsrShape<T, RB, SB>::WARP_BYTES, RB, SB>(KIND)) bwd_csr_kernel(const __grid_constant__ BwdParams p) {
   using L = Lay<T, RB, SB>;
   using Sh = CsrShape<T, RB, SB>;
   using PR = Pairs<T>;
@@ -187,53 +190,72 @@ __global__ void __launch_bounds__(CsrShape<T, RB, SB>::THREADS) bwd_csr_kernel(c
   constexpr int OQ = 0, ODO = Sh::IRS * RB, OO = 2 * Sh::IRS * RB;
   constexpr int OL = Sh::OL, OK = Sh::OK, OV = Sh::OV;
   // inline: slots of a starting item's Q / dO rows (last edge position) and O row
-  constexpr int K1 = (SE - 1) * G / 4, K2 = (SE - 2) * G / 4;
+  constexpr int NS = B / 4;
+  constexpr int K1 = Sh::RES > 0 ? (SE - 1) * G / 4 : NS;
+  constexpr int K2 = Sh::RES > 0 ? (SE - 2) * G / 4 : NS;
+  // The copies of a stage are spread over the lanes, one 4-row gather per
+  // job: jobs [0, NS) fill the K region's sets, [NS, 2 NS) the V region's
+  // (inline: item rows in the sets from K2 / K1 on of a starting stage),
+  // then, with a separate item region, 3 jobs per item set (Q, dO, O), then
+  // the lse sets; lane 0 first sets the byte count on the barrier.
+  constexpr int NJI = (Sh::RES == 0 && !L::IBULK) ? 3 * (L::QR / 4) : 0;
   auto issue = [&](int s) {
     const int4* dsc = ring.desc_at(s);
-    if (lane == 0 && dsc[0].x != -3) {
+    if (dsc[0].x != -3) {
       uint8_t* st = ring.stage_at(s);
       uint64_t* bar = ring.bar_at(s);
-      int4 qr[L::QR / 4];
-      uint32_t qmask = 0;
-#pragma unroll
-      for (int q4 = 0; q4 < L::QR / 4; ++q4) {
-        qr[q4] = ring.qset(s, q4);
-        const bool any = qr[q4].x != p.N || qr[q4].y != p.N || qr[q4].z != p.N ||
-                         qr[q4].w != p.N;
-        qmask |= uint32_t(any) << q4;
-      }
-      const uint32_t ibytes = L::IBULK ? item_rows<L>(qr[0], p.N) * 3 * RB
-                                       : __popc(qmask) * 3 * L::SET_BYTES;
+      const uint32_t qmask = ring.item_mask(s, p.N, lane);
       // inline: a stage that starts a bundle gathers edge rows only below K2
-      const int ne = (Sh::RES > 0 && qmask) ? K2 : B / 4;
-      fence_proxy_async();
-      mbar_expect_tx(bar, ibytes + (p.rows16 ? __popc(qmask) * 16 * p.H : 0) +
-                              2 * ne * L::SET_BYTES);
-#pragma unroll
-      for (int q4 = 0; q4 < L::QR / 4; ++q4)
-        if ((qmask >> q4) & 1) {
-          const int4 r = qr[q4];
-          if constexpr (Sh::RES > 0) {
-            L::gather(st + OK, 4 * (K1 + q4), &p.mi0, r.x, r.y, r.z, r.w, bar);
-            L::gather(st + OV, 4 * (K1 + q4), &p.mi1, r.x, r.y, r.z, r.w, bar);
-            L::gather(st + OK, 4 * (K2 + q4), &p.mi2, r.x, r.y, r.z, r.w, bar);
-          } else if constexpr (L::IBULK) {
-            fetch_item_rows<L>(st + OQ, p.Q, r, p.N, bar);
-            fetch_item_rows<L>(st + ODO, p.dO, r, p.N, bar);
-            fetch_item_rows<L>(st + OO, p.O, r, p.N, bar);
-          } else {
-            L::gather(st + OQ, 4 * q4, &p.mi0, r.x, r.y, r.z, r.w, bar);
-            L::gather(st + ODO, 4 * q4, &p.mi1, r.x, r.y, r.z, r.w, bar);
-            L::gather(st + OO, 4 * q4, &p.mi2, r.x, r.y, r.z, r.w, bar);
+      const int ne = (Sh::RES > 0 && qmask) ? K2 : NS;
+      const uint32_t ibytes = L::IBULK ? item_rows<L>(ring.qset(s, 0), p.N) * 3 * RB
+                                       : __popc(qmask) * 3 * L::SET_BYTES;
+      if (lane == 0)
+        mbar_expect_tx(bar, ibytes + (p.rows16 ? __popc(qmask) * 16 * p.H : 0) +
+                                2 * ne * L::SET_BYTES);
+      __syncwarp();
+      const int njobs = 2 * NS + NJI + (p.rows16 ? L::QR / 4 : 0);
+      for (int jb = lane; jb < njobs; jb += 32) {
+        if (jb < 2 * NS) {
+          const bool vr = jb >= NS;
+          const int b4 = vr ? jb - NS : jb;
+          uint8_t* reg = st + (vr ? OV : OK);
+          if (b4 < ne) {
+            const int4 r = ring.eset(s, b4);
+            fence_proxy_async();
+            L::gather(reg, 4 * b4, vr ? &p.me1 : &p.me0, r.x, r.y, r.z, r.w, bar);
+          } else if (b4 >= K1 && ((qmask >> (b4 - K1)) & 1)) {  // inline Q / dO rows
+            const int4 r = ring.qset(s, b4 - K1);
+            fence_proxy_async();
+            L::gather(reg, 4 * b4, vr ? &p.mi1 : &p.mi0, r.x, r.y, r.z, r.w, bar);
+          } else if (!vr && b4 >= K2 && b4 < K1 && ((qmask >> (b4 - K2)) & 1)) {  // inline O rows
+            const int4 r = ring.qset(s, b4 - K2);
+            fence_proxy_async();
+            L::gather(reg, 4 * b4, &p.mi2, r.x, r.y, r.z, r.w, bar);
           }
-          if (p.rows16) tma_gather4(st + OL + q4 * L::SSB, &p.ms0, 0, r.x, r.y, r.z, r.w, bar);
+        } else if (jb < 2 * NS + NJI) {  // separate item region: Q, dO, O sets
+          const int q4 = (jb - 2 * NS) / 3, w = (jb - 2 * NS) % 3;
+          if ((qmask >> q4) & 1) {
+            const int4 r = ring.qset(s, q4);
+            fence_proxy_async();
+            L::gather(st + (w == 0 ? OQ : (w == 1 ? ODO : OO)), 4 * q4,
+                      w == 0 ? &p.mi0 : (w == 1 ? &p.mi1 : &p.mi2), r.x, r.y, r.z, r.w, bar);
+          }
+        } else {  // lse rows of the starting items
+          const int q4 = jb - 2 * NS - NJI;
+          if ((qmask >> q4) & 1) {
+            const int4 r = ring.qset(s, q4);
+            fence_proxy_async();
+            tma_gather4(st + OL + q4 * L::SSB, &p.ms0, 0, r.x, r.y, r.z, r.w, bar);
+          }
         }
-#pragma unroll
-      for (int b4 = 0; b4 < B / 4; ++b4) {
-        if (b4 < ne) {
-          const int4 r = ring.eset(s, b4);
-          L::gather(st + OK, 4 * b4, &p.me0, r.x, r.y, r.z, r.w, bar);
-          L::gather(st + OV, 4 * b4, &p.me1, r.x, r.y, r.z, r.w, bar);
+      }
+      if constexpr (Sh::RES == 0 && L::IBULK) {
+        if (lane == 0 && qmask) {
+          const int4 r = ring.qset(s, 0);
+          fence_proxy_async();
+          fetch_item_rows<L>(st + OQ, p.Q, r, p.N, bar);
+          fetch_item_rows<L>(st + ODO, p.dO, r, p.N, bar);
+          fetch_item_rows<L>(st + OO, p.O, r, p.N, bar);
         }
       }
     }
@@ -273,8 +295,14 @@ __global__ void __launch_bounds__(CsrShape<T, RB, SB>::THREADS) bwd_csr_kernel(c
     const bool first = act && (d.z & kFirst);
 
     if (__any_sync(FULL, first)) {
-      // item start: q, dO, Delta = dO . O, lse (every lane joins the head reduction)
-      float part[NC], dsum[HL];
+      // item start: q, dO, Delta = dO . O, lse (every lane joins the head
+      // reduction).  Delta is summed in exactly the order of every dp = dO . v
+      // below and in the CSC pass, so that dp - Delta is exactly 0 wherever
+      // out equals a single neighbour's v (a one-edge row).
+      float dsum[HL];
+      float2 a2[HL];
+#pragma unroll
+      for (int j = 0; j < HL; ++j) a2[j] = f2s(0.f);
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
         float2 o[PP];
@@ -295,12 +323,11 @@ __global__ void __launch_bounds__(CsrShape<T, RB, SB>::THREADS) bwd_csr_kernel(c
 #pragma unroll
           for (int v = 0; v < PP; ++v) o[v] = f2s(0.f);
         }
-        float2 a2 = f2s(0.f);
 #pragma unroll
-        for (int v = 0; v < PP; ++v) a2 = f2fma(first ? gq[c][v] : f2s(0.f), o[v], a2);
-        part[c] = a2.x + a2.y;
+        for (int v = 0; v < PP; ++v)
+          a2[LH::of(c)] = f2fma(first ? gq[c][v] : f2s(0.f), o[v], a2[LH::of(c)]);
       }
-      head_sums<NC, CPH>(part, dsum);
+      head_sums2<NC, CPH>(a2, dsum);
       if (first) {
         const float* ls = reinterpret_cast<const float*>(st + OL + (g / 4) * L::SSB) + (g % 4) * p.H;
 #pragma unroll
@@ -336,32 +363,35 @@ __global__ void __launch_bounds__(CsrShape<T, RB, SB>::THREADS) bwd_csr_kernel(c
     for (int k = 0; k < SE; ++k) {
       if (k >= kmax) break;
       const bool valid = k < cnt;
-      float scp[NC], dpp[NC], sc[HL], dp[HL];
+      // slots past this group's count are read as they are (zero-filled pad
+      // rows or rows of an earlier stage): nothing below uses their results
+      float sc[HL], dp[HL];
+      float2 s2[HL], p2[HL];
+#pragma unroll
+      for (int j = 0; j < HL; ++j) s2[j] = p2[j] = f2s(0.f);
       float2 kf[NC][PP];
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
         const int off = L::off(Cur::slot(g, k), (t * NC + c) * 16);
         float2 vf[PP];
-        PR::load(valid ? lds16(ks + off) : make_uint4(0, 0, 0, 0), kf[c]);
-        PR::load(valid ? lds16(vs + off) : make_uint4(0, 0, 0, 0), vf);
-        float2 s2 = f2s(0.f), p2 = f2s(0.f);
+        PR::load(lds16(ks + off), kf[c]);
+        PR::load(lds16(vs + off), vf);
+        const int j = LH::of(c);
 #pragma unroll
         for (int v = 0; v < PP; ++v) {
-          p2 = f2fma(gq[c][v], vf[v], p2);
+          p2[j] = f2fma(gq[c][v], vf[v], p2[j]);
           if (!GAT) {
-            s2 = f2fma(q[c][v], kf[c][v], s2);
+            s2[j] = f2fma(q[c][v], kf[c][v], s2[j]);
           } else {
             const float2 z = make_float2(q[c][v].x + kf[c][v].x, q[c][v].y + kf[c][v].y);
             const float2 lr = make_float2(z.x > 0.f ? z.x : p.slope * z.x,
                                           z.y > 0.f ? z.y : p.slope * z.y);
-            s2 = f2fma(av[c][v], lr, s2);
+            s2[j] = f2fma(av[c][v], lr, s2[j]);
           }
         }
-        scp[c] = s2.x + s2.y;
-        dpp[c] = p2.x + p2.y;
       }
-      head_sums<NC, CPH>(scp, sc);
-      head_sums<NC, CPH>(dpp, dp);
+      head_sums2<NC, CPH>(s2, sc);
+      head_sums2<NC, CPH>(p2, dp);
       if (act && valid) {
         float ds[HL];
 #pragma unroll
@@ -502,7 +532,7 @@ __global__ void __launch_bounds__(CsrShape<T, RB, SB>::THREADS) bwd_csr_kernel(c
 // pass 2: CSC
 // ---------------------------------------------------------------------------
 template <typename T, int RB, int DB, int KIND, int SB>
-__global__ void __launch_bounds__(CscShape<T, RB, SB, DB>::THREADS) bwd_csc_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(CscShape<T, RB, SB, DB>::THREADS, min_blocks<CscShape<T, RB, SB, DB>::WARP_BYTES, RB, SB>(KIND)) bwd_csc_kernel(const __grid_constant__ BwdParams p) {
   using L = Lay<T, RB, SB>;
   using Sh = CscShape<T, RB, SB, DB>;
   using PR = Pairs<T>;
@@ -555,48 +585,56 @@ __global__ void __launch_bounds__(CscShape<T, RB, SB, DB>::THREADS) bwd_csc_kern
   constexpr int SROW = Sh::SROW;
   constexpr int PB = SROW < 16 ? SROW : 16;   // bytes of one statistic piece
   constexpr int PPR = SROW / PB;             // pieces per row
-  constexpr int K1 = (SE - 1) * G / 4;       // inline: first set of the last edge position
+  constexpr int NS = B / 4;
+  constexpr int K1 = Sh::RES > 0 ? (SE - 1) * G / 4 : NS;  // inline: first set of the last position
+  // The copies of a stage are spread over the lanes, one 4-row gather per
+  // job: jobs [0, NS) fill the Q region's sets, [NS, 2 NS) the dO region's
+  // (inline: a starting stage's K / V item rows in the sets from K1 on),
+  // then, with a separate item region, 2 jobs per item set (K, V); lane 0
+  // first sets the byte count on the barrier.
+  constexpr int NJI = (Sh::RES == 0 && !L::IBULK) ? 2 * (L::QR / 4) : 0;
   auto issue = [&](int s) {
     const int4* dsc = ring.desc_at(s);
     const bool live = dsc[0].x != -3;
-    if (lane == 0 && live) {
+    if (live) {
       uint8_t* st = ring.stage_at(s);
       uint64_t* bar = ring.bar_at(s);
-      int4 qr[L::QR / 4];
-      uint32_t qmask = 0;
-#pragma unroll
-      for (int q4 = 0; q4 < L::QR / 4; ++q4) {
-        qr[q4] = ring.qset(s, q4);
-        const bool any = qr[q4].x != p.N || qr[q4].y != p.N || qr[q4].z != p.N ||
-                         qr[q4].w != p.N;
-        qmask |= uint32_t(any) << q4;
-      }
-      const uint32_t ibytes = L::IBULK ? item_rows<L>(qr[0], p.N) * 2 * RB
+      const uint32_t qmask = ring.item_mask(s, p.N, lane);
+      const uint32_t ibytes = L::IBULK ? item_rows<L>(ring.qset(s, 0), p.N) * 2 * RB
                                        : __popc(qmask) * 2 * L::SET_BYTES;
-      const int ne = (Sh::RES > 0 && qmask) ? K1 : B / 4;  // sets of edge rows
-      fence_proxy_async();
-      mbar_expect_tx(bar, ibytes + 2 * ne * L::SET_BYTES);
-#pragma unroll
-      for (int q4 = 0; q4 < L::QR / 4; ++q4)
-        if ((qmask >> q4) & 1) {
-          const int4 r = qr[q4];
-          if constexpr (Sh::RES > 0) {
-            L::gather(st + OQE, 4 * (K1 + q4), &p.mi0, r.x, r.y, r.z, r.w, bar);
-            L::gather(st + OGE, 4 * (K1 + q4), &p.mi1, r.x, r.y, r.z, r.w, bar);
-          } else if constexpr (L::IBULK) {
-            fetch_item_rows<L>(st + OKI, p.K, r, p.N, bar);
-            fetch_item_rows<L>(st + OVI, p.V, r, p.N, bar);
-          } else {
-            L::gather(st + OKI, 4 * q4, &p.mi0, r.x, r.y, r.z, r.w, bar);
-            L::gather(st + OVI, 4 * q4, &p.mi1, r.x, r.y, r.z, r.w, bar);
+      const int ne = (Sh::RES > 0 && qmask) ? K1 : NS;  // sets of edge rows
+      if (lane == 0) mbar_expect_tx(bar, ibytes + 2 * ne * L::SET_BYTES);
+      __syncwarp();
+      for (int jb = lane; jb < 2 * NS + NJI; jb += 32) {
+        if (jb < 2 * NS) {
+          const bool gr = jb >= NS;
+          const int b4 = gr ? jb - NS : jb;
+          uint8_t* reg = st + (gr ? OGE : OQE);
+          if (b4 < ne) {
+            const int4 r = ring.eset(s, b4);
+            fence_proxy_async();
+            L::gather(reg, 4 * b4, gr ? &p.me1 : &p.me0, r.x, r.y, r.z, r.w, bar);
+          } else if ((qmask >> (b4 - K1)) & 1) {  // inline K / V rows
+            const int4 r = ring.qset(s, b4 - K1);
+            fence_proxy_async();
+            L::gather(reg, 4 * b4, gr ? &p.mi1 : &p.mi0, r.x, r.y, r.z, r.w, bar);
+          }
+        } else {  // separate item region: K, V sets
+          const int q4 = (jb - 2 * NS) / 2, w = (jb - 2 * NS) % 2;
+          if ((qmask >> q4) & 1) {
+            const int4 r = ring.qset(s, q4);
+            fence_proxy_async();
+            L::gather(st + (w == 0 ? OKI : OVI), 4 * q4, w == 0 ? &p.mi0 : &p.mi1, r.x, r.y, r.z,
+                      r.w, bar);
           }
         }
-#pragma unroll
-      for (int b4 = 0; b4 < B / 4; ++b4) {
-        if (b4 < ne) {
-          const int4 r = ring.eset(s, b4);
-          L::gather(st + OQE, 4 * b4, &p.me0, r.x, r.y, r.z, r.w, bar);
-          L::gather(st + OGE, 4 * b4, &p.me1, r.x, r.y, r.z, r.w, bar);
+      }
+      if constexpr (Sh::RES == 0 && L::IBULK) {
+        if (lane == 0 && qmask) {
+          const int4 r = ring.qset(s, 0);
+          fence_proxy_async();
+          fetch_item_rows<L>(st + OKI, p.K, r, p.N, bar);
+          fetch_item_rows<L>(st + OVI, p.V, r, p.N, bar);
         }
       }
     }
@@ -676,30 +714,33 @@ __global__ void __launch_bounds__(CscShape<T, RB, SB, DB>::THREADS) bwd_csc_kern
     for (int e = 0; e < SE; ++e) {
       if (e >= kmax) break;
       const bool valid = e < cnt;
-      float scp[NC], dpp[NC], sc[HL], dp[HL];
+      // slots past this group's count are read as they are (zero-filled pad
+      // rows or rows of an earlier stage): nothing below uses their results
+      float sc[HL], dp[HL];
+      float2 s2[HL], p2[HL];
+#pragma unroll
+      for (int j = 0; j < HL; ++j) s2[j] = p2[j] = f2s(0.f);
       float2 qf[NC][PP], gf[NC][PP];
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
         const int off = L::off(Cur::slot(g, e), (t * NC + c) * 16);
-        PR::load(valid ? lds16(qs + off) : make_uint4(0, 0, 0, 0), qf[c]);
-        PR::load(valid ? lds16(gs + off) : make_uint4(0, 0, 0, 0), gf[c]);
-        float2 s2 = f2s(0.f), p2 = f2s(0.f);
+        PR::load(lds16(qs + off), qf[c]);
+        PR::load(lds16(gs + off), gf[c]);
+        const int j = LH::of(c);
 #pragma unroll
         for (int v = 0; v < PP; ++v) {
-          p2 = f2fma(gf[c][v], vv[c][v], p2);
+          p2[j] = f2fma(gf[c][v], vv[c][v], p2[j]);
           if (!GAT) {
-            s2 = f2fma(qf[c][v], k[c][v], s2);
+            s2[j] = f2fma(qf[c][v], k[c][v], s2[j]);
           } else {  // qf becomes z = xl_i + xr_j
             qf[c][v] = f2add(qf[c][v], k[c][v]);
             const float2 lr = f2fma(f2s(gc1), qf[c][v], f2mul(f2s(gc2), f2abs(qf[c][v])));
-            s2 = f2fma(av[c][v], lr, s2);
+            s2[j] = f2fma(av[c][v], lr, s2[j]);
           }
         }
-        scp[c] = s2.x + s2.y;
-        dpp[c] = p2.x + p2.y;
       }
-      head_sums<NC, CPH>(scp, sc);
-      head_sums<NC, CPH>(dpp, dp);
+      head_sums2<NC, CPH>(s2, sc);
+      head_sums2<NC, CPH>(p2, dp);
       if (act && valid) {
         const float* srow = reinterpret_cast<const float*>(st + OLS + Cur::slot(g, e) * SROW);
         float pr[HL], ds[HL];

@@ -52,22 +52,24 @@ struct FwdParams {
 template <typename T, int RB, int SB>
 struct FwdShape {
   using L = Lay<T, RB, SB>;
-  // Item rows inline (attn_pipe.cuh, BundleCursor) wherever whole 4-row sets
-  // and at least one edge remain: a starting item's Q row takes the K-row
-  // slot of its group's last edge position.  Otherwise Q rows have a region
-  // of their own (IR slots).
-  static constexpr int RES = (L::G >= 4 && L::SE > 1) ? 1 : 0;
+  // Item rows inline (attn_pipe.cuh, BundleCursor) where a stage holds whole
+  // 4-row sets and at least 4 edges per item: a starting item's Q row takes
+  // the K-row slot of its group's last edge position.  Otherwise (short
+  // stages, where one edge position less per item would cost a stage in
+  // most items) Q rows have a region of their own (IR slots).
+  static constexpr int RES = (L::G >= 4 && L::SE >= 4) ? 1 : 0;
   static constexpr int IRS = RES ? 0 : L::IR;
   // [IRS Q rows] then B K rows and B V rows
   static constexpr int STAGE = RB * (IRS + 2 * L::B);
   static constexpr int WARP_BYTES = align128(kStages * STAGE + L::META);
   static constexpr int WARPS = WarpsFor<WARP_BYTES>::value;
+  static constexpr int MINB = WarpsFor<WARP_BYTES>::minb;
   static constexpr int THREADS = 32 * WARPS;
   static constexpr int SMEM = WARPS * WARP_BYTES;
 };
 
 template <typename T, int RB, int DB, int KIND, int SB>
-__global__ void __launch_bounds__(FwdShape<T, RB, SB>::THREADS) fwd_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(FwdShape<T, RB, SB>::THREADS, min_blocks<FwdShape<T, RB, SB>::WARP_BYTES, RB, SB>(KIND)) fwd_kernel(const __grid_constant__ FwdParams p) {
   using L = Lay<T, RB, SB>;
   using Sh = FwdShape<T, RB, SB>;
   using PR = Pairs<T>;
@@ -123,55 +125,48 @@ __global__ void __launch_bounds__(FwdShape<T, RB, SB>::THREADS) fwd_kernel(const
   // bundle gathers the Q rows into the K slots of the last edge position and
   // skips that position's V slots.  Bytes are counted on the slot's barrier.
   constexpr int OKR = Sh::IRS * RB, OVR = (Sh::IRS + B) * RB;  // K, V row regions
+  // The copies of a stage are spread over the lanes, one 4-row gather each:
+  // lanes [0, NS) the K-row sets, [NS, 2 NS) the V-row sets, [2 NS, 2 NS +
+  // QR / 4) the Q-row sets of a separate item region; lane 0 first sets the
+  // byte count on the barrier.
+  constexpr int NS = B / 4;
+  constexpr int KS = Sh::RES > 0 ? (SE - 1) * G / 4 : NS;  // inline: first set of the last position
   auto issue = [&](int s) {
-    if (lane == 0) {
-      const int4* dsc = ring.desc_at(s);
-      if (dsc[0].x != -3) {
-        uint8_t* st = ring.stage_at(s);
-        uint64_t* bar = ring.bar_at(s);
-        int4 qr[L::QR / 4];
-        uint32_t qmask = 0;
-#pragma unroll
-        for (int q4 = 0; q4 < L::QR / 4; ++q4) {
-          qr[q4] = ring.qset(s, q4);
-          const bool any = qr[q4].x != p.N || qr[q4].y != p.N || qr[q4].z != p.N ||
-                           qr[q4].w != p.N;
-          qmask |= uint32_t(any) << q4;
+    const int4* dsc = ring.desc_at(s);
+    if (dsc[0].x != -3) {
+      uint8_t* st = ring.stage_at(s);
+      uint64_t* bar = ring.bar_at(s);
+      const uint32_t qmask = ring.item_mask(s, p.N, lane);
+      const int ne = (Sh::RES > 0 && qmask) ? KS : NS;  // sets of edge rows in this stage
+      uint32_t bytes = (2 * ne + __popc(qmask)) * L::SET_BYTES;
+      if constexpr (Sh::RES == 0 && L::IBULK)
+        bytes = 2 * NS * L::SET_BYTES + item_rows<L>(ring.qset(s, 0), p.N) * RB;
+      if (lane == 0) mbar_expect_tx(bar, bytes);
+      __syncwarp();
+      if (lane < 2 * NS) {
+        const bool vr = lane >= NS;
+        const int b4 = vr ? lane - NS : lane;
+        if (b4 < ne) {
+          const int4 r = ring.eset(s, b4);
+          fence_proxy_async();
+          L::gather(st + (vr ? OVR : OKR), 4 * b4, vr ? &p.mv : &p.mk, r.x, r.y, r.z, r.w, bar);
+        } else if (!vr && ((qmask >> (b4 - KS)) & 1)) {  // inline Q rows
+          const int4 r = ring.qset(s, b4 - KS);
+          fence_proxy_async();
+          L::gather(st + OKR, 4 * b4, &p.mq, r.x, r.y, r.z, r.w, bar);
         }
-        fence_proxy_async();
-        if constexpr (Sh::RES > 0) {
-          constexpr int KS = (SE - 1) * G / 4;  // first 4-row set of the last edge position
-          const int ne = qmask ? KS : B / 4;    // sets of edge rows in this stage
-          mbar_expect_tx(bar, (2 * ne + __popc(qmask)) * L::SET_BYTES);
-#pragma unroll
-          for (int b4 = 0; b4 < B / 4; ++b4) {
-            if (b4 < ne) {
-              const int4 r = ring.eset(s, b4);
-              L::gather(st + OKR, 4 * b4, &p.mk, r.x, r.y, r.z, r.w, bar);
-              L::gather(st + OVR, 4 * b4, &p.mv, r.x, r.y, r.z, r.w, bar);
-            } else if ((qmask >> (b4 - KS)) & 1) {
-              const int4 r = qr[b4 - KS];
-              L::gather(st + OKR, 4 * b4, &p.mq, r.x, r.y, r.z, r.w, bar);
-            }
-          }
-        } else {
-          const uint32_t ibytes = L::IBULK ? item_rows<L>(qr[0], p.N) * RB
-                                           : __popc(qmask) * L::SET_BYTES;
-          mbar_expect_tx(bar, ibytes + 2 * (B / 4) * L::SET_BYTES);
-          if constexpr (L::IBULK) {
-            fetch_item_rows<L>(st, p.Q, qr[0], p.N, bar);
-          } else {
-#pragma unroll
-            for (int q4 = 0; q4 < L::QR / 4; ++q4)
-              if ((qmask >> q4) & 1)
-                L::gather(st, 4 * q4, &p.mq, qr[q4].x, qr[q4].y, qr[q4].z, qr[q4].w, bar);
-          }
-#pragma unroll
-          for (int b4 = 0; b4 < B / 4; ++b4) {
-            const int4 r = ring.eset(s, b4);
-            L::gather(st + OKR, 4 * b4, &p.mk, r.x, r.y, r.z, r.w, bar);
-            L::gather(st + OVR, 4 * b4, &p.mv, r.x, r.y, r.z, r.w, bar);
-          }
+      } else if (Sh::RES == 0 && !L::IBULK && lane < 2 * NS + L::QR / 4) {
+        const int q4 = lane - 2 * NS;
+        if ((qmask >> q4) & 1) {
+          const int4 r = ring.qset(s, q4);
+          fence_proxy_async();
+          L::gather(st, 4 * q4, &p.mq, r.x, r.y, r.z, r.w, bar);
+        }
+      }
+      if constexpr (Sh::RES == 0 && L::IBULK) {
+        if (lane == 0) {
+          fence_proxy_async();
+          fetch_item_rows<L>(st, p.Q, ring.qset(s, 0), p.N, bar);
         }
       }
     }
@@ -232,26 +227,29 @@ __global__ void __launch_bounds__(FwdShape<T, RB, SB>::THREADS) fwd_kernel(const
 #pragma unroll
     for (int k = 0; k < SE; ++k) {
       if (k >= kmax) break;
-      float part[NC];
+      // slots past this group's count hold zero-filled pad rows or rows of an
+      // earlier stage: their scores are discarded below, so they are read as is
+      float2 a2[HL];
+#pragma unroll
+      for (int j = 0; j < HL; ++j) a2[j] = f2s(0.f);
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
-        const uint4 kr = k < cnt ? lds16(ks + L::off(Cur::slot(g, k), (t * NC + c) * 16)) : make_uint4(0, 0, 0, 0);
+        const uint4 kr = lds16(ks + L::off(Cur::slot(g, k), (t * NC + c) * 16));
         float2 kf[PP];
         PR::load(kr, kf);
-        float2 a2 = f2s(0.f);
+        float2& acc2 = a2[LH::of(c)];
         if (!GAT) {
 #pragma unroll
-          for (int v = 0; v < PP; ++v) a2 = f2fma(q[c][v], kf[v], a2);
+          for (int v = 0; v < PP; ++v) acc2 = f2fma(q[c][v], kf[v], acc2);
         } else {
 #pragma unroll
           for (int v = 0; v < PP; ++v) {
             const float2 z = f2add(q[c][v], kf[v]);
-            a2 = f2fma(ac1[c][v], z, f2fma(ac2[c][v], f2abs(z), a2));
+            acc2 = f2fma(ac1[c][v], z, f2fma(ac2[c][v], f2abs(z), acc2));
           }
         }
-        part[c] = a2.x + a2.y;
       }
-      head_sums<NC, CPH>(part, sc[k]);
+      head_sums2<NC, CPH>(a2, sc[k]);
 #pragma unroll
       for (int j = 0; j < HL; ++j) {
         if (GAT) sc[k][j] *= kLog2e;

@@ -107,15 +107,41 @@ struct Lay {
 // Offsets are kept 128-byte aligned: tensor copies land on such addresses.
 constexpr int align128(int x) { return (x + 127) / 128 * 128; }
 
-// Warps per block: the count (1..8) that fits the most warps in an SM's
-// shared memory (1 KB per block is reserved by the system); ties go to the
-// larger block.
+// Warps per block: the count (1, 2, 4 or 8) that fits the most warps in an
+// SM's shared memory (1 KB per block is reserved by the system); ties go to
+// the larger block.
+//
+// Registers bound residency too: each of an SM's four sub-partitions holds
+// 16,384 registers, allocated per warp in units of 256, so 16 resident warps
+// need at most 128 registers a thread and 12 warps at most 168 (13 to 16
+// warps need 4 per sub-partition, hence 128).  MINB asks the compiler for
+// enough blocks per SM that registers never hold residency below what shared
+// memory allows: 16 warps' worth when shared memory holds more than 12, 12
+// when it holds 12, else the shared-memory count (the register cap follows
+// from 65,536 / (MINB x block threads)).
 template <int WARP_BYTES>
 struct WarpsFor {
   static constexpr int fit(int w) { return (kSmemPerSm / (w * WARP_BYTES + 1024)) * w; }
-  static constexpr int best(int w, int bw) { return w > 8 ? bw : best(w + 1, fit(w) >= fit(bw) ? w : bw); }
+  static constexpr int best(int w, int bw) { return w > 8 ? bw : best(2 * w, fit(w) >= fit(bw) ? w : bw); }
   static constexpr int value = best(1, 1);
+  static constexpr int smem_warps = fit(value);
+  static constexpr int target = smem_warps > 12 ? 16 : (smem_warps == 12 ? 12 : smem_warps);
+  static constexpr int minb = target / value >= 1 ? target / value : 1;
 };
+
+// Blocks per SM a kernel asks the compiler for: the residency target above
+// for the dot score.  GATv2 kernels need more registers: the 128- and
+// 256-byte-row layouts with 8 KB stages take at most the 12-warp target
+// (168 registers a thread, which they fit without spilling, as ptxas
+// reports); the other GATv2 layouts spill under that cap and get none
+// (8 resident warps at up to 255 registers).
+template <int WARP_BYTES, int RB, int SB>
+constexpr int min_blocks(int kind) {
+  using W = WarpsFor<WARP_BYTES>;
+  if (kind != GATTN_SCORE_GATV2) return W::minb;
+  if (SB < 8192 || (RB != 128 && RB != 256)) return 1;
+  return W::target > 12 ? (12 / W::value > 0 ? 12 / W::value : 1) : W::minb;
+}
 
 // ---------------------------------------------------------------------------
 // async copies
@@ -278,20 +304,17 @@ struct LaneHeads {
   __device__ __forceinline__ static constexpr int of(int c) { return c / CPL; }
 };
 
-// Per-lane-head totals y[LaneHeads::N] of per-chunk partial sums x[NC]: the
-// chunks of a lane head are summed in-thread, and heads wider than a lane
-// reduce over CPH / NC lanes.  Every lane of the warp must call this (it may
-// shuffle).
+// Per-lane-head totals y[LaneHeads::N] of per-lane-head float2 partial sums
+// x2[LaneHeads::N] (the chunks of a lane head already accumulated into one
+// pair, in chunk order): heads wider than a lane reduce over CPH / NC lanes.
+// Every lane of the warp must call this (it may shuffle).  Every dot product
+// of one kind (dO . v and dO . O in particular) goes through the same
+// accumulation order, so equal inputs give bitwise equal sums.
 template <int NC, int CPH>
-__device__ __forceinline__ void head_sums(const float* x, float* y) {
+__device__ __forceinline__ void head_sums2(const float2* x2, float* y) {
   using LH = LaneHeads<NC, CPH>;
 #pragma unroll
-  for (int j = 0; j < LH::N; ++j) {
-    float s = x[j * LH::CPL];
-#pragma unroll
-    for (int c = 1; c < LH::CPL; ++c) s += x[j * LH::CPL + c];
-    y[j] = s;
-  }
+  for (int j = 0; j < LH::N; ++j) y[j] = x2[j].x + x2[j].y;
   if constexpr (CPH > NC) {
 #pragma unroll
     for (int o = 1; o < CPH / NC; o <<= 1) y[0] += __shfl_xor_sync(0xffffffffu, y[0], o);
@@ -516,6 +539,16 @@ struct Ring {
   // rows of 4-row set q4 of stage t's items / e4 of its edges
   __device__ __forceinline__ int4 qset(int t, int q4) {
     return reinterpret_cast<const int4*>(qix_at(t))[q4];
+  }
+  // Bit q4 set when item set q4 of stage t holds a starting item (a row other
+  // than `pad`); lane q4 tests set q4, the result is the same in every lane.
+  __device__ __forceinline__ uint32_t item_mask(int t, int pad, int lane) {
+    bool any = false;
+    if (lane < L::QR / 4) {
+      const int4 r = qset(t, lane);
+      any = r.x != pad || r.y != pad || r.z != pad || r.w != pad;
+    }
+    return __ballot_sync(0xffffffffu, any);
   }
   __device__ __forceinline__ int4 eset(int t, int e4) {
     return reinterpret_cast<const int4*>(ix_at(t))[e4];
