@@ -190,72 +190,53 @@ __global__ void __launch_bounds__(CsrShape<T, RB, SB>::THREADS, min_blocks<CsrSh
   constexpr int OQ = 0, ODO = Sh::IRS * RB, OO = 2 * Sh::IRS * RB;
   constexpr int OL = Sh::OL, OK = Sh::OK, OV = Sh::OV;
   // inline: slots of a starting item's Q / dO rows (last edge position) and O row
-  constexpr int NS = B / 4;
-  constexpr int K1 = Sh::RES > 0 ? (SE - 1) * G / 4 : NS;
-  constexpr int K2 = Sh::RES > 0 ? (SE - 2) * G / 4 : NS;
-  // The copies of a stage are spread over the lanes, one 4-row gather per
-  // job: jobs [0, NS) fill the K region's sets, [NS, 2 NS) the V region's
-  // (inline: item rows in the sets from K2 / K1 on of a starting stage),
-  // then, with a separate item region, 3 jobs per item set (Q, dO, O), then
-  // the lse sets; lane 0 first sets the byte count on the barrier.
-  constexpr int NJI = (Sh::RES == 0 && !L::IBULK) ? 3 * (L::QR / 4) : 0;
+  constexpr int K1 = (SE - 1) * G / 4, K2 = (SE - 2) * G / 4;
   auto issue = [&](int s) {
     const int4* dsc = ring.desc_at(s);
-    if (dsc[0].x != -3) {
+    if (lane == 0 && dsc[0].x != -3) {
       uint8_t* st = ring.stage_at(s);
       uint64_t* bar = ring.bar_at(s);
-      const uint32_t qmask = ring.item_mask(s, p.N, lane);
-      // inline: a stage that starts a bundle gathers edge rows only below K2
-      const int ne = (Sh::RES > 0 && qmask) ? K2 : NS;
-      const uint32_t ibytes = L::IBULK ? item_rows<L>(ring.qset(s, 0), p.N) * 3 * RB
-                                       : __popc(qmask) * 3 * L::SET_BYTES;
-      if (lane == 0)
-        mbar_expect_tx(bar, ibytes + (p.rows16 ? __popc(qmask) * 16 * p.H : 0) +
-                                2 * ne * L::SET_BYTES);
-      __syncwarp();
-      const int njobs = 2 * NS + NJI + (p.rows16 ? L::QR / 4 : 0);
-      for (int jb = lane; jb < njobs; jb += 32) {
-        if (jb < 2 * NS) {
-          const bool vr = jb >= NS;
-          const int b4 = vr ? jb - NS : jb;
-          uint8_t* reg = st + (vr ? OV : OK);
-          if (b4 < ne) {
-            const int4 r = ring.eset(s, b4);
-            fence_proxy_async();
-            L::gather(reg, 4 * b4, vr ? &p.me1 : &p.me0, r.x, r.y, r.z, r.w, bar);
-          } else if (b4 >= K1 && ((qmask >> (b4 - K1)) & 1)) {  // inline Q / dO rows
-            const int4 r = ring.qset(s, b4 - K1);
-            fence_proxy_async();
-            L::gather(reg, 4 * b4, vr ? &p.mi1 : &p.mi0, r.x, r.y, r.z, r.w, bar);
-          } else if (!vr && b4 >= K2 && b4 < K1 && ((qmask >> (b4 - K2)) & 1)) {  // inline O rows
-            const int4 r = ring.qset(s, b4 - K2);
-            fence_proxy_async();
-            L::gather(reg, 4 * b4, &p.mi2, r.x, r.y, r.z, r.w, bar);
-          }
-        } else if (jb < 2 * NS + NJI) {  // separate item region: Q, dO, O sets
-          const int q4 = (jb - 2 * NS) / 3, w = (jb - 2 * NS) % 3;
-          if ((qmask >> q4) & 1) {
-            const int4 r = ring.qset(s, q4);
-            fence_proxy_async();
-            L::gather(st + (w == 0 ? OQ : (w == 1 ? ODO : OO)), 4 * q4,
-                      w == 0 ? &p.mi0 : (w == 1 ? &p.mi1 : &p.mi2), r.x, r.y, r.z, r.w, bar);
-          }
-        } else {  // lse rows of the starting items
-          const int q4 = jb - 2 * NS - NJI;
-          if ((qmask >> q4) & 1) {
-            const int4 r = ring.qset(s, q4);
-            fence_proxy_async();
-            tma_gather4(st + OL + q4 * L::SSB, &p.ms0, 0, r.x, r.y, r.z, r.w, bar);
-          }
-        }
+      int4 qr[L::QR / 4];
+      uint32_t qmask = 0;
+#pragma unroll
+      for (int q4 = 0; q4 < L::QR / 4; ++q4) {
+        qr[q4] = ring.qset(s, q4);
+        const bool any = qr[q4].x != p.N || qr[q4].y != p.N || qr[q4].z != p.N ||
+                         qr[q4].w != p.N;
+        qmask |= uint32_t(any) << q4;
       }
-      if constexpr (Sh::RES == 0 && L::IBULK) {
-        if (lane == 0 && qmask) {
-          const int4 r = ring.qset(s, 0);
-          fence_proxy_async();
-          fetch_item_rows<L>(st + OQ, p.Q, r, p.N, bar);
-          fetch_item_rows<L>(st + ODO, p.dO, r, p.N, bar);
-          fetch_item_rows<L>(st + OO, p.O, r, p.N, bar);
+      const uint32_t ibytes = L::IBULK ? item_rows<L>(qr[0], p.N) * 3 * RB
+                                       : __popc(qmask) * 3 * L::SET_BYTES;
+      // inline: a stage that starts a bundle gathers edge rows only below K2
+      const int ne = (Sh::RES > 0 && qmask) ? K2 : B / 4;
+      fence_proxy_async();
+      mbar_expect_tx(bar, ibytes + (p.rows16 ? __popc(qmask) * 16 * p.H : 0) +
+                              2 * ne * L::SET_BYTES);
+#pragma unroll
+      for (int q4 = 0; q4 < L::QR / 4; ++q4)
+        if ((qmask >> q4) & 1) {
+          const int4 r = qr[q4];
+          if constexpr (Sh::RES > 0) {
+            L::gather(st + OK, 4 * (K1 + q4), &p.mi0, r.x, r.y, r.z, r.w, bar);
+            L::gather(st + OV, 4 * (K1 + q4), &p.mi1, r.x, r.y, r.z, r.w, bar);
+            L::gather(st + OK, 4 * (K2 + q4), &p.mi2, r.x, r.y, r.z, r.w, bar);
+          } else if constexpr (L::IBULK) {
+            fetch_item_rows<L>(st + OQ, p.Q, r, p.N, bar);
+            fetch_item_rows<L>(st + ODO, p.dO, r, p.N, bar);
+            fetch_item_rows<L>(st + OO, p.O, r, p.N, bar);
+          } else {
+            L::gather(st + OQ, 4 * q4, &p.mi0, r.x, r.y, r.z, r.w, bar);
+            L::gather(st + ODO, 4 * q4, &p.mi1, r.x, r.y, r.z, r.w, bar);
+            L::gather(st + OO, 4 * q4, &p.mi2, r.x, r.y, r.z, r.w, bar);
+          }
+          if (p.rows16) tma_gather4(st + OL + q4 * L::SSB, &p.ms0, 0, r.x, r.y, r.z, r.w, bar);
+        }
+#pragma unroll
+      for (int b4 = 0; b4 < B / 4; ++b4) {
+        if (b4 < ne) {
+          const int4 r = ring.eset(s, b4);
+          L::gather(st + OK, 4 * b4, &p.me0, r.x, r.y, r.z, r.w, bar);
+          L::gather(st + OV, 4 * b4, &p.me1, r.x, r.y, r.z, r.w, bar);
         }
       }
     }
@@ -358,10 +339,8 @@ __global__ void __launch_bounds__(CsrShape<T, RB, SB>::THREADS, min_blocks<CsrSh
 
     const uint8_t* ks = st + OK;
     const uint8_t* vs = st + OV;
-    const int kmax = __reduce_max_sync(FULL, cnt);
 #pragma unroll
     for (int k = 0; k < SE; ++k) {
-      if (k >= kmax) break;
       const bool valid = k < cnt;
       // slots past this group's count are read as they are (zero-filled pad
       // rows or rows of an earlier stage): nothing below uses their results
@@ -585,56 +564,48 @@ __global__ void __launch_bounds__(CscShape<T, RB, SB, DB>::THREADS, min_blocks<C
   constexpr int SROW = Sh::SROW;
   constexpr int PB = SROW < 16 ? SROW : 16;   // bytes of one statistic piece
   constexpr int PPR = SROW / PB;             // pieces per row
-  constexpr int NS = B / 4;
-  constexpr int K1 = Sh::RES > 0 ? (SE - 1) * G / 4 : NS;  // inline: first set of the last position
-  // The copies of a stage are spread over the lanes, one 4-row gather per
-  // job: jobs [0, NS) fill the Q region's sets, [NS, 2 NS) the dO region's
-  // (inline: a starting stage's K / V item rows in the sets from K1 on),
-  // then, with a separate item region, 2 jobs per item set (K, V); lane 0
-  // first sets the byte count on the barrier.
-  constexpr int NJI = (Sh::RES == 0 && !L::IBULK) ? 2 * (L::QR / 4) : 0;
+  constexpr int K1 = (SE - 1) * G / 4;       // inline: first set of the last edge position
   auto issue = [&](int s) {
     const int4* dsc = ring.desc_at(s);
     const bool live = dsc[0].x != -3;
-    if (live) {
+    if (lane == 0 && live) {
       uint8_t* st = ring.stage_at(s);
       uint64_t* bar = ring.bar_at(s);
-      const uint32_t qmask = ring.item_mask(s, p.N, lane);
-      const uint32_t ibytes = L::IBULK ? item_rows<L>(ring.qset(s, 0), p.N) * 2 * RB
+      int4 qr[L::QR / 4];
+      uint32_t qmask = 0;
+#pragma unroll
+      for (int q4 = 0; q4 < L::QR / 4; ++q4) {
+        qr[q4] = ring.qset(s, q4);
+        const bool any = qr[q4].x != p.N || qr[q4].y != p.N || qr[q4].z != p.N ||
+                         qr[q4].w != p.N;
+        qmask |= uint32_t(any) << q4;
+      }
+      const uint32_t ibytes = L::IBULK ? item_rows<L>(qr[0], p.N) * 2 * RB
                                        : __popc(qmask) * 2 * L::SET_BYTES;
-      const int ne = (Sh::RES > 0 && qmask) ? K1 : NS;  // sets of edge rows
-      if (lane == 0) mbar_expect_tx(bar, ibytes + 2 * ne * L::SET_BYTES);
-      __syncwarp();
-      for (int jb = lane; jb < 2 * NS + NJI; jb += 32) {
-        if (jb < 2 * NS) {
-          const bool gr = jb >= NS;
-          const int b4 = gr ? jb - NS : jb;
-          uint8_t* reg = st + (gr ? OGE : OQE);
-          if (b4 < ne) {
-            const int4 r = ring.eset(s, b4);
-            fence_proxy_async();
-            L::gather(reg, 4 * b4, gr ? &p.me1 : &p.me0, r.x, r.y, r.z, r.w, bar);
-          } else if ((qmask >> (b4 - K1)) & 1) {  // inline K / V rows
-            const int4 r = ring.qset(s, b4 - K1);
-            fence_proxy_async();
-            L::gather(reg, 4 * b4, gr ? &p.mi1 : &p.mi0, r.x, r.y, r.z, r.w, bar);
-          }
-        } else {  // separate item region: K, V sets
-          const int q4 = (jb - 2 * NS) / 2, w = (jb - 2 * NS) % 2;
-          if ((qmask >> q4) & 1) {
-            const int4 r = ring.qset(s, q4);
-            fence_proxy_async();
-            L::gather(st + (w == 0 ? OKI : OVI), 4 * q4, w == 0 ? &p.mi0 : &p.mi1, r.x, r.y, r.z,
-                      r.w, bar);
+      const int ne = (Sh::RES > 0 && qmask) ? K1 : B / 4;  // sets of edge rows
+      fence_proxy_async();
+      mbar_expect_tx(bar, ibytes + 2 * ne * L::SET_BYTES);
+#pragma unroll
+      for (int q4 = 0; q4 < L::QR / 4; ++q4)
+        if ((qmask >> q4) & 1) {
+          const int4 r = qr[q4];
+          if constexpr (Sh::RES > 0) {
+            L::gather(st + OQE, 4 * (K1 + q4), &p.mi0, r.x, r.y, r.z, r.w, bar);
+            L::gather(st + OGE, 4 * (K1 + q4), &p.mi1, r.x, r.y, r.z, r.w, bar);
+          } else if constexpr (L::IBULK) {
+            fetch_item_rows<L>(st + OKI, p.K, r, p.N, bar);
+            fetch_item_rows<L>(st + OVI, p.V, r, p.N, bar);
+          } else {
+            L::gather(st + OKI, 4 * q4, &p.mi0, r.x, r.y, r.z, r.w, bar);
+            L::gather(st + OVI, 4 * q4, &p.mi1, r.x, r.y, r.z, r.w, bar);
           }
         }
-      }
-      if constexpr (Sh::RES == 0 && L::IBULK) {
-        if (lane == 0 && qmask) {
-          const int4 r = ring.qset(s, 0);
-          fence_proxy_async();
-          fetch_item_rows<L>(st + OKI, p.K, r, p.N, bar);
-          fetch_item_rows<L>(st + OVI, p.V, r, p.N, bar);
+#pragma unroll
+      for (int b4 = 0; b4 < B / 4; ++b4) {
+        if (b4 < ne) {
+          const int4 r = ring.eset(s, b4);
+          L::gather(st + OQE, 4 * b4, &p.me0, r.x, r.y, r.z, r.w, bar);
+          L::gather(st + OGE, 4 * b4, &p.me1, r.x, r.y, r.z, r.w, bar);
         }
       }
     }
@@ -709,10 +680,8 @@ __global__ void __launch_bounds__(CscShape<T, RB, SB, DB>::THREADS, min_blocks<C
     const uint8_t* qs = st + OQE;
     const uint8_t* gs = st + OGE;
 
-    const int kmax = __reduce_max_sync(FULL, cnt);
 #pragma unroll
     for (int e = 0; e < SE; ++e) {
-      if (e >= kmax) break;
       const bool valid = e < cnt;
       // slots past this group's count are read as they are (zero-filled pad
       // rows or rows of an earlier stage): nothing below uses their results

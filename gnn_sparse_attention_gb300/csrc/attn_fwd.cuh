@@ -124,49 +124,62 @@ __global__ void __launch_bounds__(FwdShape<T, RB, SB>::THREADS, min_blocks<FwdSh
   // the zero-filled pad row N.  With inline item rows, a stage that starts a
   // bundle gathers the Q rows into the K slots of the last edge position and
   // skips that position's V slots.  Bytes are counted on the slot's barrier.
+    // rows of stage s into its ring slot by TMA gathers issued from lane 0:
+  // Q rows of the items that start here (only the 4-row sets that hold one),
+  // then the K rows and the V rows of the stage's edges; unused slots gather
+  // the zero-filled pad row N.  With inline item rows, a stage that starts a
+  // bundle gathers the Q rows into the K slots of the last edge position and
+  // skips that position's V slots.  Bytes are counted on the slot's barrier.
   constexpr int OKR = Sh::IRS * RB, OVR = (Sh::IRS + B) * RB;  // K, V row regions
-  // The copies of a stage are spread over the lanes, one 4-row gather each:
-  // lanes [0, NS) the K-row sets, [NS, 2 NS) the V-row sets, [2 NS, 2 NS +
-  // QR / 4) the Q-row sets of a separate item region; lane 0 first sets the
-  // byte count on the barrier.
-  constexpr int NS = B / 4;
-  constexpr int KS = Sh::RES > 0 ? (SE - 1) * G / 4 : NS;  // inline: first set of the last position
   auto issue = [&](int s) {
-    const int4* dsc = ring.desc_at(s);
-    if (dsc[0].x != -3) {
-      uint8_t* st = ring.stage_at(s);
-      uint64_t* bar = ring.bar_at(s);
-      const uint32_t qmask = ring.item_mask(s, p.N, lane);
-      const int ne = (Sh::RES > 0 && qmask) ? KS : NS;  // sets of edge rows in this stage
-      uint32_t bytes = (2 * ne + __popc(qmask)) * L::SET_BYTES;
-      if constexpr (Sh::RES == 0 && L::IBULK)
-        bytes = 2 * NS * L::SET_BYTES + item_rows<L>(ring.qset(s, 0), p.N) * RB;
-      if (lane == 0) mbar_expect_tx(bar, bytes);
-      __syncwarp();
-      if (lane < 2 * NS) {
-        const bool vr = lane >= NS;
-        const int b4 = vr ? lane - NS : lane;
-        if (b4 < ne) {
-          const int4 r = ring.eset(s, b4);
-          fence_proxy_async();
-          L::gather(st + (vr ? OVR : OKR), 4 * b4, vr ? &p.mv : &p.mk, r.x, r.y, r.z, r.w, bar);
-        } else if (!vr && ((qmask >> (b4 - KS)) & 1)) {  // inline Q rows
-          const int4 r = ring.qset(s, b4 - KS);
-          fence_proxy_async();
-          L::gather(st + OKR, 4 * b4, &p.mq, r.x, r.y, r.z, r.w, bar);
+    if (lane == 0) {
+      const int4* dsc = ring.desc_at(s);
+      if (dsc[0].x != -3) {
+        uint8_t* st = ring.stage_at(s);
+        uint64_t* bar = ring.bar_at(s);
+        int4 qr[L::QR / 4];
+        uint32_t qmask = 0;
+#pragma unroll
+        for (int q4 = 0; q4 < L::QR / 4; ++q4) {
+          qr[q4] = ring.qset(s, q4);
+          const bool any = qr[q4].x != p.N || qr[q4].y != p.N || qr[q4].z != p.N ||
+                           qr[q4].w != p.N;
+          qmask |= uint32_t(any) << q4;
         }
-      } else if (Sh::RES == 0 && !L::IBULK && lane < 2 * NS + L::QR / 4) {
-        const int q4 = lane - 2 * NS;
-        if ((qmask >> q4) & 1) {
-          const int4 r = ring.qset(s, q4);
-          fence_proxy_async();
-          L::gather(st, 4 * q4, &p.mq, r.x, r.y, r.z, r.w, bar);
-        }
-      }
-      if constexpr (Sh::RES == 0 && L::IBULK) {
-        if (lane == 0) {
-          fence_proxy_async();
-          fetch_item_rows<L>(st, p.Q, ring.qset(s, 0), p.N, bar);
+        fence_proxy_async();
+        if constexpr (Sh::RES > 0) {
+          constexpr int KS = (SE - 1) * G / 4;  // first 4-row set of the last edge position
+          const int ne = qmask ? KS : B / 4;    // sets of edge rows in this stage
+          mbar_expect_tx(bar, (2 * ne + __popc(qmask)) * L::SET_BYTES);
+#pragma unroll
+          for (int b4 = 0; b4 < B / 4; ++b4) {
+            if (b4 < ne) {
+              const int4 r = ring.eset(s, b4);
+              L::gather(st + OKR, 4 * b4, &p.mk, r.x, r.y, r.z, r.w, bar);
+              L::gather(st + OVR, 4 * b4, &p.mv, r.x, r.y, r.z, r.w, bar);
+            } else if ((qmask >> (b4 - KS)) & 1) {
+              const int4 r = qr[b4 - KS];
+              L::gather(st + OKR, 4 * b4, &p.mq, r.x, r.y, r.z, r.w, bar);
+            }
+          }
+        } else {
+          const uint32_t ibytes = L::IBULK ? item_rows<L>(qr[0], p.N) * RB
+                                           : __popc(qmask) * L::SET_BYTES;
+          mbar_expect_tx(bar, ibytes + 2 * (B / 4) * L::SET_BYTES);
+          if constexpr (L::IBULK) {
+            fetch_item_rows<L>(st, p.Q, qr[0], p.N, bar);
+          } else {
+#pragma unroll
+            for (int q4 = 0; q4 < L::QR / 4; ++q4)
+              if ((qmask >> q4) & 1)
+                L::gather(st, 4 * q4, &p.mq, qr[q4].x, qr[q4].y, qr[q4].z, qr[q4].w, bar);
+          }
+#pragma unroll
+          for (int b4 = 0; b4 < B / 4; ++b4) {
+            const int4 r = ring.eset(s, b4);
+            L::gather(st + OKR, 4 * b4, &p.mk, r.x, r.y, r.z, r.w, bar);
+            L::gather(st + OVR, 4 * b4, &p.mv, r.x, r.y, r.z, r.w, bar);
+          }
         }
       }
     }
@@ -222,11 +235,9 @@ __global__ void __launch_bounds__(FwdShape<T, RB, SB>::THREADS, min_blocks<FwdSh
 
     const uint8_t* ks = st + OKR;
     const uint8_t* vs = st + OVR;
-    const int kmax = __reduce_max_sync(FULL, cnt);  // edges of the warp's longest item here
     float sc[SE][HL];
 #pragma unroll
     for (int k = 0; k < SE; ++k) {
-      if (k >= kmax) break;
       // slots past this group's count hold zero-filled pad rows or rows of an
       // earlier stage: their scores are discarded below, so they are read as is
       float2 a2[HL];

@@ -125,7 +125,7 @@ struct WarpsFor {
   static constexpr int best(int w, int bw) { return w > 8 ? bw : best(2 * w, fit(w) >= fit(bw) ? w : bw); }
   static constexpr int value = best(1, 1);
   static constexpr int smem_warps = fit(value);
-  static constexpr int target = smem_warps > 12 ? 16 : (smem_warps == 12 ? 12 : smem_warps);
+  static constexpr int target = smem_warps >= 16 ? 16 : (smem_warps >= 12 ? 12 : smem_warps);
   static constexpr int minb = target / value >= 1 ? target / value : 1;
 };
 
@@ -540,16 +540,7 @@ struct Ring {
   __device__ __forceinline__ int4 qset(int t, int q4) {
     return reinterpret_cast<const int4*>(qix_at(t))[q4];
   }
-  // Bit q4 set when item set q4 of stage t holds a starting item (a row other
-  // than `pad`); lane q4 tests set q4, the result is the same in every lane.
-  __device__ __forceinline__ uint32_t item_mask(int t, int pad, int lane) {
-    bool any = false;
-    if (lane < L::QR / 4) {
-      const int4 r = qset(t, lane);
-      any = r.x != pad || r.y != pad || r.z != pad || r.w != pad;
-    }
-    return __ballot_sync(0xffffffffu, any);
-  }
+
   __device__ __forceinline__ int4 eset(int t, int e4) {
     return reinterpret_cast<const int4*>(ix_at(t))[e4];
   }

@@ -36,9 +36,9 @@
 // them in fp32, as in FlashAttention.
 //
 // Schedule: one CTA per SM walks its row blocks (grid stride), the heads
-// and the tiles; with two operand slots (D = 64) the next step's loads are
-// in flight while the current one computes; step descriptors from the plan
-// are loaded two steps ahead.  Every mbarrier wait is bounded; a wait that
+// and the tiles; with three operand slots (D = 64) the loads of the next two
+// steps are in flight while the current one computes (one slot for D = 128);
+// step descriptors from the plan are loaded two steps ahead.  Every mbarrier wait is bounded; a wait that
 // gives up is reported through the plan's error word, the block drains what
 // it issued (again bounded), frees its TMEM and returns.
 #include <cuda.h>
@@ -66,10 +66,10 @@ struct FwdSmem {
   static constexpr int V = 2 * KB * kTB;
   static constexpr int MASK = 3 * KB * kTB;
   static constexpr int SLOT = MASK + kMaskB;
-  static constexpr int P = NS * SLOT;               // [2][128 rows][128 B]
+  static constexpr int P = NS * SLOT;               // P tile: [2][128 rows][128 B]
   static constexpr int RED = P + 2 * kTB;           // [4 chunks][128 rows] fp32 maxima / sums
-  static constexpr int BAR = RED + 4 * kT * 4;
-  static constexpr int END = BAR + 64;
+  static constexpr int BAR = RED + 4 * kT * 4;       // NS + 3 barriers, then the TMEM address
+  static constexpr int END = BAR + 8 * (NS + 3) + 8;
   static constexpr int BYTES = END + 1024;          // slack to align the base to 1024
   static_assert(SLOT % 1024 == 0 && P % 1024 == 0, "swizzled tiles start on 1024-byte boundaries");
   static_assert(BYTES <= 227 * 1024, "shared memory of one CTA");
@@ -92,11 +92,11 @@ __global__ void __launch_bounds__(kThr, 1) tile_fwd_kernel(const __grid_constant
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* sP = smem + SM::P;
   float* sRed = reinterpret_cast<float*>(smem + SM::RED);
-  uint64_t* barL = reinterpret_cast<uint64_t*>(smem + SM::BAR);  // [2] operand slots
-  uint64_t* barS = barL + 2;
-  uint64_t* barO = barL + 3;
-  uint64_t* barR = barL + 4;  // residual out tile of the epilogue
-  uint32_t* sTmem = reinterpret_cast<uint32_t*>(barL + 5);
+  uint64_t* barL = reinterpret_cast<uint64_t*>(smem + SM::BAR);  // [NS] operand slots
+  uint64_t* barS = barL + NS;
+  uint64_t* barO = barL + NS + 1;
+  uint64_t* barR = barL + NS + 2;  // residual out tile of the epilogue
+  uint32_t* sTmem = reinterpret_cast<uint32_t*>(barL + NS + 3);
 
   const int tid = threadIdx.x, warp = tid >> 5;
   const int r = (warp & 3) * 32 + (tid & 31);  // row of the block = TMEM lane
@@ -152,10 +152,16 @@ __global__ void __launch_bounds__(kThr, 1) tile_fwd_kernel(const __grid_constant
     if (nx.g >= 0) dn = p.desc[nx.q];
     if (tid == 0) issue(cur, dc, 0);
     pendL = 1u;
+    if constexpr (NS == 3) {  // three slots: loads run two steps ahead
+      if (nx.g >= 0) {
+        if (tid == 0) issue(nx, dn, 1);
+        pendL |= 2u;
+      }
+    }
   }
   float m = neg_inf(), l = 0.f;  // the row's running maximum (base 2) and this chunk's share of its sum
   for (int k = 0; cur.g >= 0; ++k) {
-    const int s = NS == 2 ? (k & 1) : 0;
+    const int s = k % NS;
     const bool more = nx.g >= 0;
     const TileStep n2 = more ? tile_step_after(p, nx, dn) : TileStep{-1, 0, 0, 0, -1};
     const int4 d2 = n2.g >= 0 ? p.desc[n2.q] : make_int4(0, 0, 0, 0);  // used next step
@@ -170,6 +176,16 @@ __global__ void __launch_bounds__(kThr, 1) tile_fwd_kernel(const __grid_constant
           issue(nx, dn, s ^ 1);
         }
         pendL |= 1u << (s ^ 1);
+      }
+    } else if constexpr (NS == 3) {
+      if (n2.g >= 0) {
+        // slot (k + 2) % 3 held the previous step, released the same way
+        const int s2 = (k + 2) % 3;
+        if (tid == 0) {
+          bulk_wait_read();
+          issue(n2, d2, s2);
+        }
+        pendL |= 1u << s2;
       }
     }
     const int node = dc.x * kT + r;
@@ -392,7 +408,7 @@ gattn_status launch_tile_fwd(const TileParams& p, int D, int num_sms, cudaStream
     }
     return GATTN_OK;
   };
-  if (D == 64) return go(tile_fwd_kernel<64, 2>, FwdSmem<64, 2>::BYTES);
+  if (D == 64) return go(tile_fwd_kernel<64, 3>, FwdSmem<64, 3>::BYTES);
   return go(tile_fwd_kernel<128, 1>, FwdSmem<128, 1>::BYTES);
 }
 
