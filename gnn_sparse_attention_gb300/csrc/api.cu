@@ -136,38 +136,40 @@ gattn_status launched(const char* what) {
 }  // namespace
 
 // switch key of a (row bytes, stage bytes) pair
+#define GATTN_STAGE_KEY(RB_, SB_) ((RB_) * 16 + ((SB_) == kStageSmall ? 1 : 2))
 #define GATTN_ROW_CASE(PASS_NAME, PT, TNAME, RB_, SB_) \
-  case RB_ * 16 + SB_ / 4096:                          \
+  case GATTN_STAGE_KEY(RB_, SB_):                      \
     return launch_##PASS_NAME##_##TNAME##_##RB_##_##SB_(db, kind, p, num_sms, st, g);
 
 gattn_status launch_fwd(gattn_dtype dt, int rb, int db, int kind, int sb, const FwdParams& p,
                         int num_sms, cudaStream_t st, int* g) {
   if (dt == GATTN_F32) {
-    switch (rb * 16 + sb / 4096) { GATTN_FOR_ROWS(GATTN_ROW_CASE, fwd, FwdParams, f32) }
+    switch (GATTN_STAGE_KEY(rb, sb)) { GATTN_FOR_ROWS(GATTN_ROW_CASE, fwd, FwdParams, f32) }
   } else {
-    switch (rb * 16 + sb / 4096) { GATTN_FOR_ROWS(GATTN_ROW_CASE, fwd, FwdParams, bf16) }
+    switch (GATTN_STAGE_KEY(rb, sb)) { GATTN_FOR_ROWS(GATTN_ROW_CASE, fwd, FwdParams, bf16) }
   }
   return GATTN_ERR_UNSUPPORTED;
 }
 gattn_status launch_bwd_csr(gattn_dtype dt, int rb, int db, int kind, int sb, const BwdParams& p,
                             int num_sms, cudaStream_t st, int* g) {
   if (dt == GATTN_F32) {
-    switch (rb * 16 + sb / 4096) { GATTN_FOR_ROWS(GATTN_ROW_CASE, csr, BwdParams, f32) }
+    switch (GATTN_STAGE_KEY(rb, sb)) { GATTN_FOR_ROWS(GATTN_ROW_CASE, csr, BwdParams, f32) }
   } else {
-    switch (rb * 16 + sb / 4096) { GATTN_FOR_ROWS(GATTN_ROW_CASE, csr, BwdParams, bf16) }
+    switch (GATTN_STAGE_KEY(rb, sb)) { GATTN_FOR_ROWS(GATTN_ROW_CASE, csr, BwdParams, bf16) }
   }
   return GATTN_ERR_UNSUPPORTED;
 }
 gattn_status launch_bwd_csc(gattn_dtype dt, int rb, int db, int kind, int sb, const BwdParams& p,
                             int num_sms, cudaStream_t st, int* g) {
   if (dt == GATTN_F32) {
-    switch (rb * 16 + sb / 4096) { GATTN_FOR_ROWS(GATTN_ROW_CASE, csc, BwdParams, f32) }
+    switch (GATTN_STAGE_KEY(rb, sb)) { GATTN_FOR_ROWS(GATTN_ROW_CASE, csc, BwdParams, f32) }
   } else {
-    switch (rb * 16 + sb / 4096) { GATTN_FOR_ROWS(GATTN_ROW_CASE, csc, BwdParams, bf16) }
+    switch (GATTN_STAGE_KEY(rb, sb)) { GATTN_FOR_ROWS(GATTN_ROW_CASE, csc, BwdParams, bf16) }
   }
   return GATTN_ERR_UNSUPPORTED;
 }
 #undef GATTN_ROW_CASE
+#undef GATTN_STAGE_KEY
 
 }  // namespace gattn
 

@@ -371,12 +371,16 @@ __global__ void __launch_bounds__(CsrShape<T, RB, SB>::THREADS, min_blocks<CsrSh
       }
       head_sums2<NC, CPH>(s2, sc);
       head_sums2<NC, CPH>(p2, dp);
-      if (act && valid) {
+      // dot score branch-free: ds is 0 for a slot past the group's count (a
+      // select, so whatever such a slot's rows hold never reaches the sums);
+      // GATv2 keeps the branch (its longer body spills without it)
+      if (!GAT || (act && valid)) {
+        const bool use = act && valid;
         float ds[HL];
 #pragma unroll
         for (int j = 0; j < HL; ++j) {
           const float pr = ex2((GAT ? sc[j] * kLog2e : sc[j]) - lse2[j]);
-          ds[j] = pr * (dp[j] - dlt[j]);
+          ds[j] = use ? pr * (dp[j] - dlt[j]) : 0.f;
         }
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
@@ -710,7 +714,11 @@ __global__ void __launch_bounds__(CscShape<T, RB, SB, DB>::THREADS, min_blocks<C
       }
       head_sums2<NC, CPH>(s2, sc);
       head_sums2<NC, CPH>(p2, dp);
-      if (act && valid) {
+      // dot score branch-free: p and ds are 0 for a slot past the group's
+      // count (a select, so whatever such a slot's rows hold never reaches
+      // the sums); GATv2 keeps the branch
+      if (!GAT || (act && valid)) {
+        const bool use = act && valid;
         const float* srow = reinterpret_cast<const float*>(st + OLS + Cur::slot(g, e) * SROW);
         float pr[HL], ds[HL];
 #pragma unroll
@@ -718,8 +726,9 @@ __global__ void __launch_bounds__(CscShape<T, RB, SB, DB>::THREADS, min_blocks<C
           const int hh = head[j * LH::CPL];
           const float ls2 = srow[hh];
           const float dl = srow[Sh::H + hh];
-          pr[j] = ex2((GAT ? sc[j] * kLog2e : sc[j]) - ls2);
-          ds[j] = pr[j] * (dp[j] - dl);
+          const float pe = ex2((GAT ? sc[j] * kLog2e : sc[j]) - ls2);
+          pr[j] = use ? pe : 0.f;
+          ds[j] = use ? pe * (dp[j] - dl) : 0.f;
         }
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
