@@ -150,16 +150,22 @@ __global__ void __launch_bounds__(FwdShape<T, RB, SB>::THREADS, min_blocks<FwdSh
         if constexpr (Sh::RES > 0) {
           constexpr int KS = (SE - 1) * G / 4;  // first 4-row set of the last edge position
           const int ne = qmask ? KS : B / 4;    // sets of edge rows in this stage
-          mbar_expect_tx(bar, (2 * ne + __popc(qmask)) * L::SET_BYTES);
+          // a starting stage: Q rows into the K slots of the last position,
+          // zero-filled pad rows into its V slots (every V slot then holds a
+          // real row or zeros, which the value sum below relies on)
+          mbar_expect_tx(bar, (B / 4 + ne + __popc(qmask)) * L::SET_BYTES);
 #pragma unroll
           for (int b4 = 0; b4 < B / 4; ++b4) {
             if (b4 < ne) {
               const int4 r = ring.eset(s, b4);
               L::gather(st + OKR, 4 * b4, &p.mk, r.x, r.y, r.z, r.w, bar);
               L::gather(st + OVR, 4 * b4, &p.mv, r.x, r.y, r.z, r.w, bar);
-            } else if ((qmask >> (b4 - KS)) & 1) {
-              const int4 r = qr[b4 - KS];
-              L::gather(st + OKR, 4 * b4, &p.mq, r.x, r.y, r.z, r.w, bar);
+            } else {
+              if ((qmask >> (b4 - KS)) & 1) {
+                const int4 r = qr[b4 - KS];
+                L::gather(st + OKR, 4 * b4, &p.mq, r.x, r.y, r.z, r.w, bar);
+              }
+              L::gather(st + OVR, 4 * b4, &p.mv, p.N, p.N, p.N, p.N, bar);
             }
           }
         } else {
@@ -273,8 +279,7 @@ __global__ void __launch_bounds__(FwdShape<T, RB, SB>::THREADS, min_blocks<FwdSh
       for (int j = 0; j < HL; ++j) {
         float mx = m[j];
 #pragma unroll
-        for (int k = 0; k < SE; ++k)
-          if (k < cnt) mx = fmaxf(mx, sc[k][j]);
+        for (int k = 0; k < SE; ++k) mx = fmaxf(mx, sc[k][j]);  // -inf past the count
         base[j] = mx == neg_inf() ? 0.f : mx;
         corr[j] = ex2(m[j] - base[j]);
         l[j] *= corr[j];
@@ -284,9 +289,12 @@ __global__ void __launch_bounds__(FwdShape<T, RB, SB>::THREADS, min_blocks<FwdSh
       for (int c = 0; c < NC; ++c)
 #pragma unroll
         for (int v = 0; v < PP; ++v) acc[c][v] = f2mul(acc[c][v], f2s(corr[LH::of(c)]));
+      // branch-free for the dot score: past the count the score is -inf, so
+      // the weight is 0, and the V slot holds a zero-filled pad row (or a
+      // real row): the sum takes 0 there.  GATv2 keeps the branch.
 #pragma unroll
       for (int k = 0; k < SE; ++k) {
-        if (k < cnt) {
+        if (!GAT || k < cnt) {
           float pk[HL];
 #pragma unroll
           for (int j = 0; j < HL; ++j) {
