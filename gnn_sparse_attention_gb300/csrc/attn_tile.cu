@@ -36,9 +36,10 @@
 // them in fp32, as in FlashAttention.
 //
 // Schedule: one CTA per SM walks its row blocks (grid stride), the heads
-// and the tiles; with three operand slots (D = 64) the loads of the next two
-// steps are in flight while the current one computes (one slot for D = 128);
-// step descriptors from the plan are loaded two steps ahead.  Every mbarrier wait is bounded; a wait that
+// and the tiles; with two operand slots (D = 64; the kernel also takes three)
+// the next step's loads are in flight while the current one computes (one
+// slot for D = 128); step descriptors from the plan are loaded two steps
+// ahead.  Every mbarrier wait is bounded; a wait that
 // gives up is reported through the plan's error word, the block drains what
 // it issued (again bounded), frees its TMEM and returns.
 #include <cuda.h>
@@ -408,7 +409,9 @@ gattn_status launch_tile_fwd(const TileParams& p, int D, int num_sms, cudaStream
     }
     return GATTN_OK;
   };
-  if (D == 64) return go(tile_fwd_kernel<64, 3>, FwdSmem<64, 3>::BYTES);
+  // D = 64: two operand slots (three, with the loads of two steps in flight,
+  // measured no faster on the block-model graphs and take 50 KB more)
+  if (D == 64) return go(tile_fwd_kernel<64, 2>, FwdSmem<64, 2>::BYTES);
   return go(tile_fwd_kernel<128, 1>, FwdSmem<128, 1>::BYTES);
 }
 

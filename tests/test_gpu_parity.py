@@ -44,6 +44,24 @@ def test_small_heavy_split(dtype, H, D, kind):
 
 
 @pytest.mark.parametrize("kind", ["dot", "gatv2"])
+@pytest.mark.parametrize("dtype,H,D", SHAPES)
+def test_long_items_every_row_size(dtype, H, D, kind):
+    """Work items of ~40-64 edges (threshold/chunk 64): every pass takes its
+    long-item stages, with the starting items' rows inline where a stage holds
+    whole 4-row sets, for every row size; a hub destination and a hub source
+    add chunks and merge trees."""
+    indptr, indices = hp.graph_with_source_hub(7, 600, 40.0, isolated=0.03, hub_deg=500,
+                                               frac=0.5)
+    case = hp.GpuCase(indptr, indices, H, D, dtype, kind, seed=13, T=64, C=64)
+    try:
+        e = np.diff(indptr)
+        assert e.sum() / max(1, len(e)) > 16           # mean item above the short-item bar
+        hp.compare(case.run(), hp.full_oracle(case), hp.TOL[dtype])
+    finally:
+        case.close()
+
+
+@pytest.mark.parametrize("kind", ["dot", "gatv2"])
 @pytest.mark.parametrize("dtype,H,D", [("f32", 2, 16), ("bf16", 8, 16), ("bf16", 4, 32),
                                        ("bf16", 8, 64)])
 def test_default_plan(dtype, H, D, kind):
